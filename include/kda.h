@@ -1,0 +1,189 @@
+/*
+ * kda.h - C ABI of the GB300 (sm_103a) Kimi Delta Attention library (libkda.so).
+ *
+ * Operations
+ *   kda_chunk_fwd             chunkwise KDA forward over one batch of sequences
+ *   kda_chunk_workspace_size  scratch bytes kda_chunk_fwd needs for given arguments
+ *   kda_decode_step           fused T=1 decode step on a packed q|k|v row with a slot pool
+ *   kda_version               library version string
+ *
+ * What is computed (per sequence n and head h; math state S is [dk, dv], stored
+ * transposed as [dv, dk] with dk contiguous):
+ *   S~  = diag(e^{g_t}) S                        decay on the key index
+ *   u_t = beta_t (v_t - S~^T k_t)                delta rule (u_t = v_t with KDA_FLAG_DELTA_OFF)
+ *   S   = S~ + k_t u_t^T
+ *   o_t = scale S^T q_t
+ * ("TileLang 实战：KDA 从零到一" §1 gives this recurrence in the transposed
+ * (d_v, d_k) form; "FlashKDA里的L矩阵和Mqk矩阵" §背景 gives the same token
+ * recurrence in delta form.) kda_chunk_fwd evaluates it in 16-token chunks
+ * through the per-chunk L matrix, the Mqk matrix, the exact Neumann inverse of
+ * (I + L) and a serial cross-chunk state recurrence (the same page, sections
+ * L矩阵的构造, Mqk矩阵的构造, 为什么CHUNK=16, K2 内核如何消费).
+ *
+ * Conventions shared by every call
+ *   - All tensor pointers are caller-owned DEVICE memory, contiguous row-major,
+ *     16-byte aligned. The library never allocates, frees or synchronises.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default).
+ *   - Argument errors are detected on the host before any launch and return
+ *     KDA_ERR_INVALID_ARG or KDA_ERR_UNSUPPORTED; nothing is launched then.
+ *   - A failed launch returns KDA_ERR_CUDA.
+ *   - Problems only visible on the device (a bad cu_seqlens array, an
+ *     out-of-range slot index, a bounded wait that ran out) are written as a
+ *     kda_status code into the optional device word `err` (if non-NULL); the
+ *     affected work is skipped. `err` is never cleared by the library.
+ *   - Not thread-safe per stream in any special way: calls on one stream run
+ *     in order; concurrent calls on different streams must not share outputs
+ *     or workspace.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ABI-identical to cudaStream_t; declared here so this header needs no CUDA headers. */
+typedef struct CUstream_st* kda_stream_t;
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, bad index array */
+  KDA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (e.g. dk = 96) */
+  KDA_ERR_CUDA = 3,         /* a CUDA launch or runtime call failed */
+  KDA_ERR_TIMEOUT = 4       /* a bounded device-side wait expired (reported through err) */
+} kda_status;
+
+typedef enum {
+  KDA_DTYPE_BF16 = 0,  /* q, k, v, beta/b and o in bfloat16; tensor-core path */
+  KDA_DTYPE_FP32 = 1   /* q, k, v, beta/b and o in float32; CUDA-core fp32 path */
+} kda_dtype;
+
+typedef enum {
+  KDA_GATE_NONE = 0,    /* g = 0 (no decay) */
+  KDA_GATE_G = 1,       /* log-decay g given: fp32 [B, T, H, dk] */
+  KDA_GATE_INPUTS = 2   /* g = -exp(A_log[h]) * softplus(a + dt_bias) computed in the kernel */
+} kda_gate_mode;
+
+typedef enum {
+  KDA_BETA_VALUES = 0,  /* beta given: [B, T, H] in the input dtype */
+  KDA_BETA_LOGITS = 1   /* logits b given: beta = sigmoid(b), [B, T, H] in the input dtype */
+} kda_beta_mode;
+
+/* flags */
+#define KDA_FLAG_L2NORM_QK 0x1u  /* q <- q / sqrt(sum q^2 + 1e-6), same for k, in the kernel */
+#define KDA_FLAG_DELTA_OFF 0x2u  /* u_t = v_t: plain (gated) linear attention, beta ignored */
+
+/*
+ * Arguments of kda_chunk_fwd.
+ *
+ * Shapes (row-major, contiguous):
+ *   q, k      [B, T, H, dk]        dtype
+ *   v, o      [B, T, H, dv]        dtype
+ *   g         [B, T, H, dk]        fp32   (KDA_GATE_G)
+ *   a         [B, T, H*dk]         fp32   (KDA_GATE_INPUTS)
+ *   A_log     [H]                  fp32   (KDA_GATE_INPUTS)
+ *   dt_bias   [H*dk]               fp32   (KDA_GATE_INPUTS)
+ *   beta      [B, T, H]            dtype  (values or logits, per beta_mode)
+ *   h0, hT    [N, H, dv, dk]       fp32   (either may be NULL: zero initial state /
+ *                                          no final state)
+ *   cu_seqlens [N + 1]             int32  device array, or NULL
+ * Without cu_seqlens the batch holds N = B independent sequences of length T.
+ * With cu_seqlens, B must be 1 and the N sequences are packed along T:
+ * sequence n spans tokens [cu_seqlens[n], cu_seqlens[n+1]). cu_seqlens must
+ * start at 0, never decrease and end at T; this is checked on the device and a
+ * violation writes KDA_ERR_INVALID_ARG to err and skips the call's work.
+ * Chunks of 16 tokens restart at every sequence start.
+ * Supported: dtype BF16 with dk = dv in {64, 128}; dtype FP32 with dk, dv in {64, 128}.
+ * Numerics of the BF16 path: S stays fp32 on chip; the contractions run on
+ * tensor cores with fp32 accumulation, S rounded to bf16 as an operand, and
+ * (with the delta rule on) the corrected values U in fp16, which assumes
+ * |U| < 65504 (values are saturated, never turned into inf).
+ */
+typedef struct kda_chunk_args {
+  int32_t dtype;       /* kda_dtype */
+  int32_t B, T, H, dk, dv;
+  int32_t N;           /* number of sequences (B without cu_seqlens) */
+  int32_t gate_mode;   /* kda_gate_mode */
+  int32_t beta_mode;   /* kda_beta_mode; ignored with KDA_FLAG_DELTA_OFF */
+  uint32_t flags;      /* KDA_FLAG_* */
+  float scale;         /* output scale, typically dk^-0.5 */
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* a;
+  const float* A_log;
+  const float* dt_bias;
+  const void* beta;
+  const float* h0;
+  const int32_t* cu_seqlens;
+  void* o;
+  float* hT;
+  int32_t* err;        /* optional device status word */
+} kda_chunk_args;
+
+/*
+ * Bytes of device scratch memory kda_chunk_fwd needs for these arguments
+ * (0 when the arguments are invalid). The workspace is caller-owned; its
+ * contents on entry do not matter and are garbage on exit.
+ */
+size_t kda_chunk_workspace_size(const kda_chunk_args* args);
+
+/*
+ * Chunkwise KDA forward. Writes o (and hT when non-NULL). `workspace` is device
+ * memory of at least kda_chunk_workspace_size(args) bytes, 256-byte aligned.
+ * Returns KDA_OK once the work is enqueued.
+ */
+kda_status kda_chunk_fwd(const kda_chunk_args* args, void* workspace, size_t workspace_bytes,
+                         kda_stream_t stream);
+
+/*
+ * Arguments of kda_decode_step (sglang PR #26586, fused_recurrent_kda_packed_decode:
+ * one token per batch row, read from a packed [q | k | v] row).
+ *
+ *   packed_qkv [B, 2*H*K + HV*V]   bf16  row = [q (H*K) | k (H*K) | v (HV*V)]
+ *   a          [B, HV*K]           bf16  gate input
+ *   b          [B, HV]             bf16  beta logits (beta = sigmoid(b))
+ *   A_log      [HV]                fp32
+ *   dt_bias    [HV*K]              fp32
+ *   state_pool [num_slots, HV, V, K] fp32, updated IN PLACE for the valid rows
+ *   indices    [B]                 int32 slot of each row; negative = padding row
+ *   o          [B, HV, V]          bf16
+ * Value head hv uses query/key head hv / (HV / H); HV must be a multiple of H.
+ * g = -exp(A_log[hv]) * softplus(a + dt_bias); with KDA_FLAG_L2NORM_QK q and k
+ * are L2-normalised (eps 1e-6 inside the root); q is multiplied by scale.
+ * A padding row writes o = 0 and touches no state. Valid indices must be
+ * distinct (rows sharing a slot race). An index >= num_slots writes
+ * KDA_ERR_INVALID_ARG to err, zeroes that row's o and touches no state.
+ * Supported: K, V in {64, 128}.
+ */
+typedef struct kda_decode_args {
+  int32_t B, H, HV, K, V;
+  int32_t num_slots;
+  uint32_t flags;      /* KDA_FLAG_L2NORM_QK */
+  float scale;
+  const void* packed_qkv;
+  const void* a;
+  const void* b;
+  const float* A_log;
+  const float* dt_bias;
+  float* state_pool;
+  const int32_t* indices;
+  void* o;
+  int32_t* err;        /* optional device status word */
+} kda_decode_args;
+
+/* Fused T=1 decode step. Returns KDA_OK once the work is enqueued. */
+kda_status kda_decode_step(const kda_decode_args* args, kda_stream_t stream);
+
+/* Version string of the library, e.g. "kda-gb300 0.1.0 sm_103a". */
+const char* kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

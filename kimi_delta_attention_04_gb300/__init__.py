@@ -1,0 +1,21 @@
+"""GB300-native Kimi Delta Attention: chunkwise forward and fused T=1 decode.
+
+The computation lives in libkda.so (hand-written sm_103a CUDA behind the C ABI
+of include/kda.h); this package is its thin Python binding. Importing the
+package does not load the library; the first call does, and raises if the
+library has not been built (python -m kimi_delta_attention_04_gb300.build).
+"""
+
+from ._lib import (  # noqa: F401
+    KdaError,
+    chunk_workspace_size,
+    kda_chunk_fwd,
+    kda_decode_step,
+    lib_path,
+    load,
+    make_chunk_args,
+    make_decode_args,
+    version,
+)
+
+__version__ = "0.1.0"

@@ -1,0 +1,223 @@
+"""ctypes binding of libkda.so (include/kda.h).
+
+Argument marshalling only: every step of the computation runs in the library's
+CUDA kernels. PyTorch supplies device memory, the current stream and the output
+allocations. There is no CPU or PyTorch fallback: if libkda.so is missing or a
+tensor is not on a CUDA device, the call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import threading
+from pathlib import Path
+
+import torch
+
+_LIB_PATH = Path(__file__).resolve().parent / "libkda.so"
+_lock = threading.Lock()
+_lib = None
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_CUDA = 3
+KDA_ERR_TIMEOUT = 4
+STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
+                4: "KDA_ERR_TIMEOUT"}
+
+KDA_DTYPE_BF16 = 0
+KDA_DTYPE_FP32 = 1
+KDA_GATE_NONE, KDA_GATE_G, KDA_GATE_INPUTS = 0, 1, 2
+KDA_BETA_VALUES, KDA_BETA_LOGITS = 0, 1
+KDA_FLAG_L2NORM_QK = 0x1
+KDA_FLAG_DELTA_OFF = 0x2
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class ChunkArgs(ctypes.Structure):
+    _fields_ = [
+        ("dtype", ctypes.c_int32), ("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32),
+        ("dk", ctypes.c_int32), ("dv", ctypes.c_int32), ("N", ctypes.c_int32),
+        ("gate_mode", ctypes.c_int32), ("beta_mode", ctypes.c_int32), ("flags", ctypes.c_uint32),
+        ("scale", ctypes.c_float),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("g", ctypes.c_void_p),
+        ("a", ctypes.c_void_p), ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("beta", ctypes.c_void_p), ("h0", ctypes.c_void_p), ("cu_seqlens", ctypes.c_void_p),
+        ("o", ctypes.c_void_p), ("hT", ctypes.c_void_p), ("err", ctypes.c_void_p),
+    ]
+
+
+class DecodeArgs(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("HV", ctypes.c_int32), ("K", ctypes.c_int32),
+        ("V", ctypes.c_int32), ("num_slots", ctypes.c_int32), ("flags", ctypes.c_uint32),
+        ("scale", ctypes.c_float),
+        ("packed_qkv", ctypes.c_void_p), ("a", ctypes.c_void_p), ("b", ctypes.c_void_p),
+        ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p), ("state_pool", ctypes.c_void_p),
+        ("indices", ctypes.c_void_p), ("o", ctypes.c_void_p), ("err", ctypes.c_void_p),
+    ]
+
+
+EXPORTS = ("kda_chunk_fwd", "kda_chunk_workspace_size", "kda_decode_step", "kda_version")
+
+
+def lib_path() -> Path:
+    return _LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load libkda.so (once). Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not _LIB_PATH.exists():
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build the CUDA library first "
+                "(python -m kimi_delta_attention_04_gb300.build). There is no fallback path.")
+        lib = ctypes.CDLL(str(_LIB_PATH))
+        lib.kda_chunk_fwd.restype = ctypes.c_int
+        lib.kda_chunk_fwd.argtypes = [ctypes.POINTER(ChunkArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        lib.kda_chunk_workspace_size.restype = ctypes.c_size_t
+        lib.kda_chunk_workspace_size.argtypes = [ctypes.POINTER(ChunkArgs)]
+        lib.kda_decode_step.restype = ctypes.c_int
+        lib.kda_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
+        lib.kda_version.restype = ctypes.c_char_p
+        lib.kda_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def version() -> str:
+    return load().kda_version().decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"expected a torch.Tensor, got {type(t).__name__}")
+    if not t.is_cuda:
+        raise ValueError("libkda works on CUDA tensors only (no CPU fallback)")
+    if not t.is_contiguous():
+        raise ValueError("libkda needs contiguous tensors")
+    return t.data_ptr()
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return KDA_DTYPE_BF16
+    if dt == torch.float32:
+        return KDA_DTYPE_FP32
+    raise ValueError(f"unsupported input dtype {dt}; use torch.bfloat16 or torch.float32")
+
+
+def make_chunk_args(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None, beta=None, b=None,
+                    h0=None, cu_seqlens=None, l2norm_qk=False, delta=True, o=None, hT=None, err=None):
+    """Fill the C argument struct from tensors (no allocation, no launch)."""
+    B, T, H, dk = q.shape
+    dv = v.shape[-1]
+    if cu_seqlens is not None:
+        N = cu_seqlens.numel() - 1
+    else:
+        N = B
+    if g is not None:
+        gate_mode = KDA_GATE_G
+    elif a is not None:
+        gate_mode = KDA_GATE_INPUTS
+    else:
+        gate_mode = KDA_GATE_NONE
+    if beta is not None:
+        beta_mode, beta_t = KDA_BETA_VALUES, beta
+    else:
+        beta_mode, beta_t = KDA_BETA_LOGITS, b
+    flags = (KDA_FLAG_L2NORM_QK if l2norm_qk else 0) | (0 if delta else KDA_FLAG_DELTA_OFF)
+    args = ChunkArgs()
+    args.dtype = _dtype_code(q.dtype)
+    args.B, args.T, args.H, args.dk, args.dv, args.N = B, T, H, dk, dv, N
+    args.gate_mode, args.beta_mode, args.flags = gate_mode, beta_mode, flags
+    args.scale = float(scale)
+    args.q, args.k, args.v = _ptr(q), _ptr(k), _ptr(v)
+    args.g, args.a, args.A_log, args.dt_bias = _ptr(g), _ptr(a), _ptr(A_log), _ptr(dt_bias)
+    args.beta = _ptr(beta_t)
+    args.h0, args.cu_seqlens = _ptr(h0), _ptr(cu_seqlens)
+    args.o, args.hT, args.err = _ptr(o), _ptr(hT), _ptr(err)
+    return args
+
+
+def chunk_workspace_size(args: ChunkArgs) -> int:
+    return int(load().kda_chunk_workspace_size(ctypes.byref(args)))
+
+
+def kda_chunk_fwd(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None, beta=None, b=None,
+                  h0=None, cu_seqlens=None, l2norm_qk=False, delta=True, o=None, hT=None,
+                  output_final_state=True, workspace=None, err=None, stream=None):
+    """Chunkwise KDA forward through libkda (see include/kda.h for the contract).
+
+    q, k [B, T, H, dk]; v [B, T, H, dv] (bf16 or fp32, same dtype). The gate is
+    g (fp32 [B, T, H, dk]) or gate inputs a (fp32 [B, T, H*dk]) + dt_bias
+    (fp32 [H*dk]) + A_log (fp32 [H]), or neither (g = 0). beta [B, T, H] is given
+    as values (beta=) or logits (b=). h0 / returned hT are fp32 [N, H, dv, dk].
+    Returns (o, hT) with hT None when output_final_state is False.
+    """
+    lib = load()
+    B, T, H, _ = q.shape
+    if o is None:
+        o = torch.empty(B, T, H, v.shape[-1], dtype=q.dtype, device=q.device)
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else B
+    if hT is None and output_final_state:
+        hT = torch.empty(N, H, v.shape[-1], q.shape[-1], dtype=torch.float32, device=q.device)
+    args = make_chunk_args(q, k, v, scale=scale, g=g, a=a, dt_bias=dt_bias, A_log=A_log, beta=beta, b=b,
+                           h0=h0, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk, delta=delta, o=o, hT=hT,
+                           err=err)
+    need = int(lib.kda_chunk_workspace_size(ctypes.byref(args)))
+    if need == 0:
+        st = lib.kda_chunk_fwd(ctypes.byref(args), None, 0, _stream_ptr(stream))
+        raise KdaError(st if st != KDA_OK else KDA_ERR_INVALID_ARG, "kda_chunk_fwd")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = lib.kda_chunk_fwd(ctypes.byref(args), ctypes.c_void_p(_ptr(workspace)), need, _stream_ptr(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_fwd")
+    return o, hT
+
+
+def make_decode_args(packed_qkv, a, b, A_log, dt_bias, state_pool, indices, *, H, HV, K, V, scale,
+                     l2norm_qk=True, o=None, err=None):
+    args = DecodeArgs()
+    args.B = packed_qkv.shape[0]
+    args.H, args.HV, args.K, args.V = H, HV, K, V
+    args.num_slots = state_pool.shape[0]
+    args.flags = KDA_FLAG_L2NORM_QK if l2norm_qk else 0
+    args.scale = float(scale)
+    args.packed_qkv, args.a, args.b = _ptr(packed_qkv), _ptr(a), _ptr(b)
+    args.A_log, args.dt_bias = _ptr(A_log), _ptr(dt_bias)
+    args.state_pool, args.indices = _ptr(state_pool), _ptr(indices)
+    args.o, args.err = _ptr(o), _ptr(err)
+    return args
+
+
+def kda_decode_step(packed_qkv, a, b, A_log, dt_bias, state_pool, indices, *, H, HV, K, V, scale,
+                    l2norm_qk=True, o=None, err=None, stream=None):
+    """Fused T=1 decode through libkda; state_pool is updated in place. Returns o [B, HV, V] bf16."""
+    lib = load()
+    if o is None:
+        o = torch.empty(packed_qkv.shape[0], HV, V, dtype=torch.bfloat16, device=packed_qkv.device)
+    args = make_decode_args(packed_qkv, a, b, A_log, dt_bias, state_pool, indices, H=H, HV=HV, K=K, V=V,
+                            scale=scale, l2norm_qk=l2norm_qk, o=o, err=err)
+    st = lib.kda_decode_step(ctypes.byref(args), _stream_ptr(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_step")
+    return o

@@ -1,0 +1,167 @@
+// Host side of the C ABI declared in include/kda.h: argument validation,
+// workspace layout and kernel dispatch. No allocation, no synchronisation.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+#include "kda_internal.h"
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool chunk_dims_supported(const kda_chunk_args& a) {
+  if (a.dtype == KDA_DTYPE_BF16) return a.dk == a.dv && (a.dk == 64 || a.dk == 128);
+  if (a.dtype == KDA_DTYPE_FP32) return (a.dk == 64 || a.dk == 128) && (a.dv == 64 || a.dv == 128);
+  return false;
+}
+
+// Returns KDA_OK and fills geometry when the arguments are well formed.
+kda_status check_chunk(const kda_chunk_args* a, kda::ChunkGeom* geo, size_t* rec_bytes) {
+  if (a == nullptr) return KDA_ERR_INVALID_ARG;
+  if (a->dtype != KDA_DTYPE_BF16 && a->dtype != KDA_DTYPE_FP32) return KDA_ERR_INVALID_ARG;
+  if (a->B < 1 || a->T < 0 || a->H < 1 || a->dk < 1 || a->dv < 1 || a->N < 1) return KDA_ERR_INVALID_ARG;
+  if (a->flags & ~(KDA_FLAG_L2NORM_QK | KDA_FLAG_DELTA_OFF)) return KDA_ERR_INVALID_ARG;
+  if (a->gate_mode < KDA_GATE_NONE || a->gate_mode > KDA_GATE_INPUTS) return KDA_ERR_INVALID_ARG;
+  const bool delta = !(a->flags & KDA_FLAG_DELTA_OFF);
+  if (delta && a->beta_mode != KDA_BETA_VALUES && a->beta_mode != KDA_BETA_LOGITS) return KDA_ERR_INVALID_ARG;
+  if (a->cu_seqlens == nullptr) {
+    if (a->N != a->B) return KDA_ERR_INVALID_ARG;
+  } else {
+    if (a->B != 1) return KDA_ERR_INVALID_ARG;
+    if (!aligned(a->cu_seqlens, 4)) return KDA_ERR_INVALID_ARG;
+  }
+  const int64_t tokens = static_cast<int64_t>(a->B) * a->T;
+  if (tokens * a->H * (a->dk > a->dv ? a->dk : a->dv) > INT64_C(1) << 40) return KDA_ERR_INVALID_ARG;
+  if (tokens > INT32_MAX / 2) return KDA_ERR_INVALID_ARG;
+  if (!chunk_dims_supported(*a)) return KDA_ERR_UNSUPPORTED;
+  if (tokens > 0) {
+    if (!a->q || !a->k || !a->v || !a->o) return KDA_ERR_INVALID_ARG;
+    if (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->o, 16)) return KDA_ERR_INVALID_ARG;
+    if (a->gate_mode == KDA_GATE_G && (!a->g || !aligned(a->g, 16))) return KDA_ERR_INVALID_ARG;
+    if (a->gate_mode == KDA_GATE_INPUTS) {
+      if (!a->a || !a->A_log || !a->dt_bias) return KDA_ERR_INVALID_ARG;
+      if (!aligned(a->a, 16) || !aligned(a->A_log, 4) || !aligned(a->dt_bias, 4)) return KDA_ERR_INVALID_ARG;
+    }
+    if (delta) {
+      const size_t el = a->dtype == KDA_DTYPE_BF16 ? 2 : 4;
+      if (!a->beta || !aligned(a->beta, el)) return KDA_ERR_INVALID_ARG;
+    }
+  }
+  if (a->h0 && !aligned(a->h0, 16)) return KDA_ERR_INVALID_ARG;
+  if (a->hT && !aligned(a->hT, 16)) return KDA_ERR_INVALID_ARG;
+  if (a->err && !aligned(a->err, 4)) return KDA_ERR_INVALID_ARG;
+
+  geo->N = a->N;
+  geo->T = a->T;
+  geo->H = a->H;
+  geo->cu_seqlens = a->cu_seqlens;
+  geo->chunk_off = nullptr;
+  geo->chunks_per_seq = (a->T + 15) / 16;
+  if (a->cu_seqlens == nullptr) {
+    geo->max_chunks = a->B * geo->chunks_per_seq;
+  } else {
+    geo->max_chunks = geo->chunks_per_seq + a->N;  // each sequence adds at most one partial chunk
+  }
+  *rec_bytes = a->dtype == KDA_DTYPE_BF16 ? kda::record_bytes_tc(a->dk) : kda::record_bytes_f32(a->dk, a->dv);
+  if (*rec_bytes == 0) return KDA_ERR_UNSUPPORTED;
+  return KDA_OK;
+}
+
+size_t workspace_bytes(const kda::ChunkGeom& geo, size_t rec_bytes) {
+  return kda::plan_header_bytes(geo.N) + static_cast<size_t>(geo.max_chunks) * geo.H * rec_bytes;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_chunk_workspace_size(const kda_chunk_args* args) {
+  kda::ChunkGeom geo;
+  size_t rec = 0;
+  if (check_chunk(args, &geo, &rec) != KDA_OK) return 0;
+  return workspace_bytes(geo, rec);
+}
+
+kda_status kda_chunk_fwd(const kda_chunk_args* args, void* workspace, size_t ws_bytes, kda_stream_t stream) {
+  kda::ChunkGeom geo;
+  size_t rec = 0;
+  kda_status st = check_chunk(args, &geo, &rec);
+  if (st != KDA_OK) return st;
+  const size_t need = workspace_bytes(geo, rec);
+  if (workspace == nullptr || ws_bytes < need || !aligned(workspace, 256)) return KDA_ERR_INVALID_ARG;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  kda::ChunkCall c;
+  c.geo = geo;
+  c.geo.chunk_off = static_cast<int32_t*>(workspace);
+  c.dk = args->dk;
+  c.dv = args->dv;
+  c.gate_mode = args->gate_mode;
+  c.beta_mode = args->beta_mode;
+  c.l2norm = (args->flags & KDA_FLAG_L2NORM_QK) != 0;
+  c.delta = (args->flags & KDA_FLAG_DELTA_OFF) == 0;
+  c.scale = args->scale;
+  c.q = args->q;
+  c.k = args->k;
+  c.v = args->v;
+  c.g = args->g;
+  c.a = args->a;
+  c.A_log = args->A_log;
+  c.dt_bias = args->dt_bias;
+  c.beta = args->beta;
+  c.h0 = args->h0;
+  c.o = args->o;
+  c.hT = args->hT;
+  c.err = args->err;
+  c.records = static_cast<unsigned char*>(workspace) + kda::plan_header_bytes(geo.N);
+
+  cudaError_t e = cudaSuccess;
+  if (geo.cu_seqlens != nullptr) e = kda::launch_plan(c, s);
+  if (e == cudaSuccess) {
+    e = args->dtype == KDA_DTYPE_BF16 ? kda::launch_chunk_tc(c, s) : kda::launch_chunk_f32(c, s);
+  }
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_decode_step(const kda_decode_args* a, kda_stream_t stream) {
+  if (a == nullptr) return KDA_ERR_INVALID_ARG;
+  if (a->B < 0 || a->H < 1 || a->HV < 1 || a->K < 1 || a->V < 1 || a->num_slots < 0) return KDA_ERR_INVALID_ARG;
+  if (a->HV % a->H != 0) return KDA_ERR_INVALID_ARG;
+  if (a->flags & ~KDA_FLAG_L2NORM_QK) return KDA_ERR_INVALID_ARG;
+  if (!((a->K == 64 || a->K == 128) && (a->V == 64 || a->V == 128))) return KDA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(a->B) * a->HV > INT32_MAX) return KDA_ERR_INVALID_ARG;
+  if (a->B > 0) {
+    if (!a->packed_qkv || !a->a || !a->b || !a->A_log || !a->dt_bias || !a->indices || !a->o)
+      return KDA_ERR_INVALID_ARG;
+    if (!aligned(a->packed_qkv, 16) || !aligned(a->a, 16) || !aligned(a->b, 2) || !aligned(a->A_log, 4) ||
+        !aligned(a->dt_bias, 16) || !aligned(a->indices, 4) || !aligned(a->o, 16))
+      return KDA_ERR_INVALID_ARG;
+    if (a->num_slots > 0 && (!a->state_pool || !aligned(a->state_pool, 16))) return KDA_ERR_INVALID_ARG;
+  }
+  if (a->err && !aligned(a->err, 4)) return KDA_ERR_INVALID_ARG;
+  kda::DecodeCall c;
+  c.B = a->B;
+  c.H = a->H;
+  c.HV = a->HV;
+  c.K = a->K;
+  c.V = a->V;
+  c.num_slots = a->num_slots;
+  c.l2norm = (a->flags & KDA_FLAG_L2NORM_QK) != 0;
+  c.scale = a->scale;
+  c.packed_qkv = a->packed_qkv;
+  c.a = a->a;
+  c.b = a->b;
+  c.A_log = a->A_log;
+  c.dt_bias = a->dt_bias;
+  c.state_pool = a->state_pool;
+  c.indices = a->indices;
+  c.o = a->o;
+  c.err = a->err;
+  const cudaError_t e = kda::launch_decode(c, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+const char* kda_version(void) { return "kda-gb300 0.1.0 sm_103a"; }
+
+}  // extern "C"

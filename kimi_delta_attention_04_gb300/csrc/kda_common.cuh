@@ -1,0 +1,210 @@
+// Device helpers shared by the KDA kernels: warp-level tensor-core MMA
+// (mma.sync m16n8k16, fp32 accumulation), ldmatrix, cp.async, packing and
+// warp reductions. sm_103a only.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda_internal.h"
+
+namespace kda {
+
+// ---------------------------------------------------------------------------
+// Element types of MMA operands
+// ---------------------------------------------------------------------------
+struct Bf16 {
+  using T = __nv_bfloat16;
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  static __device__ __forceinline__ T cvt(float x) { return __float2bfloat16_rn(x); }
+  static __device__ __forceinline__ float to_float(T x) { return __bfloat162float(x); }
+};
+
+struct F16 {
+  using T = __half;
+  // Saturating conversion: values beyond the fp16 range become +-65504, never inf.
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+  }
+  static __device__ __forceinline__ T cvt(float x) {
+    uint32_t r = pack(x, 0.f);
+    return *reinterpret_cast<__half*>(&r);
+  }
+  static __device__ __forceinline__ float to_float(T x) { return __half2float(x); }
+};
+
+// D = A * B + D for one m16n8k16 tile; A 16x16 (row), B 16x8 (col), fp32 accumulators.
+template <typename Op>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1);
+
+template <>
+__device__ __forceinline__ void mma16816<Bf16>(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <>
+__device__ __forceinline__ void mma16816<F16>(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Four 8x8 b16 matrices; lane l supplies the row address of matrix l/8, row l%8.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t (&r)[2], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(smem_u32(p)));
+}
+
+// 16-byte asynchronous global -> shared copy (L2-only caching).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// Sum of 16 per-lane values over the warp. On return the total of value j sits
+// in lanes 2j and 2j+1, i.e. lane l holds the total of value (l >> 1) & 15.
+// 16 shuffles for 16 reductions (each round halves the values a lane keeps).
+__device__ __forceinline__ float warp_transpose_reduce16(float (&v)[16], int lane) {
+  float w8[8], w4[4], w2[2];
+  {
+    const bool up = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float send = up ? v[i] : v[i + 8];
+      float keep = up ? v[i + 8] : v[i];
+      w8[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+  }
+  {
+    const bool up = lane & 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float send = up ? w8[i] : w8[i + 4];
+      float keep = up ? w8[i + 4] : w8[i];
+      w4[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+  }
+  {
+    const bool up = lane & 4;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      float send = up ? w4[i] : w4[i + 2];
+      float keep = up ? w4[i + 2] : w4[i];
+      w2[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+  }
+  float w1;
+  {
+    const bool up = lane & 2;
+    float send = up ? w2[0] : w2[1];
+    float keep = up ? w2[1] : w2[0];
+    w1 = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+  }
+  return w1 + __shfl_xor_sync(0xffffffffu, w1, 1);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// softplus with the usual linear branch above 20 (the two differ by < 2.1e-9 there).
+__device__ __forceinline__ float softplus_f(float x) { return x <= 20.f ? log1pf(expf(x)) : x; }
+
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+
+__device__ __forceinline__ void set_err(int32_t* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+// ---------------------------------------------------------------------------
+// Chunk bookkeeping shared by the chunk kernels
+// ---------------------------------------------------------------------------
+constexpr int kChunk = 16;
+
+// Position of one chunk: sequence n, chunk c within it, first global token and
+// number of real tokens (1..16).
+struct ChunkPos {
+  int n, c, tok0, ntok;
+};
+
+// Maps a global chunk index to its sequence. Returns false past the last chunk
+// or when the varlen plan was rejected.
+__device__ __forceinline__ bool locate_chunk(const ChunkGeom& geo, int cg, ChunkPos& pos) {
+  if (geo.cu_seqlens == nullptr) {
+    const int n = cg / geo.chunks_per_seq;
+    if (n >= geo.N) return false;
+    const int c = cg - n * geo.chunks_per_seq;
+    pos.n = n;
+    pos.c = c;
+    pos.tok0 = n * geo.T + c * kChunk;
+    pos.ntok = min(kChunk, geo.T - c * kChunk);
+    return pos.ntok > 0;
+  }
+  const int32_t* off = geo.chunk_off;
+  if (off[geo.N + 1] != 1) return false;  // plan flag: cu_seqlens rejected
+  if (cg >= off[geo.N]) return false;
+  int lo = 0, hi = geo.N - 1;  // largest n with off[n] <= cg
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= cg) lo = mid; else hi = mid - 1;
+  }
+  pos.n = lo;
+  pos.c = cg - off[lo];
+  const int s = geo.cu_seqlens[lo], e = geo.cu_seqlens[lo + 1];
+  pos.tok0 = s + pos.c * kChunk;
+  pos.ntok = min(kChunk, e - pos.tok0);
+  return pos.ntok > 0;
+}
+
+// Sequence bounds and first global chunk of sequence n. Returns false when the
+// varlen plan was rejected.
+__device__ __forceinline__ bool locate_seq(const ChunkGeom& geo, int n, int& tok_start, int& tok_end,
+                                           int& chunk_base) {
+  if (geo.cu_seqlens == nullptr) {
+    tok_start = n * geo.T;
+    tok_end = tok_start + geo.T;
+    chunk_base = n * geo.chunks_per_seq;
+    return true;
+  }
+  if (geo.chunk_off[geo.N + 1] != 1) return false;
+  tok_start = geo.cu_seqlens[n];
+  tok_end = geo.cu_seqlens[n + 1];
+  chunk_base = geo.chunk_off[n];
+  return true;
+}
+
+}  // namespace kda

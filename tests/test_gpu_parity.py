@@ -1,0 +1,255 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle, element
+by element, on seeded synthetic inputs.
+
+Tolerances (from the acceptance criteria of the method): fp32 inputs max abs
+<= 1e-4; bf16 inputs relative Frobenius <= 5e-3 and max abs <= 2e-2 for o and
+hT, against the oracle on the same bf16-rounded inputs. Padded decode rows are
+bit-exact (zero output, untouched state)."""
+
+import numpy as np
+import pytest
+import torch
+
+import kimi_delta_attention_04_gb300 as kda
+from kimi_delta_attention_04_gb300 import workloads as W
+from oracle import kda_oracle as ko
+
+from kda_cases import (assert_close, gpu_chunk, np64, oracle_chunk, subset_heads, subset_sequence)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from kimi_delta_attention_04_gb300 import build
+    build.build()
+    kda.load()
+
+
+def _check_chunk(wl, name, h0=True):
+    o, hT = gpu_chunk(wl, h0=h0)
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle_chunk(wl, h0=h0)
+    assert_close(f"{name} o", np64(o), o_ref, wl["dtype"])
+    assert_close(f"{name} hT", np64(hT), h_ref, wl["dtype"])
+    return o, hT
+
+
+# --------------------------------------------------------------------------
+# Chunk forward
+# --------------------------------------------------------------------------
+
+def test_fp32_small_gate_inputs():
+    """fp32, B=1, H=2, T=128, d=64, gate inputs, beta logits, L2 norm, zero h0."""
+    _check_chunk(W.fp32_small(), "fp32_small")
+
+
+def test_fp32_small_gate_g_and_values():
+    wl = W.fp32_small(seed=10)
+    # the same run with the gate passed as g (from the oracle's gate) and beta as values
+    T, H, K = wl["T"], wl["H"], wl["K"]
+    g = ko.kda_gate(np64(wl["a"]).reshape(1, T, H, K), np64(wl["dt_bias"]).reshape(H, K), np64(wl["A_log"]))
+    wl2 = dict(wl)
+    wl2["g"] = torch.from_numpy(g).float()
+    wl2["a"] = wl2["dt_bias"] = wl2["A_log"] = None
+    wl2["beta"] = torch.sigmoid(wl["b"].double()).float()
+    wl2["b"] = None
+    _check_chunk(wl2, "fp32_small_g")
+
+
+@pytest.mark.parametrize("T", [1, 15, 16, 17, 100])
+def test_fp32_ragged_lengths(T):
+    wl = W.chunk_workload(seed=20 + T, B=2, T=T, H=2, K=64, V=128, dtype=torch.float32, h0_std=0.1)
+    _check_chunk(wl, f"fp32_T{T}")
+
+
+def test_linear_attention_full():
+    """Plain causal linear attention (g = 0, delta off), bf16, B=2, H=4, T=1024, d=128."""
+    _check_chunk(W.linear_attn(), "linear_attn")
+
+
+@pytest.mark.parametrize("T", [1, 16, 37, 200])
+def test_bf16_kda_small(T):
+    wl = W.prefill(T=T, H=3, seed=30 + T)
+    _check_chunk(wl, f"prefill_T{T}")
+
+
+def test_bf16_kda_d64_batch():
+    wl = W.chunk_workload(seed=41, B=3, T=77, H=2, K=64, V=64)
+    _check_chunk(wl, "bf16_d64")
+
+
+def test_bf16_gate_g_beta_values_no_h0():
+    wl = W.chunk_workload(seed=42, B=2, T=150, H=2, gate="g", beta="values", h0_std=None)
+    _check_chunk(wl, "bf16_gate_g", h0=False)
+
+
+def test_bf16_no_l2norm_delta():
+    wl = W.chunk_workload(seed=43, B=1, T=96, H=2, l2norm=False, qkv_std=1.0 / 128 ** 0.5)
+    _check_chunk(wl, "bf16_no_l2norm")
+
+
+def test_bf16_gated_delta_off():
+    wl = W.chunk_workload(seed=44, B=1, T=70, H=2, delta=False, beta="none", qkv_std=0.1)
+    _check_chunk(wl, "bf16_gla")
+
+
+def test_bf16_prefill_reduced():
+    """The prefill recipe at T=1024 on 4 heads: checked in full."""
+    _check_chunk(W.prefill(T=1024, H=4), "prefill_1024")
+
+
+def test_bf16_prefill_full_size_sampled_heads():
+    """Full prefill (B=1, H=32, T=8192) in the benchmark's launch; the oracle
+    recomputes three heads (heads are independent)."""
+    wl = W.prefill()
+    o, hT = gpu_chunk(wl)
+    torch.cuda.synchronize()
+    heads = [0, 17, 31]
+    sub = subset_heads(wl, heads)
+    o_ref, h_ref = oracle_chunk(sub)
+    o_g = np64(o)[:, :, heads]
+    h_g = np64(hT)[:, heads]
+    assert_close("prefill_full o", o_g, o_ref, wl["dtype"])
+    assert_close("prefill_full hT", h_g, h_ref, wl["dtype"])
+    assert torch.isfinite(o.float()).all() and torch.isfinite(hT).all()
+
+
+def test_bf16_varlen_reduced():
+    lengths = [5, 16, 33, 0, 200, 1, 64]
+    wl = W.chunk_workload(seed=50, lengths=lengths, H=3)
+    _check_chunk(wl, "varlen_small")
+
+
+def test_bf16_varlen_full_size_sampled():
+    """16 packed sequences, lengths ~U[512, 8192], H=32: the oracle recomputes
+    three sequences on two heads."""
+    wl = W.varlen()
+    o, hT = gpu_chunk(wl)
+    torch.cuda.synchronize()
+    cu = wl["cu_seqlens"].tolist()
+    for n in (0, 5, 15):
+        for_heads = [3, 30]
+        sub = subset_heads(subset_sequence(wl, n), for_heads)
+        o_ref, h_ref = oracle_chunk(sub)
+        o_g = np64(o)[:, cu[n]:cu[n + 1]][:, :, for_heads]
+        assert_close(f"varlen seq {n} o", o_g, o_ref, wl["dtype"])
+        assert_close(f"varlen seq {n} hT", np64(hT)[n:n + 1, for_heads], h_ref, wl["dtype"])
+
+
+def test_split_sequence_resume():
+    """fwd(T) == fwd(T1) then fwd(T - T1) from the returned state (GPU only)."""
+    wl = W.prefill(T=300, H=2, seed=60)
+    o, hT = gpu_chunk(wl)
+    for T1 in (16, 123):
+        a = dict(wl)
+        b = dict(wl)
+        for key in ("q", "k", "v", "a", "b"):
+            a[key] = wl[key][:, :T1].contiguous()
+            b[key] = wl[key][:, T1:].contiguous()
+        a["T"], b["T"] = T1, 300 - T1
+        o1, h1 = gpu_chunk(a)
+        b["h0"] = h1.cpu()
+        o2, h2 = gpu_chunk(b)
+        torch.cuda.synchronize()
+        both = torch.cat([o1, o2], dim=1)
+        assert (both.float() - o.float()).abs().max().item() < 2e-2
+        assert (h2 - hT).abs().max().item() < 2e-2
+
+
+def test_deterministic():
+    wl = W.prefill(T=500, H=4, seed=61)
+    o1, h1 = gpu_chunk(wl)
+    o2, h2 = gpu_chunk(wl)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+
+
+def test_bad_cu_seqlens_reports_on_device():
+    wl = W.chunk_workload(seed=62, lengths=[20, 30], H=2)
+    wl["cu_seqlens"] = torch.tensor([0, 35, 20], dtype=torch.int32)  # decreasing
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gpu_chunk(wl, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 1
+
+
+# --------------------------------------------------------------------------
+# Decode
+# --------------------------------------------------------------------------
+
+def _decode(wl, err=None):
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in wl.items()}
+    pool = d["state_pool"].clone()
+    o = kda.kda_decode_step(d["packed_qkv"], d["a"], d["b"], d["A_log"], d["dt_bias"], pool, d["indices"],
+                            H=wl["H"], HV=wl["HV"], K=wl["K"], V=wl["V"], scale=wl["scale"], err=err)
+    torch.cuda.synchronize()
+    return o, pool
+
+
+def _decode_oracle(wl):
+    return ko.kda_decode(np64(wl["packed_qkv"]), np64(wl["a"]), np64(wl["b"]), np64(wl["A_log"]),
+                         np64(wl["dt_bias"]), np64(wl["state_pool"]), wl["indices"].numpy(), H=wl["H"],
+                         HV=wl["HV"], K=wl["K"], V=wl["V"], scale=wl["scale"])
+
+
+def _check_decode(wl):
+    o, pool = _decode(wl)
+    o_ref, pool_ref = _decode_oracle(wl)
+    idx = wl["indices"]
+    valid = idx[idx >= 0].long()
+    assert_close("decode o", np64(o), o_ref, torch.bfloat16)
+    assert_close("decode state", np64(pool[valid.cuda()]), pool_ref[valid.numpy()], torch.bfloat16)
+    # padding rows: bit-exact zero output; every slot not indexed is untouched
+    pads = (idx < 0).nonzero().flatten()
+    assert torch.equal(o[pads.cuda()], torch.zeros_like(o[pads.cuda()]))
+    untouched = torch.ones(wl["num_slots"], dtype=torch.bool)
+    untouched[valid] = False
+    ut = untouched.nonzero().flatten().cuda()
+    assert torch.equal(pool[ut], wl["state_pool"].cuda()[ut])
+    return o, pool
+
+
+@pytest.mark.parametrize("B,H,HV,K,V", [(1, 1, 1, 128, 128), (4, 2, 2, 128, 128), (32, 2, 4, 64, 64),
+                                        (13, 1, 4, 128, 64), (7, 2, 2, 64, 128)])
+def test_decode_small(B, H, HV, K, V):
+    wl = W.decode_workload(seed=70 + B, B=B, H=H, HV=HV, K=K, V=V, num_slots=2 * B + 3, pad_frac=0.25)
+    _check_decode(wl)
+
+
+def test_decode_full_size():
+    """B=256, H=HV=32, K=V=128, fp32 pool [512, 32, 128, 128], 26 padded rows."""
+    _check_decode(W.decode())
+
+
+def test_decode_all_padding_and_bad_slot():
+    wl = W.decode_workload(seed=80, B=6, H=2, HV=2, num_slots=8, pad_frac=0.0)
+    wl["indices"] = torch.tensor([-1, -1, 3, 99, -1, 2], dtype=torch.int32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, pool = _decode(wl, err=err)
+    assert int(err.item()) == 1
+    assert torch.equal(o[[0, 1, 3, 4]], torch.zeros_like(o[[0, 1, 3, 4]]))
+    assert torch.equal(pool[[0, 1, 4, 5, 6, 7]], wl["state_pool"].cuda()[[0, 1, 4, 5, 6, 7]])
+    o_ref, pool_ref = _decode_oracle(dict(wl, indices=torch.tensor([-1, -1, 3, -1, -1, 2], dtype=torch.int32)))
+    assert_close("decode o", np64(o), o_ref, torch.bfloat16)
+    assert_close("decode state", np64(pool[[2, 3]]), pool_ref[[2, 3]], torch.bfloat16)
+
+
+def test_prefill_state_feeds_decode():
+    """A prefill's hT placed in a pool slot, then one decode token, equals the
+    oracle running the whole sequence plus that token."""
+    wl = W.prefill(T=64, H=2, seed=90)
+    _, hT = gpu_chunk(wl)
+    dw = W.decode_workload(seed=91, B=1, H=2, HV=2, num_slots=2, pad_frac=0.0)
+    dw["indices"] = torch.tensor([1], dtype=torch.int32)
+    dw["state_pool"][1] = hT[0].cpu()
+    o, pool = _decode(dw)
+    # oracle: prefill, then the decode step on the oracle's own state
+    _, h_ref = oracle_chunk(wl)
+    dref = dict(dw)
+    pool_ref_in = np64(dw["state_pool"]).copy()
+    pool_ref_in[1] = h_ref[0]
+    o_ref, _ = ko.kda_decode(np64(dw["packed_qkv"]), np64(dw["a"]), np64(dw["b"]), np64(dw["A_log"]),
+                             np64(dw["dt_bias"]), pool_ref_in, np.array([1]), H=2, HV=2, K=128, V=128,
+                             scale=dref["scale"])
+    assert_close("prefill->decode o", np64(o), o_ref, torch.bfloat16)

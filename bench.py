@@ -1,0 +1,385 @@
+"""Benchmark of the KDA hot path on GB300.
+
+One step = one chunk forward over the prefill workload (bf16, B=1, H=32,
+T=8192, d=128, gate inputs, beta logits, L2 norm, fp32 h0) followed by one fused
+decode step over the decode workload (B=256, H=HV=32, K=V=128, fp32 slot pool
+[512, 32, 128, 128], 26 padding rows). Inputs are seeded synthetic data,
+resident in HBM before timing; every input is larger than L2, so no flush is
+needed between steps.
+
+Prints ONE JSON line (rank 0). value = chunk-forward tokens/s (whole job), with
+decode microseconds per step, both roofline fractions, the e2e figure through
+host buffers, the oracle's CPU throughput and the clocks seen while timing.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (the reference arm of this benchmark). Under torchrun each rank runs
+its own replica of the workload (weak scaling; the path needs no collective).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "KDA chunk-fwd tokens/s (H=32,d=128) + % roofline; decode μs/step at B=256"
+UNIT = "tokens/s"
+WORKLOAD = "KDA prefill bf16 B=1 H=32 T=8192 dk=dv=128 (gate inputs, beta logits, L2 norm, h0) + fused decode B=256 H=HV=32 K=V=128 (fp32 pool 512 slots, 26 pads)"
+
+# Algorithmic bytes (each input read once, each output written once).
+PREFILL_T, PREFILL_H, D = 8192, 32, 128
+BYTES_PER_TOKEN = PREFILL_H * (D * 2 * 3 + D * 4 + 2 + D * 2)  # q,k,v bf16 + a fp32 + b bf16 + o bf16 = 49,216
+STATE_BYTES = PREFILL_H * D * D * 4                            # one fp32 state set (h0 or hT)
+PARAM_BYTES = PREFILL_H * D * 4 + PREFILL_H * 4                # dt_bias + A_log
+
+
+def prefill_algorithmic_bytes(T=PREFILL_T):
+    return T * BYTES_PER_TOKEN + 2 * STATE_BYTES + PARAM_BYTES
+
+
+def prefill_algorithmic_flops(T=PREFILL_T):
+    """Tensor work per token and head of the chunk form (C = 16, d = 128):
+    K_dec S, Q_dec S (2 * 2 d^2), state update K_res^T U (2 d^2), L and Mqk
+    (2 * 2 * C d / 2, lower triangles), Mqk U (C d), INV (Neumann, 6 C^2 per token),
+    W and U~ (2 * 2 C d)."""
+    C = 16
+    per = 4 * D * D + 2 * D * D + 2 * C * D + C * D + 6 * C * C + 4 * C * D
+    return T * PREFILL_H * per
+
+
+def decode_algorithmic_bytes(n_valid, H=32, HV=32, K=128, V=128, B=256):
+    state = n_valid * HV * V * K * 4 * 2                            # read + write of each valid slot
+    io = n_valid * (2 * H * K * 2 + HV * V * 2 + HV * K * 2 + HV * 2)  # packed q,k,v + a + b of valid rows
+    params = HV * 4 + HV * K * 4 + B * 4                               # A_log, dt_bias, indices
+    return state + io + params + B * HV * V * 2                         # + o
+
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def kernel_sources_sha(names):
+    h = hashlib.sha256()
+    for n in names:
+        h.update((ROOT / "kimi_delta_attention_04_gb300" / "csrc" / n).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(kernel_key, sha):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source; otherwise None."""
+    p = ROOT / "profiles" / "traffic.json"
+    if not p.exists():
+        return None
+    d = json.loads(p.read_text()).get(kernel_key)
+    if not d or d.get("source_sha") != sha:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except FileNotFoundError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_sample(T_sample=None, budget_s=20.0):
+    """Time the fp64 oracle (token recurrence, as it stands) on the first tokens
+    of the prefill workload, all 32 heads. Returns (tokens/s, sample text, cores)."""
+    import numpy as np  # noqa: F401
+
+    from kimi_delta_attention_04_gb300 import workloads as W
+    from oracle import kda_oracle as ko
+
+    wl = W.prefill()
+    np64 = lambda t: None if t is None else t.double().numpy()  # noqa: E731
+    # calibrate on 32 tokens, then size the sample to the time budget
+    T_cal = 32
+    t0 = time.perf_counter()
+    ko.kda_forward(np64(wl["q"][:, :T_cal]), np64(wl["k"][:, :T_cal]), np64(wl["v"][:, :T_cal]),
+                   scale=wl["scale"], a=np64(wl["a"][:, :T_cal]), dt_bias=np64(wl["dt_bias"]),
+                   A_log=np64(wl["A_log"]), b=np64(wl["b"][:, :T_cal]), h0=np64(wl["h0"]), l2norm_qk=True)
+    per_tok = (time.perf_counter() - t0) / T_cal
+    if T_sample is None:
+        T_sample = int(max(64, min(PREFILL_T, budget_s / max(per_tok, 1e-6))))
+    t0 = time.perf_counter()
+    ko.kda_forward(np64(wl["q"][:, :T_sample]), np64(wl["k"][:, :T_sample]), np64(wl["v"][:, :T_sample]),
+                   scale=wl["scale"], a=np64(wl["a"][:, :T_sample]), dt_bias=np64(wl["dt_bias"]),
+                   A_log=np64(wl["A_log"]), b=np64(wl["b"][:, :T_sample]), h0=np64(wl["h0"]), l2norm_qk=True)
+    dt = time.perf_counter() - t0
+    sample = (f"fp64 token-recurrence oracle, first {T_sample} of 8192 tokens of the prefill workload, "
+              f"all 32 heads, one process ({dt:.1f} s)")
+    return T_sample / dt, sample, 1
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    budget = max(3.0, 60.0 / max(args.steps + args.warmup, 1))
+    vals = []
+    sample = ""
+    for i in range(args.warmup + args.steps):
+        v, sample, cores = oracle_sample(budget_s=budget)
+        if i >= args.warmup:
+            vals.append(v)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * PREFILL_T / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "impl": "fp64 CPU oracle (token recurrence)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    world, rank, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", init_method="env://")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    from kimi_delta_attention_04_gb300 import build as kbuild
+    kbuild.build()
+    import kimi_delta_attention_04_gb300 as kda
+    from kimi_delta_attention_04_gb300 import workloads as W
+
+    stream = torch.cuda.current_stream(dev)
+    # --- inputs (replica per rank: seeds differ, shapes identical) ---
+    T = args.seq_len
+    wl = W.prefill(seed=2 + 100 * rank, T=T)
+    dw = W.decode(seed=4 + 100 * rank) if args.only != "chunk" else W.decode(seed=4, B=8, num_slots=16)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in wl.items()}
+    dd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in dw.items()}
+    o = torch.empty(1, T, PREFILL_H, D, dtype=torch.bfloat16, device=dev)
+    hT = torch.empty(1, PREFILL_H, D, D, dtype=torch.float32, device=dev)
+    args_c = kda.make_chunk_args(d["q"], d["k"], d["v"], scale=d["scale"], a=d["a"], dt_bias=d["dt_bias"],
+                                 A_log=d["A_log"], b=d["b"], h0=d["h0"], l2norm_qk=True, o=o, hT=hT)
+    ws = torch.empty(kda.chunk_workspace_size(args_c), dtype=torch.uint8, device=dev)
+    pool = dd["state_pool"]
+    od = torch.empty(dw["B"], dw["HV"], dw["V"], dtype=torch.bfloat16, device=dev)
+    n_valid = int((dw["indices"] >= 0).sum())
+
+    def chunk_step():
+        if args.only == "decode":
+            return
+        kda.kda_chunk_fwd(d["q"], d["k"], d["v"], scale=d["scale"], a=d["a"], dt_bias=d["dt_bias"],
+                          A_log=d["A_log"], b=d["b"], h0=d["h0"], l2norm_qk=True, o=o, hT=hT, workspace=ws,
+                          stream=stream)
+
+    def decode_step():
+        if args.only == "chunk":
+            return
+        kda.kda_decode_step(dd["packed_qkv"], dd["a"], dd["b"], dd["A_log"], dd["dt_bias"], pool, dd["indices"],
+                            H=dw["H"], HV=dw["HV"], K=dw["K"], V=dw["V"], scale=dw["scale"], o=od, stream=stream)
+
+    for _ in range(args.warmup):
+        chunk_step()
+        decode_step()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index) as clocks:
+        e0.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            chunk_step()
+            ev[i][1].record(stream)
+            decode_step()
+            ev[i][2].record(stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    chunk_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    total_ms = e0.elapsed_time(e1)
+
+    # --- e2e through the public API with pinned host buffers ---
+    host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in wl.items()}
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    hT_h = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
+    names = ("q", "k", "v", "a", "dt_bias", "A_log", "b", "h0")
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = o_h.numel() * o_h.element_size() + hT_h.numel() * hT_h.element_size()
+    e2e_steps = max(2, min(K, 5)) if args.only != "decode" else 0
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        dev_in = {n: host[n].to(dev, non_blocking=True) for n in names}
+        kda.kda_chunk_fwd(dev_in["q"], dev_in["k"], dev_in["v"], scale=wl["scale"], a=dev_in["a"],
+                          dt_bias=dev_in["dt_bias"], A_log=dev_in["A_log"], b=dev_in["b"], h0=dev_in["h0"],
+                          l2norm_qk=True, o=o, hT=hT, workspace=ws, stream=stream)
+        o_h.copy_(o, non_blocking=True)
+        hT_h.copy_(hT, non_blocking=True)
+        torch.cuda.synchronize(dev)
+    e2e_s = (time.perf_counter() - t0) / max(e2e_steps, 1)
+
+    # --- reduce over ranks: max time ---
+    t_chunk = sum(chunk_ms) / 1000.0
+    t_dec = sum(dec_ms) / 1000.0
+    t_total = total_ms / 1000.0
+    vals = torch.tensor([t_chunk, t_dec, t_total, e2e_s], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
+    t_chunk, t_dec, t_total, e2e_s = vals.tolist()
+    tokens = T * K * world
+    value = tokens / t_chunk if t_chunk > 0 else 0.0
+
+    hbm, tflops, peak_kind = load_peaks()
+    chunk_avg = t_chunk / K
+    dec_avg = t_dec / K
+    abytes = prefill_algorithmic_bytes(T)
+    aflops = prefill_algorithmic_flops(T)
+    achieved = abytes / chunk_avg / 1e9 if chunk_avg > 0 else 0.0
+    t_roof = max(abytes / (hbm * 1e9), aflops / (tflops * 1e12))
+    dbytes = decode_algorithmic_bytes(n_valid)
+    dach = dbytes / dec_avg / 1e9 if dec_avg > 0 else 0.0
+    chunk_sha = kernel_sources_sha(["kda_chunk_tc.cu", "kda_common.cuh"])
+    dec_sha = kernel_sources_sha(["kda_decode.cu", "kda_common.cuh"])
+    clk = clocks.summary()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * t_total / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": PREFILL_T,
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (prefill 403 MB, decode ~964 MB touched); no flush",
+                       "step": "one chunk forward (prefill) then one decode step (B=256)"},
+            "chunk_fwd": {"ms": 1000.0 * chunk_avg, "tokens_per_s": value,
+                          "roofline_time_us": 1e6 * t_roof, "frac_of_roofline": t_roof / chunk_avg if chunk_avg > 0 else 0.0},
+            "decode": {"us_per_step": 1e6 * dec_avg, "n_valid_rows": n_valid,
+                       "roofline": {"bound": "hbm", "achieved": dach, "peak": hbm, "unit": "GB/s",
+                                    "frac": dach / hbm, "algorithmic_bytes": dbytes,
+                                    "traffic": stored_traffic("kda_decode", dec_sha), "peak_kind": peak_kind}},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": stored_traffic("kda_chunk_fwd", chunk_sha), "kernel": "chunk forward (prep + recurrence launches)",
+                         "algorithmic_bytes": abytes, "peak_kind": peak_kind},
+            "e2e": {"value": T * world / e2e_s if e2e_steps else None, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": (2 if args.only != "decode" else 0) * K + (1 if args.only != "chunk" else 0) * K,
+            "clocks": clk,
+        }
+        if args.only != "all" or T != PREFILL_T:
+            line["config"]["partial"] = f"only={args.only}, seq_len={T}: a profiling run, not the benchmark line"
+        if world == 1 and not args.no_cpu_baseline:
+            v, sample, cores = oracle_sample(budget_s=args.cpu_budget)
+            line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "chunk", "decode"], default="all",
+                    help="time only one part (profiling runs; the benchmark line uses all)")
+    ap.add_argument("--seq-len", type=int, default=PREFILL_T, help="prefill tokens (profiling runs use fewer)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -16,6 +16,10 @@ bool chunk_dims_supported(const kda_chunk_args& a) {
   return false;
 }
 
+// bf16 with dk = dv = 128 runs the fused cluster kernel (prep and recurrence in
+// one launch); other shapes run the two-kernel path through workspace records.
+bool uses_fused(const kda_chunk_args& a) { return a.dtype == KDA_DTYPE_BF16 && a.dk == 128 && a.dv == 128; }
+
 // Returns KDA_OK and fills geometry when the arguments are well formed.
 kda_status check_chunk(const kda_chunk_args* a, kda::ChunkGeom* geo, size_t* rec_bytes) {
   if (a == nullptr) return KDA_ERR_INVALID_ARG;
@@ -62,6 +66,10 @@ kda_status check_chunk(const kda_chunk_args* a, kda::ChunkGeom* geo, size_t* rec
     geo->max_chunks = a->B * geo->chunks_per_seq;
   } else {
     geo->max_chunks = geo->chunks_per_seq + a->N;  // each sequence adds at most one partial chunk
+  }
+  if (uses_fused(*a)) {
+    *rec_bytes = 0;  // prep and recurrence exchange chunks on chip: no records
+    return KDA_OK;
   }
   *rec_bytes = a->dtype == KDA_DTYPE_BF16 ? kda::record_bytes_tc(a->dk) : kda::record_bytes_f32(a->dk, a->dv);
   if (*rec_bytes == 0) return KDA_ERR_UNSUPPORTED;
@@ -119,7 +127,8 @@ kda_status kda_chunk_fwd(const kda_chunk_args* args, void* workspace, size_t ws_
   cudaError_t e = cudaSuccess;
   if (geo.cu_seqlens != nullptr) e = kda::launch_plan(c, s);
   if (e == cudaSuccess) {
-    e = args->dtype == KDA_DTYPE_BF16 ? kda::launch_chunk_tc(c, s) : kda::launch_chunk_f32(c, s);
+    if (uses_fused(*args)) e = kda::launch_chunk_fused(c, s);
+    else e = args->dtype == KDA_DTYPE_BF16 ? kda::launch_chunk_tc(c, s) : kda::launch_chunk_f32(c, s);
   }
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

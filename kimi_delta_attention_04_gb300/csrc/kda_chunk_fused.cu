@@ -1,0 +1,631 @@
+// Fused chunkwise KDA forward for bf16 inputs, dk = dv = 128: one 4-CTA
+// thread-block cluster per (sequence, head), prep and recurrence in one kernel.
+//
+// Mathematics as in kda_chunk_tc.cu ("FlashKDA里的L矩阵和Mqk矩阵": L, Mqk, the
+// Neumann inverse, the K2 chunk step; the sequence kept out of the grid and d_v
+// split across CTAs as in "TileLang 实战：KDA 从零到一" §6.4). What changes is the
+// placement:
+//
+//  * CTA r of the cluster owns value rows [32r, 32r + 32) of the state. Its four
+//    recurrence warps are (16-row block) x (half of the key channels): each holds
+//    S^T[16 x 64] fp32 in registers as mma.sync accumulators. The U^T partial
+//    sums of the two key halves are exchanged through shared memory once per
+//    chunk (split-K), which halves the serial MMA chain per warp.
+//  * The same CTA's four prep warps prepare every 4th chunk (chunks c = r mod 4):
+//    gate, beta, L2 norm, decay products, L / Mqk, Neumann inverse, W and U~.
+//    Inputs for the producer's next chunk are prefetched with cp.async while the
+//    current one is computed.
+//  * A prepared chunk is pushed from the producer's shared memory into stage
+//    c mod 4 of all four CTAs' rings with cp.async.bulk over distributed shared
+//    memory (the shared operands to every CTA, each CTA's 32 rows of U~ to it),
+//    counted on the destination's "full" mbarrier. Consumers release a stage by
+//    arriving on the producer's "empty" mbarrier. Nothing goes through global
+//    memory between prep and recurrence.
+//  * Every mbarrier wait is bounded (KDA_ERR_TIMEOUT in err on expiry); loop trip
+//    counts never depend on a wait, so named barriers stay matched and every CTA
+//    reaches the closing cluster barrier.
+#include <type_traits>
+
+#include "kda_cluster.cuh"
+#include "kda_common.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int FD = 128;              // dk = dv
+constexpr int kCtas = 4;             // cluster size
+constexpr int kRows = FD / kCtas;    // value rows per CTA
+constexpr int kRing = 4;             // ring stages (= cluster size: stage s is produced by CTA s)
+constexpr int kFusedThreads = 256;   // 4 recurrence warps + 4 prep warps
+constexpr int kPad = FD + 8;         // padded 16-bit row (conflict-free ldmatrix)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+struct __align__(16) Stage {
+  uint16_t W[16][kPad];    // bf16, -W = -INV diag(beta) k_dec
+  uint16_t qd[16][kPad];   // bf16, scale q e^{G}
+  uint16_t kr[16][kPad];   // st2, k e^{G_last - G}
+  uint16_t mqk[16][24];    // st2
+  float gamma[FD];         // e^{G_last}
+  float ut[kRows][16];     // U~ rows of this CTA (transposed)
+};
+constexpr uint32_t kSharedBytes = offsetof(Stage, ut);
+constexpr uint32_t kUtSliceBytes = sizeof(float) * kRows * 16;
+constexpr uint32_t kStageTx = kSharedBytes + kUtSliceBytes;
+static_assert(kSharedBytes % 16 == 0 && kStageTx == sizeof(Stage), "stage layout");
+
+struct __align__(16) PrepOut {
+  uint16_t W[16][kPad];
+  uint16_t qd[16][kPad];
+  uint16_t kr[16][kPad];
+  uint16_t mqk[16][24];
+  float gamma[FD];
+  float ut[FD][16];  // all value rows
+};
+static_assert(offsetof(PrepOut, ut) == kSharedBytes, "prep-out and stage share the layout");
+
+struct __align__(16) PrepIn {
+  __nv_bfloat16 q[16][FD];
+  __nv_bfloat16 k[16][FD];
+  __nv_bfloat16 v[16][FD];
+  float a[16][FD];  // gate inputs a, or log-decay g
+};
+
+template <typename Q>
+struct __align__(16) PrepScratch {
+  Q A_lv[4][16][kPad];
+  Q B_lv[4][8][kPad];
+  Q kdec[16][kPad];
+  __nv_bfloat16 vs[16][kPad];
+  Q invq[16][24];
+  __nv_bfloat16 invhi[16][24];
+  __nv_bfloat16 invlo[16][24];
+  float Lm[16][17];
+  float Mq[16][17];
+  float X[4][16][17];
+  float red[4][48];
+  float rnq[16], rnk[16], beta[16];
+};
+
+struct __align__(16) RecScratch {
+  float xch[2][2][2][32][16];        // [chunk parity][row block][key half][lane][8 U + 8 O]
+  __nv_bfloat16 ost[2][16][16];      // per row block: [token][value row]
+};
+
+template <typename Q>
+struct __align__(128) FusedSmem {
+  Stage ring[kRing];
+  PrepOut pout;
+  PrepIn pin[2];
+  PrepScratch<Q> ps;
+  RecScratch rs;
+  uint64_t full[kRing];
+  uint64_t empty[kRing];
+  int failed;
+};
+
+__device__ __forceinline__ int row_tok_f(int s, int r) { return (r / s) * 2 * s + s + (r % s); }
+__device__ __forceinline__ int col_tok_f(int s, int r) { return (r / s) * 2 * s + (r % s); }
+
+template <typename Op>
+__device__ __forceinline__ void warp_mm16_f(const float* A, bool addIA, const float* B, bool addIB, float* C,
+                                            int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  auto ea = [&](int r, int c) { return A[r * 17 + c] + ((addIA && r == c) ? 1.f : 0.f); };
+  auto eb = [&](int r, int c) { return B[r * 17 + c] + ((addIB && r == c) ? 1.f : 0.f); };
+  uint32_t a[4];
+  a[0] = Op::pack(ea(g, 2 * t), ea(g, 2 * t + 1));
+  a[1] = Op::pack(ea(g + 8, 2 * t), ea(g + 8, 2 * t + 1));
+  a[2] = Op::pack(ea(g, 2 * t + 8), ea(g, 2 * t + 9));
+  a[3] = Op::pack(ea(g + 8, 2 * t + 8), ea(g + 8, 2 * t + 9));
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    const int n = 8 * nt + g;
+    const uint32_t b0 = Op::pack(eb(2 * t, n), eb(2 * t + 1, n));
+    const uint32_t b1 = Op::pack(eb(2 * t + 8, n), eb(2 * t + 9, n));
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    mma16816<Op>(c, a, b0, b1);
+    const int col = 8 * nt + 2 * t;
+    C[g * 17 + col] = c[0];
+    C[g * 17 + col + 1] = c[1];
+    C[(g + 8) * 17 + col] = c[2];
+    C[(g + 8) * 17 + col + 1] = c[3];
+  }
+  __syncwarp();
+}
+
+// Issue the loads of one chunk's inputs into a PrepIn buffer (prep threads).
+__device__ __forceinline__ void prefetch_inputs(const ChunkCall& p, PrepIn& in, int h, int tok0, int ntok, int pt) {
+  const int H = p.geo.H;
+  const size_t rs = static_cast<size_t>(H) * FD;
+  // q, k, v: 16 rows x 16 vectors of 16 B each
+  for (int i = pt; i < 3 * 16 * 16; i += 128) {
+    const int which = i >> 8, row = (i >> 4) & 15, vec = i & 15;
+    const __nv_bfloat16* src = which == 0 ? reinterpret_cast<const __nv_bfloat16*>(p.q)
+                             : which == 1 ? reinterpret_cast<const __nv_bfloat16*>(p.k)
+                                          : reinterpret_cast<const __nv_bfloat16*>(p.v);
+    __nv_bfloat16* dst = which == 0 ? &in.q[row][vec * 8] : which == 1 ? &in.k[row][vec * 8] : &in.v[row][vec * 8];
+    const bool valid = row < ntok;
+    const __nv_bfloat16* s = src + (valid ? (static_cast<size_t>(tok0 + row) * H + h) * FD + vec * 8 : 0);
+    cp_async16_zfill(dst, s, valid ? 16u : 0u);
+  }
+  if (p.gate_mode != 0) {
+    const float* src = p.gate_mode == 1 ? p.g : p.a;  // both [tokens, H * FD] fp32
+    for (int i = pt; i < 16 * 32; i += 128) {
+      const int row = i >> 5, vec = i & 31;
+      const bool valid = row < ntok;
+      const float* s = src + (valid ? (static_cast<size_t>(tok0 + row) * H + h) * FD + vec * 4 : 0);
+      cp_async16_zfill(&in.a[row][vec * 4], s, valid ? 16u : 0u);
+    }
+  }
+}
+
+template <bool DELTA, bool L2N>
+__global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1)
+    kda_chunk_fused_kernel(const ChunkCall p) {
+  using QK = std::conditional_t<L2N, F16, Bf16>;
+  using ST2 = std::conditional_t<DELTA, F16, Bf16>;
+  using Q = typename QK::T;
+  using Smem = FusedSmem<Q>;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+
+  const int H = p.geo.H;
+  const uint32_t rank = cluster_ctarank();
+  const int unit = blockIdx.x / kCtas;
+  const int n = unit / H;
+  const int h = unit - n * H;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int ts = 0, te = 0, cb = 0;
+  const bool ok = locate_seq(p.geo, n, ts, te, cb);
+  const int nch = ok ? (te - ts + kChunk - 1) / kChunk : 0;
+
+  if (tid == 0) {
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], kCtas * 4);
+    }
+    sm.failed = 0;
+    fence_mbarrier_init_cluster();
+  }
+  cluster_sync_all();
+
+  if (warp < 4) {
+    // ===================== recurrence warps =====================
+    const int dvb = warp >> 1, dkh = warp & 1;
+    const int g = lane >> 2, t = lane & 3;
+    const int row0 = static_cast<int>(rank) * kRows + dvb * 16;  // first value row of this warp
+    const int kc0 = dkh * 64;                                    // first key channel of this warp
+    float S[8][4];
+    if (ok && p.h0 != nullptr) {
+      const float* src = p.h0 + (static_cast<size_t>(n) * H + h) * FD * FD;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        const float2 x = *reinterpret_cast<const float2*>(src + (row0 + g) * FD + kc0 + 8 * nt + 2 * t);
+        const float2 y = *reinterpret_cast<const float2*>(src + (row0 + g + 8) * FD + kc0 + 8 * nt + 2 * t);
+        S[nt][0] = x.x; S[nt][1] = x.y; S[nt][2] = y.x; S[nt][3] = y.y;
+      }
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.f;
+    }
+    bool failed = false;
+    for (int c = 0; c < nch; ++c) {
+      const int s = c & (kRing - 1);
+      const uint32_t par = static_cast<uint32_t>(c / kRing) & 1u;
+      if (!failed && !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.full[s])), par,
+                                        kWaitLimitNs)) {
+        failed = true;
+        if (lane == 0) set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
+      }
+      const Stage& st = sm.ring[s];
+      uint32_t sa[4][4];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        sa[kk][0] = Bf16::pack(S[2 * kk][0], S[2 * kk][1]);
+        sa[kk][1] = Bf16::pack(S[2 * kk][2], S[2 * kk][3]);
+        sa[kk][2] = Bf16::pack(S[2 * kk + 1][0], S[2 * kk + 1][1]);
+        sa[kk][3] = Bf16::pack(S[2 * kk + 1][2], S[2 * kk + 1][3]);
+      }
+      float u[2][4], o[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        if (dkh == 0) {
+          const float2 x = *reinterpret_cast<const float2*>(&st.ut[dvb * 16 + g][8 * nt + 2 * t]);
+          const float2 y = *reinterpret_cast<const float2*>(&st.ut[dvb * 16 + g + 8][8 * nt + 2 * t]);
+          u[nt][0] = x.x; u[nt][1] = x.y; u[nt][2] = y.x; u[nt][3] = y.y;
+        } else {
+          u[nt][0] = u[nt][1] = u[nt][2] = u[nt][3] = 0.f;
+        }
+        o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+      }
+      const int brow = ((lane >> 4) << 3) + (lane & 7);
+      const int bcol = ((lane >> 3) & 1) * 8;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t b[4];
+        if (DELTA) {
+          ldsm_x4(b, &st.W[brow][kc0 + 16 * kk + bcol]);
+          mma16816<Bf16>(u[0], sa[kk], b[0], b[1]);
+          mma16816<Bf16>(u[1], sa[kk], b[2], b[3]);
+        }
+        ldsm_x4(b, &st.qd[brow][kc0 + 16 * kk + bcol]);
+        mma16816<Bf16>(o[0], sa[kk], b[0], b[1]);
+        mma16816<Bf16>(o[1], sa[kk], b[2], b[3]);
+      }
+      // exchange the key-half partial sums of U^T (and O^T) within the warp pair
+      {
+        float* mine = sm.rs.xch[c & 1][dvb][dkh][lane];
+        *reinterpret_cast<float4*>(mine + 0) = make_float4(u[0][0], u[0][1], u[0][2], u[0][3]);
+        *reinterpret_cast<float4*>(mine + 4) = make_float4(u[1][0], u[1][1], u[1][2], u[1][3]);
+        if (dkh == 1) {
+          *reinterpret_cast<float4*>(mine + 8) = make_float4(o[0][0], o[0][1], o[0][2], o[0][3]);
+          *reinterpret_cast<float4*>(mine + 12) = make_float4(o[1][0], o[1][1], o[1][2], o[1][3]);
+        }
+        named_bar_sync(2 + dvb, 64);
+        const float* other = sm.rs.xch[c & 1][dvb][dkh ^ 1][lane];
+        const float4 a0 = *reinterpret_cast<const float4*>(other + 0);
+        const float4 a1 = *reinterpret_cast<const float4*>(other + 4);
+        u[0][0] += a0.x; u[0][1] += a0.y; u[0][2] += a0.z; u[0][3] += a0.w;
+        u[1][0] += a1.x; u[1][1] += a1.y; u[1][2] += a1.z; u[1][3] += a1.w;
+        if (dkh == 0) {
+          const float4 b0 = *reinterpret_cast<const float4*>(other + 8);
+          const float4 b1 = *reinterpret_cast<const float4*>(other + 12);
+          o[0][0] += b0.x; o[0][1] += b0.y; o[0][2] += b0.z; o[0][3] += b0.w;
+          o[1][0] += b1.x; o[1][1] += b1.y; o[1][2] += b1.z; o[1][3] += b1.w;
+        }
+      }
+      uint32_t ua[4];
+      ua[0] = ST2::pack(u[0][0], u[0][1]);
+      ua[1] = ST2::pack(u[0][2], u[0][3]);
+      ua[2] = ST2::pack(u[1][0], u[1][1]);
+      ua[3] = ST2::pack(u[1][2], u[1][3]);
+      // state update on this warp's key half: S^T = S^T diag(gamma) + U^T k_res
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        uint32_t b[4];
+        ldsm_x4_trans(b, &st.kr[lane & 15][kc0 + 16 * np + (lane >> 4) * 8]);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int nt = 2 * np + half;
+          const float2 gm = *reinterpret_cast<const float2*>(&st.gamma[kc0 + 8 * nt + 2 * t]);
+          S[nt][0] *= gm.x; S[nt][1] *= gm.y; S[nt][2] *= gm.x; S[nt][3] *= gm.y;
+          mma16816<ST2>(S[nt], ua, b[2 * half], b[2 * half + 1]);
+        }
+      }
+      if (dkh == 0) {
+        uint32_t b[4];
+        ldsm_x4(b, &st.mqk[brow][bcol]);
+        mma16816<ST2>(o[0], ua, b[0], b[1]);
+        mma16816<ST2>(o[1], ua, b[2], b[3]);
+        __nv_bfloat16 (&ost)[16][16] = sm.rs.ost[dvb];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          const int tok = 8 * nt + 2 * t;
+          ost[tok][g] = __float2bfloat16_rn(o[nt][0]);
+          ost[tok + 1][g] = __float2bfloat16_rn(o[nt][1]);
+          ost[tok][g + 8] = __float2bfloat16_rn(o[nt][2]);
+          ost[tok + 1][g + 8] = __float2bfloat16_rn(o[nt][3]);
+        }
+        __syncwarp();
+        const int tok0 = ts + c * kChunk;
+        const int ntok = min(kChunk, te - tok0);
+        const int row = lane >> 1, hv = lane & 1;
+        if (row < ntok) {
+          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.o) +
+                               (static_cast<size_t>(tok0 + row) * H + h) * FD + row0 + hv * 8;
+          *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&ost[row][hv * 8]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0)
+        mbar_arrive_cluster(mapa_shared(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.empty[s])),
+                                        static_cast<uint32_t>(s)));
+    }
+    if (ok && p.hT != nullptr) {
+      float* dst = p.hT + (static_cast<size_t>(n) * H + h) * FD * FD;
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt) {
+        *reinterpret_cast<float2*>(dst + (row0 + g) * FD + kc0 + 8 * nt + 2 * t) = make_float2(S[nt][0], S[nt][1]);
+        *reinterpret_cast<float2*>(dst + (row0 + g + 8) * FD + kc0 + 8 * nt + 2 * t) =
+            make_float2(S[nt][2], S[nt][3]);
+      }
+    }
+  } else {
+    // ===================== prep warps =====================
+    const int pt = tid - 128;  // key / value channel owned by this thread
+    const int pw = pt >> 5;    // prep warp index 0..3
+    auto prep_bar = [] { named_bar_sync(1, 128); };
+    const float Aexp = (p.gate_mode == 2) ? expf(p.A_log[h]) : 0.f;
+    const float dtb = (p.gate_mode == 2) ? p.dt_bias[h * FD + pt] : 0.f;
+    bool failed = false;
+    int c = static_cast<int>(rank);
+    float beta_next = 0.f;
+    auto load_beta = [&](int cc) {
+      float bt = 0.f;
+      const int tk0 = ts + cc * kChunk;
+      if (DELTA && pt < 16 && tk0 + pt < te) {
+        const float raw = __bfloat162float(
+            reinterpret_cast<const __nv_bfloat16*>(p.beta)[static_cast<size_t>(tk0 + pt) * H + h]);
+        bt = (p.beta_mode == 1) ? sigmoid_f(raw) : raw;
+      }
+      return bt;
+    };
+    if (c < nch) {
+      prefetch_inputs(p, sm.pin[0], h, ts + c * kChunk, min(kChunk, te - (ts + c * kChunk)), pt);
+      cp_async_commit();
+      beta_next = load_beta(c);
+    }
+    for (int j = 0; c < nch; ++j, c += kCtas) {
+      const int buf = j & 1;
+      const int tok0 = ts + c * kChunk;
+      const int ntok = min(kChunk, te - tok0);
+      const float beta_cur = beta_next;
+      if (c + kCtas < nch) {
+        const int t1 = ts + (c + kCtas) * kChunk;
+        prefetch_inputs(p, sm.pin[buf ^ 1], h, t1, min(kChunk, te - t1), pt);
+        cp_async_commit();
+        beta_next = load_beta(c + kCtas);
+        cp_async_wait<1>();
+      } else {
+        cp_async_wait<0>();
+      }
+      if (pt == 0) bulk_wait_read_all();  // the previous push has finished reading pout
+      for (int i = pt; i < 16 * 17; i += 128) {
+        (&sm.ps.Lm[0][0])[i] = 0.f;
+        (&sm.ps.Mq[0][0])[i] = 0.f;
+      }
+      if (pt < 16) sm.ps.beta[pt] = beta_cur;
+      prep_bar();
+      const PrepIn& in = sm.pin[buf];
+      float qv[16], kv[16], al[16], vv[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        qv[i] = __bfloat162float(in.q[i][pt]);
+        kv[i] = __bfloat162float(in.k[i][pt]);
+        vv[i] = __bfloat162float(in.v[i][pt]);
+        float a = 1.f;
+        if (i < ntok) {
+          if (p.gate_mode == 1) a = __expf(in.a[i][pt]);
+          else if (p.gate_mode == 2) {
+            const float x = in.a[i][pt] + dtb;
+            const float sp = x <= 20.f ? __logf(1.f + __expf(x)) : x;
+            a = __expf(-Aexp * sp);
+          }
+        }
+        al[i] = a;
+      }
+      {
+        float red[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) red[i] = qv[i] * qv[i];
+        const float t1 = warp_transpose_reduce16(red, lane);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) red[i] = kv[i] * kv[i];
+        const float t2 = warp_transpose_reduce16(red, lane);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) red[i] = qv[i] * kv[i];
+        const float t3 = warp_transpose_reduce16(red, lane);
+        if ((lane & 1) == 0) {
+          const int jj = lane >> 1;
+          sm.ps.red[pw][jj] = t1;
+          sm.ps.red[pw][16 + jj] = t2;
+          sm.ps.red[pw][32 + jj] = t3;
+        }
+      }
+      prep_bar();
+      if (pt < 16) {
+        float sq = 0.f, sk = 0.f, sqk = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          sq += sm.ps.red[w][pt];
+          sk += sm.ps.red[w][16 + pt];
+          sqk += sm.ps.red[w][32 + pt];
+        }
+        const float rq = L2N ? rsqrtf(sq + 1e-6f) : 1.f;
+        const float rk = L2N ? rsqrtf(sk + 1e-6f) : 1.f;
+        sm.ps.rnq[pt] = rq;
+        sm.ps.rnk[pt] = rk;
+        sm.ps.Mq[pt][pt] = p.scale * sqk * rq * rk;
+      }
+      prep_bar();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        qv[i] *= sm.ps.rnq[i];
+        kv[i] *= sm.ps.rnk[i];
+      }
+      float P[16], Rs[16];
+      P[0] = al[0];
+#pragma unroll
+      for (int i = 1; i < 16; ++i) P[i] = P[i - 1] * al[i];
+      Rs[15] = 1.f;
+#pragma unroll
+      for (int i = 14; i >= 0; --i) Rs[i] = Rs[i + 1] * al[i + 1];
+      {
+        PrepOut& po = sm.pout;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const __nv_bfloat16 qd = __float2bfloat16_rn(p.scale * qv[i] * P[i]);
+          po.qd[i][pt] = *reinterpret_cast<const uint16_t*>(&qd);
+          const typename ST2::T kr = ST2::cvt(kv[i] * Rs[i]);
+          po.kr[i][pt] = *reinterpret_cast<const uint16_t*>(&kr);
+          if (DELTA) {
+            sm.ps.kdec[i][pt] = QK::cvt(kv[i] * P[i]);
+            sm.ps.vs[i][pt] = __float2bfloat16_rn(vv[i]);
+          }
+        }
+        po.gamma[pt] = P[15];
+        if (!DELTA) {
+          float4* ut = reinterpret_cast<float4*>(&po.ut[pt][0]);
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) ut[i / 4] = make_float4(vv[i], vv[i + 1], vv[i + 2], vv[i + 3]);
+        }
+#pragma unroll
+        for (int lv = 0; lv < 4; ++lv) {
+          const int s = 8 >> lv;
+#pragma unroll
+          for (int blk = 0; blk < 8 / s; ++blk) {
+            const int m = blk * 2 * s + s;
+            float f = 1.f;
+#pragma unroll
+            for (int i = m; i < m + s; ++i) {
+              if (i > m) f *= al[i];
+              const int r = blk * s + (i - m);
+              if (DELTA) sm.ps.A_lv[lv][r][pt] = QK::cvt(kv[i] * f);
+              sm.ps.A_lv[lv][8 + r][pt] = QK::cvt(qv[i] * f);
+            }
+            f = 1.f;
+#pragma unroll
+            for (int i = m - 1; i >= m - s; --i) {
+              f *= al[i + 1];
+              sm.ps.B_lv[lv][blk * s + (i - (m - s))][pt] = QK::cvt(kv[i] * f);
+            }
+          }
+        }
+      }
+      prep_bar();
+      {  // level pw of the anchored split: L (rows 0-7) and Mqk (rows 8-15)
+        const int lv = pw;
+        const int s = 8 >> lv;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < FD / 16; ++kk) {
+          uint32_t a[4], b[2];
+          ldsm_x4(a, &sm.ps.A_lv[lv][lane & 15][16 * kk + (lane >> 4) * 8]);
+          ldsm_x2(b, &sm.ps.B_lv[lv][lane & 7][16 * kk + ((lane >> 3) & 1) * 8]);
+          mma16816<QK>(acc, a, b[0], b[1]);
+        }
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = g + ((e & 2) ? 8 : 0);
+          const int cidx = 2 * t + (e & 1);
+          const int rr = r & 7;
+          if (rr / s != cidx / s) continue;
+          const int i = row_tok_f(s, rr), jx = col_tok_f(s, cidx);
+          if (r < 8) {
+            if (DELTA) sm.ps.Lm[i][jx] = sm.ps.beta[i] * acc[e];
+          } else {
+            sm.ps.Mq[i][jx] = p.scale * acc[e];
+          }
+        }
+      }
+      prep_bar();
+      for (int e = pt; e < 256; e += 128) {
+        const typename ST2::T v = ST2::cvt(sm.ps.Mq[e >> 4][e & 15]);
+        sm.pout.mqk[e >> 4][e & 15] = *reinterpret_cast<const uint16_t*>(&v);
+      }
+      if (DELTA) {
+        if (pw == 0) {
+          float* X0 = &sm.ps.X[0][0][0];
+          float* X1 = &sm.ps.X[1][0][0];
+          float* X2 = &sm.ps.X[2][0][0];
+          float* X3 = &sm.ps.X[3][0][0];
+          for (int e = lane; e < 256; e += 32) X0[(e >> 4) * 17 + (e & 15)] = -sm.ps.Lm[e >> 4][e & 15];
+          __syncwarp();
+          warp_mm16_f<QK>(X0, false, X0, false, X1, lane);
+          warp_mm16_f<QK>(X1, false, X1, false, X2, lane);
+          warp_mm16_f<QK>(X0, true, X1, true, X3, lane);
+          warp_mm16_f<QK>(X2, false, X2, false, X0, lane);
+          warp_mm16_f<QK>(X3, false, X2, true, X1, lane);
+          warp_mm16_f<QK>(X1, false, X0, true, X3, lane);
+          for (int e = lane; e < 256; e += 32) {
+            const int i = e >> 4, jx = e & 15;
+            const float v = X3[i * 17 + jx] * sm.ps.beta[jx];
+            sm.ps.invq[i][jx] = QK::cvt(v);
+            const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+            sm.ps.invhi[i][jx] = hi;
+            sm.ps.invlo[i][jx] = __float2bfloat16_rn(v - __bfloat162float(hi));
+          }
+        }
+        prep_bar();
+        const int g = lane >> 2, t = lane & 3;
+        uint32_t a[4], ahi[4], alo[4];
+        ldsm_x4(a, &sm.ps.invq[lane & 15][(lane >> 4) * 8]);
+        ldsm_x4(ahi, &sm.ps.invhi[lane & 15][(lane >> 4) * 8]);
+        ldsm_x4(alo, &sm.ps.invlo[lane & 15][(lane >> 4) * 8]);
+#pragma unroll
+        for (int pp = 0; pp < 2; ++pp) {
+          const int n0 = pw * 32 + 16 * pp;
+          uint32_t b[4];
+          ldsm_x4_trans(b, &sm.ps.kdec[lane & 15][n0 + (lane >> 4) * 8]);
+          float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+          mma16816<QK>(c0, a, b[0], b[1]);
+          mma16816<QK>(c1, a, b[2], b[3]);
+          *reinterpret_cast<uint32_t*>(&sm.pout.W[g][n0 + 2 * t]) = Bf16::pack(-c0[0], -c0[1]);
+          *reinterpret_cast<uint32_t*>(&sm.pout.W[g + 8][n0 + 2 * t]) = Bf16::pack(-c0[2], -c0[3]);
+          *reinterpret_cast<uint32_t*>(&sm.pout.W[g][n0 + 8 + 2 * t]) = Bf16::pack(-c1[0], -c1[1]);
+          *reinterpret_cast<uint32_t*>(&sm.pout.W[g + 8][n0 + 8 + 2 * t]) = Bf16::pack(-c1[2], -c1[3]);
+          ldsm_x4_trans(b, &sm.ps.vs[lane & 15][n0 + (lane >> 4) * 8]);
+          float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};
+          mma16816<Bf16>(u0, ahi, b[0], b[1]);
+          mma16816<Bf16>(u0, alo, b[0], b[1]);
+          mma16816<Bf16>(u1, ahi, b[2], b[3]);
+          mma16816<Bf16>(u1, alo, b[2], b[3]);
+          sm.pout.ut[n0 + 2 * t][g] = u0[0];
+          sm.pout.ut[n0 + 2 * t + 1][g] = u0[1];
+          sm.pout.ut[n0 + 2 * t][g + 8] = u0[2];
+          sm.pout.ut[n0 + 2 * t + 1][g + 8] = u0[3];
+          sm.pout.ut[n0 + 8 + 2 * t][g] = u1[0];
+          sm.pout.ut[n0 + 8 + 2 * t + 1][g] = u1[1];
+          sm.pout.ut[n0 + 8 + 2 * t][g + 8] = u1[2];
+          sm.pout.ut[n0 + 8 + 2 * t + 1][g + 8] = u1[3];
+        }
+      }
+      fence_proxy_async_smem();  // make pout visible to the bulk-copy (async) proxy
+      prep_bar();
+      if (pt == 0) {
+        const int s = c & (kRing - 1);  // == rank
+        const int k = c / kRing;
+        if (k >= 1 && !failed &&
+            !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.empty[s])),
+                               static_cast<uint32_t>(k - 1) & 1u, kWaitLimitNs)) {
+          failed = true;
+          set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
+        }
+        const uint32_t src = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pout));
+        const uint32_t dst_local = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.ring[s]));
+        const uint32_t bar_local = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.full[s]));
+#pragma unroll
+        for (uint32_t r2 = 0; r2 < kCtas; ++r2) {
+          const uint32_t dst = mapa_shared(dst_local, r2);
+          const uint32_t bar = mapa_shared(bar_local, r2);
+          mbar_arrive_expect_tx_cluster(bar, kStageTx);
+          bulk_copy_s2s(dst, src, kSharedBytes, bar);
+          bulk_copy_s2s(dst + kSharedBytes, src + kSharedBytes + r2 * kUtSliceBytes, kUtSliceBytes, bar);
+        }
+        bulk_commit();
+      }
+    }
+    if (pt == 0) bulk_wait_read_all();
+  }
+  cluster_sync_all();
+}
+
+template <bool DELTA, bool L2N>
+cudaError_t launch_fused_t(const ChunkCall& c, cudaStream_t s) {
+  using QK = std::conditional_t<L2N, F16, Bf16>;
+  const size_t smem = sizeof(FusedSmem<typename QK::T>);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(kda_chunk_fused_kernel<DELTA, L2N>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const unsigned grid = static_cast<unsigned>(c.geo.N) * static_cast<unsigned>(c.geo.H) * kCtas;
+  if (grid == 0) return cudaSuccess;
+  kda_chunk_fused_kernel<DELTA, L2N><<<grid, kFusedThreads, smem, s>>>(c);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t fused_smem_bytes() { return sizeof(FusedSmem<__half>); }
+
+cudaError_t launch_chunk_fused(const ChunkCall& c, cudaStream_t s) {
+  if (c.dk != FD || c.dv != FD) return cudaErrorInvalidValue;
+  if (c.delta) return c.l2norm ? launch_fused_t<true, true>(c, s) : launch_fused_t<true, false>(c, s);
+  return c.l2norm ? launch_fused_t<false, true>(c, s) : launch_fused_t<false, false>(c, s);
+}
+
+}  // namespace kda

@@ -70,6 +70,8 @@ size_t record_bytes_f32(int dk, int dv);  // fp32 path
 cudaError_t launch_plan(const ChunkCall& c, cudaStream_t s);
 cudaError_t launch_chunk_tc(const ChunkCall& c, cudaStream_t s);
 cudaError_t launch_chunk_f32(const ChunkCall& c, cudaStream_t s);
+cudaError_t launch_chunk_fused(const ChunkCall& c, cudaStream_t s);  // bf16, dk = dv = 128
+size_t fused_smem_bytes();
 cudaError_t launch_decode(const DecodeCall& c, cudaStream_t s);
 
 }  // namespace kda

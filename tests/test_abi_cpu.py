@@ -96,15 +96,16 @@ def _fwd(lib, a, ws_ptr=FAKE, ws_bytes=1 << 40):
 
 def test_workspace_size_formula(lib):
     a = _chunk()
-    # header (N + 2 int32 rounded to 256) + ceil(100/16) chunks * H * record(128)
-    rec = 3 * 16 * 128 * 2 + 128 * 16 * 4 + 16 * 16 * 2 + 128 * 4
-    assert _ws(lib, a) == 256 + 7 * 2 * rec
+    # bf16 d=128 runs the fused kernel: only the varlen plan header (N + 2 int32, rounded to 256)
+    assert _ws(lib, a) == 256
+    assert _ws(lib, _chunk(cu_seqlens=FAKE, N=100)) == 512
+    # two-kernel path: header + ceil(100/16) chunks * H * record
     a.dk = a.dv = 64
     rec64 = 3 * 16 * 64 * 2 + 64 * 16 * 4 + 16 * 16 * 2 + 64 * 4
     assert _ws(lib, a) == 256 + 7 * 2 * rec64
     # varlen: one extra partial chunk per sequence at most
-    v = _chunk(cu_seqlens=FAKE, N=4)
-    assert _ws(lib, v) == 256 + (7 + 4) * 2 * rec
+    v = _chunk(cu_seqlens=FAKE, N=4, dk=64, dv=64)
+    assert _ws(lib, v) == 256 + (7 + 4) * 2 * rec64
     f = _chunk(dtype=_lib.KDA_DTYPE_FP32, dk=64, dv=128)
     recf = 3 * 16 * 64 * 4 + 128 * 16 * 4 + 16 * 16 * 4 + 64 * 4
     assert _ws(lib, f) == 256 + 7 * 2 * recf

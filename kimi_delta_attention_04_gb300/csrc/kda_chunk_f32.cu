@@ -301,14 +301,14 @@ __global__ void __launch_bounds__(kRecThreads32) kda_recur_f32_kernel(const Chun
     {
       float u = sm.ut[j][i];
       if (DELTA) {
-        for (int c = 0; c < DK; ++c) u = fmaf(sm.W[i][c], sm.S[c][j], u);
+        for (int kc = 0; kc < DK; ++kc) u = fmaf(sm.W[i][kc], sm.S[kc][j], u);
       }
       sm.U[i][j] = u;
     }
     __syncthreads();
     {
       float o = 0.f;
-      for (int c = 0; c < DK; ++c) o = fmaf(sm.qd[i][c], sm.S[c][j], o);
+      for (int kc = 0; kc < DK; ++kc) o = fmaf(sm.qd[i][kc], sm.S[kc][j], o);
       for (int m = 0; m <= i; ++m) o = fmaf(sm.mqk[i][m], sm.U[m][j], o);
       const int tok = ts + c * kChunk + i;
       if (tok < te) reinterpret_cast<float*>(p.o)[(static_cast<size_t>(tok) * H + h) * DV + dv0 + j] = o;

@@ -36,7 +36,7 @@ constexpr int FD = 128;              // dk = dv
 constexpr int kCtas = 4;             // cluster size
 constexpr int kRows = FD / kCtas;    // value rows per CTA
 constexpr int kRing = 4;             // ring stages (= cluster size: stage s is produced by CTA s)
-constexpr int kFusedThreads = 256;   // 4 recurrence warps + 4 prep warps
+constexpr int kFusedThreads = 288;   // 4 recurrence warps + 4 prep warps + 1 mover warp
 constexpr int kPad = FD + 8;         // padded 16-bit row (conflict-free ldmatrix)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -76,12 +76,8 @@ struct __align__(16) PrepScratch {
   Q B_lv[4][8][kPad];
   Q kdec[16][kPad];
   __nv_bfloat16 vs[16][kPad];
-  Q invq[16][24];
-  __nv_bfloat16 invhi[16][24];
-  __nv_bfloat16 invlo[16][24];
   float Lm[16][17];
   float Mq[16][17];
-  float X[4][16][17];
   float red[4][48];
   float rnq[16], rnk[16], beta[16];
 };
@@ -94,49 +90,23 @@ struct __align__(16) RecScratch {
 template <typename Q>
 struct __align__(128) FusedSmem {
   Stage ring[kRing];
-  PrepOut pout;
+  PrepOut pout[2];
   PrepIn pin[2];
   PrepScratch<Q> ps;
   RecScratch rs;
   uint64_t full[kRing];
   uint64_t empty[kRing];
+  uint64_t pfull[2];   // prep output buffer b written (prep -> mover)
+  uint64_t pempty[2];  // prep output buffer b read by the pushes (mover -> prep)
   int failed;
 };
 
 __device__ __forceinline__ int row_tok_f(int s, int r) { return (r / s) * 2 * s + s + (r % s); }
 __device__ __forceinline__ int col_tok_f(int s, int r) { return (r / s) * 2 * s + (r % s); }
 
-template <typename Op>
-__device__ __forceinline__ void warp_mm16_f(const float* A, bool addIA, const float* B, bool addIB, float* C,
-                                            int lane) {
-  const int g = lane >> 2, t = lane & 3;
-  auto ea = [&](int r, int c) { return A[r * 17 + c] + ((addIA && r == c) ? 1.f : 0.f); };
-  auto eb = [&](int r, int c) { return B[r * 17 + c] + ((addIB && r == c) ? 1.f : 0.f); };
-  uint32_t a[4];
-  a[0] = Op::pack(ea(g, 2 * t), ea(g, 2 * t + 1));
-  a[1] = Op::pack(ea(g + 8, 2 * t), ea(g + 8, 2 * t + 1));
-  a[2] = Op::pack(ea(g, 2 * t + 8), ea(g, 2 * t + 9));
-  a[3] = Op::pack(ea(g + 8, 2 * t + 8), ea(g + 8, 2 * t + 9));
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt) {
-    const int n = 8 * nt + g;
-    const uint32_t b0 = Op::pack(eb(2 * t, n), eb(2 * t + 1, n));
-    const uint32_t b1 = Op::pack(eb(2 * t + 8, n), eb(2 * t + 9, n));
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
-    mma16816<Op>(c, a, b0, b1);
-    const int col = 8 * nt + 2 * t;
-    C[g * 17 + col] = c[0];
-    C[g * 17 + col + 1] = c[1];
-    C[(g + 8) * 17 + col] = c[2];
-    C[(g + 8) * 17 + col + 1] = c[3];
-  }
-  __syncwarp();
-}
-
 // Issue the loads of one chunk's inputs into a PrepIn buffer (prep threads).
 __device__ __forceinline__ void prefetch_inputs(const ChunkCall& p, PrepIn& in, int h, int tok0, int ntok, int pt) {
   const int H = p.geo.H;
-  const size_t rs = static_cast<size_t>(H) * FD;
   // q, k, v: 16 rows x 16 vectors of 16 B each
   for (int i = pt; i < 3 * 16 * 16; i += 128) {
     const int which = i >> 8, row = (i >> 4) & 15, vec = i & 15;
@@ -183,6 +153,10 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], kCtas * 4);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.pfull[b], 1);
+      mbar_init(&sm.pempty[b], 1);
     }
     sm.failed = 0;
     fence_mbarrier_init_cluster();
@@ -240,14 +214,25 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       }
       const int brow = ((lane >> 4) << 3) + (lane & 7);
       const int bcol = ((lane >> 3) & 1) * 8;
+      if (DELTA) {  // U first: it is on the serial path; two chains per n-tile
+        float u2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        uint32_t b[4][4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) ldsm_x4(b[kk], &st.W[brow][kc0 + 16 * kk + bcol]);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          float (&acc)[2][4] = (kk & 1) ? u2 : u;
+          mma16816<Bf16>(acc[0], sa[kk], b[kk][0], b[kk][1]);
+          mma16816<Bf16>(acc[1], sa[kk], b[kk][2], b[kk][3]);
+        }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) u[nt][e] += u2[nt][e];
+      }
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         uint32_t b[4];
-        if (DELTA) {
-          ldsm_x4(b, &st.W[brow][kc0 + 16 * kk + bcol]);
-          mma16816<Bf16>(u[0], sa[kk], b[0], b[1]);
-          mma16816<Bf16>(u[1], sa[kk], b[2], b[3]);
-        }
         ldsm_x4(b, &st.qd[brow][kc0 + 16 * kk + bcol]);
         mma16816<Bf16>(o[0], sa[kk], b[0], b[1]);
         mma16816<Bf16>(o[1], sa[kk], b[2], b[3]);
@@ -330,7 +315,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
             make_float2(S[nt][2], S[nt][3]);
       }
     }
-  } else {
+  } else if (warp < 8) {
     // ===================== prep warps =====================
     const int pt = tid - 128;  // key / value channel owned by this thread
     const int pw = pt >> 5;    // prep warp index 0..3
@@ -339,16 +324,15 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     const float dtb = (p.gate_mode == 2) ? p.dt_bias[h * FD + pt] : 0.f;
     bool failed = false;
     int c = static_cast<int>(rank);
+    // beta is loaded raw one producer step ahead; its sigmoid is taken when it
+    // is stored, so the load latency never sits on the prep's critical path.
     float beta_next = 0.f;
     auto load_beta = [&](int cc) {
-      float bt = 0.f;
+      float raw = 0.f;
       const int tk0 = ts + cc * kChunk;
-      if (DELTA && pt < 16 && tk0 + pt < te) {
-        const float raw = __bfloat162float(
-            reinterpret_cast<const __nv_bfloat16*>(p.beta)[static_cast<size_t>(tk0 + pt) * H + h]);
-        bt = (p.beta_mode == 1) ? sigmoid_f(raw) : raw;
-      }
-      return bt;
+      if (DELTA && pt < 16 && tk0 + pt < te)
+        raw = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.beta)[static_cast<size_t>(tk0 + pt) * H + h]);
+      return raw;
     };
     if (c < nch) {
       prefetch_inputs(p, sm.pin[0], h, ts + c * kChunk, min(kChunk, te - (ts + c * kChunk)), pt);
@@ -369,12 +353,21 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       } else {
         cp_async_wait<0>();
       }
-      if (pt == 0) bulk_wait_read_all();  // the previous push has finished reading pout
+      PrepOut& po = sm.pout[buf];
+      if (j >= 2 && pt == 0 && !failed &&
+          !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pempty[buf])),
+                             static_cast<uint32_t>((j >> 1) - 1) & 1u, kWaitLimitNs)) {
+        failed = true;  // the pushes of chunk c - 8 have not read this buffer yet
+        set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
+      }
       for (int i = pt; i < 16 * 17; i += 128) {
         (&sm.ps.Lm[0][0])[i] = 0.f;
         (&sm.ps.Mq[0][0])[i] = 0.f;
       }
-      if (pt < 16) sm.ps.beta[pt] = beta_cur;
+      if (pt < 16) {
+        const float bt = (p.beta_mode == 1) ? sigmoid_f(beta_cur) : beta_cur;
+        sm.ps.beta[pt] = (DELTA && pt < ntok) ? bt : 0.f;
+      }
       prep_bar();
       const PrepIn& in = sm.pin[buf];
       float qv[16], kv[16], al[16], vv[16];
@@ -383,16 +376,26 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         qv[i] = __bfloat162float(in.q[i][pt]);
         kv[i] = __bfloat162float(in.k[i][pt]);
         vv[i] = __bfloat162float(in.v[i][pt]);
-        float a = 1.f;
-        if (i < ntok) {
-          if (p.gate_mode == 1) a = __expf(in.a[i][pt]);
-          else if (p.gate_mode == 2) {
-            const float x = in.a[i][pt] + dtb;
-            const float sp = x <= 20.f ? __logf(1.f + __expf(x)) : x;
-            a = __expf(-Aexp * sp);
-          }
+      }
+      // One branch for the gate mode around the whole token loop, so the 16
+      // independent exp/log chains interleave; padded tokens select alpha = 1.
+      if (p.gate_mode == 2) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float x = in.a[i][pt] + dtb;
+          const float sp = x <= 20.f ? __logf(1.f + __expf(x)) : x;
+          const float a = __expf(-Aexp * sp);
+          al[i] = i < ntok ? a : 1.f;
         }
-        al[i] = a;
+      } else if (p.gate_mode == 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a = __expf(in.a[i][pt]);
+          al[i] = i < ntok ? a : 1.f;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) al[i] = 1.f;
       }
       {
         float red[16];
@@ -441,7 +444,6 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
 #pragma unroll
       for (int i = 14; i >= 0; --i) Rs[i] = Rs[i + 1] * al[i + 1];
       {
-        PrepOut& po = sm.pout;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const __nv_bfloat16 qd = __float2bfloat16_rn(p.scale * qv[i] * P[i]);
@@ -512,37 +514,26 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       prep_bar();
       for (int e = pt; e < 256; e += 128) {
         const typename ST2::T v = ST2::cvt(sm.ps.Mq[e >> 4][e & 15]);
-        sm.pout.mqk[e >> 4][e & 15] = *reinterpret_cast<const uint16_t*>(&v);
+        po.mqk[e >> 4][e & 15] = *reinterpret_cast<const uint16_t*>(&v);
       }
       if (DELTA) {
-        if (pw == 0) {
-          float* X0 = &sm.ps.X[0][0][0];
-          float* X1 = &sm.ps.X[1][0][0];
-          float* X2 = &sm.ps.X[2][0][0];
-          float* X3 = &sm.ps.X[3][0][0];
-          for (int e = lane; e < 256; e += 32) X0[(e >> 4) * 17 + (e & 15)] = -sm.ps.Lm[e >> 4][e & 15];
-          __syncwarp();
-          warp_mm16_f<QK>(X0, false, X0, false, X1, lane);
-          warp_mm16_f<QK>(X1, false, X1, false, X2, lane);
-          warp_mm16_f<QK>(X0, true, X1, true, X3, lane);
-          warp_mm16_f<QK>(X2, false, X2, false, X0, lane);
-          warp_mm16_f<QK>(X3, false, X2, true, X1, lane);
-          warp_mm16_f<QK>(X1, false, X0, true, X3, lane);
-          for (int e = lane; e < 256; e += 32) {
-            const int i = e >> 4, jx = e & 15;
-            const float v = X3[i * 17 + jx] * sm.ps.beta[jx];
-            sm.ps.invq[i][jx] = QK::cvt(v);
-            const __nv_bfloat16 hi = __float2bfloat16_rn(v);
-            sm.ps.invhi[i][jx] = hi;
-            sm.ps.invlo[i][jx] = __float2bfloat16_rn(v - __bfloat162float(hi));
-          }
-        }
-        prep_bar();
+        // every prep warp forms INV' = (I + L)^{-1} diag(beta) in registers
         const int g = lane >> 2, t = lane & 3;
+        Frag16 inv = neumann_inverse16<QK>(&sm.ps.Lm[0][0], 17, lane);
+        Frag16 ihi, ilo;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float v = inv.c[nt][e] * sm.ps.beta[8 * nt + 2 * t + (e & 1)];
+            inv.c[nt][e] = v;
+            ihi.c[nt][e] = __bfloat162float(__float2bfloat16_rn(v));
+            ilo.c[nt][e] = v - ihi.c[nt][e];
+          }
         uint32_t a[4], ahi[4], alo[4];
-        ldsm_x4(a, &sm.ps.invq[lane & 15][(lane >> 4) * 8]);
-        ldsm_x4(ahi, &sm.ps.invhi[lane & 15][(lane >> 4) * 8]);
-        ldsm_x4(alo, &sm.ps.invlo[lane & 15][(lane >> 4) * 8]);
+        frag_as_a<QK>(inv, a);
+        frag_as_a<Bf16>(ihi, ahi);
+        frag_as_a<Bf16>(ilo, alo);
 #pragma unroll
         for (int pp = 0; pp < 2; ++pp) {
           const int n0 = pw * 32 + 16 * pp;
@@ -551,40 +542,53 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
           mma16816<QK>(c0, a, b[0], b[1]);
           mma16816<QK>(c1, a, b[2], b[3]);
-          *reinterpret_cast<uint32_t*>(&sm.pout.W[g][n0 + 2 * t]) = Bf16::pack(-c0[0], -c0[1]);
-          *reinterpret_cast<uint32_t*>(&sm.pout.W[g + 8][n0 + 2 * t]) = Bf16::pack(-c0[2], -c0[3]);
-          *reinterpret_cast<uint32_t*>(&sm.pout.W[g][n0 + 8 + 2 * t]) = Bf16::pack(-c1[0], -c1[1]);
-          *reinterpret_cast<uint32_t*>(&sm.pout.W[g + 8][n0 + 8 + 2 * t]) = Bf16::pack(-c1[2], -c1[3]);
+          *reinterpret_cast<uint32_t*>(&po.W[g][n0 + 2 * t]) = Bf16::pack(-c0[0], -c0[1]);
+          *reinterpret_cast<uint32_t*>(&po.W[g + 8][n0 + 2 * t]) = Bf16::pack(-c0[2], -c0[3]);
+          *reinterpret_cast<uint32_t*>(&po.W[g][n0 + 8 + 2 * t]) = Bf16::pack(-c1[0], -c1[1]);
+          *reinterpret_cast<uint32_t*>(&po.W[g + 8][n0 + 8 + 2 * t]) = Bf16::pack(-c1[2], -c1[3]);
           ldsm_x4_trans(b, &sm.ps.vs[lane & 15][n0 + (lane >> 4) * 8]);
           float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};
           mma16816<Bf16>(u0, ahi, b[0], b[1]);
           mma16816<Bf16>(u0, alo, b[0], b[1]);
           mma16816<Bf16>(u1, ahi, b[2], b[3]);
           mma16816<Bf16>(u1, alo, b[2], b[3]);
-          sm.pout.ut[n0 + 2 * t][g] = u0[0];
-          sm.pout.ut[n0 + 2 * t + 1][g] = u0[1];
-          sm.pout.ut[n0 + 2 * t][g + 8] = u0[2];
-          sm.pout.ut[n0 + 2 * t + 1][g + 8] = u0[3];
-          sm.pout.ut[n0 + 8 + 2 * t][g] = u1[0];
-          sm.pout.ut[n0 + 8 + 2 * t + 1][g] = u1[1];
-          sm.pout.ut[n0 + 8 + 2 * t][g + 8] = u1[2];
-          sm.pout.ut[n0 + 8 + 2 * t + 1][g + 8] = u1[3];
+          po.ut[n0 + 2 * t][g] = u0[0];
+          po.ut[n0 + 2 * t + 1][g] = u0[1];
+          po.ut[n0 + 2 * t][g + 8] = u0[2];
+          po.ut[n0 + 2 * t + 1][g + 8] = u0[3];
+          po.ut[n0 + 8 + 2 * t][g] = u1[0];
+          po.ut[n0 + 8 + 2 * t + 1][g] = u1[1];
+          po.ut[n0 + 8 + 2 * t][g + 8] = u1[2];
+          po.ut[n0 + 8 + 2 * t + 1][g + 8] = u1[3];
         }
       }
-      fence_proxy_async_smem();  // make pout visible to the bulk-copy (async) proxy
+      fence_proxy_async_smem();  // make po visible to the bulk-copy (async) proxy
       prep_bar();
-      if (pt == 0) {
-        const int s = c & (kRing - 1);  // == rank
-        const int k = c / kRing;
-        if (k >= 1 && !failed &&
-            !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.empty[s])),
-                               static_cast<uint32_t>(k - 1) & 1u, kWaitLimitNs)) {
+      if (pt == 0) mbar_arrive_local(&sm.pfull[buf]);
+    }
+  } else {
+    // ===================== mover warp =====================
+    // Pushes each prepared chunk into stage (c mod 4) of all four CTAs once the
+    // consumers have released that stage, so prep never blocks on the ring.
+    if (lane == 0) {
+      bool failed = false;
+      const uint32_t s = rank;  // every chunk this CTA prepares goes to stage rank
+      const uint32_t dst_local = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.ring[s]));
+      const uint32_t bar_local = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.full[s]));
+      for (int j = 0, c = static_cast<int>(rank); c < nch; ++j, c += kCtas) {
+        const int b = j & 1;
+        if (!failed && !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pfull[b])),
+                                          static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs)) {
           failed = true;
           set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
         }
-        const uint32_t src = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pout));
-        const uint32_t dst_local = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.ring[s]));
-        const uint32_t bar_local = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.full[s]));
+        if (j >= 1 && !failed &&
+            !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.empty[s])),
+                               static_cast<uint32_t>(j - 1) & 1u, kWaitLimitNs)) {
+          failed = true;
+          set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
+        }
+        const uint32_t src = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pout[b]));
 #pragma unroll
         for (uint32_t r2 = 0; r2 < kCtas; ++r2) {
           const uint32_t dst = mapa_shared(dst_local, r2);
@@ -594,9 +598,11 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           bulk_copy_s2s(dst + kSharedBytes, src + kSharedBytes + r2 * kUtSliceBytes, kUtSliceBytes, bar);
         }
         bulk_commit();
+        bulk_wait_read_all();
+        mbar_arrive_local(&sm.pempty[b]);
       }
     }
-    if (pt == 0) bulk_wait_read_all();
+    __syncwarp();
   }
   cluster_sync_all();
 }

@@ -37,16 +37,25 @@ __device__ __forceinline__ void fence_mbarrier_init_cluster() {
 
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
+// Tests the phase; if it is not complete the thread may be suspended (not
+// spinning, so it frees issue slots) for up to ~20 us or until completion.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n"
-      " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(20000u)
       : "memory");
   return ok != 0;
+}
+
+// Local (CTA-scope) arrive on an mbarrier of this CTA.
+__device__ __forceinline__ void mbar_arrive_local(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(bar)))
+               : "memory");
 }
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
@@ -66,14 +75,17 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   return true;
 }
 
-// Arrive (release, cluster scope) on an mbarrier of any CTA of the cluster.
+// Arrive on an mbarrier of any CTA of the cluster. Default (release, CTA scope)
+// semantics: the data a phase guards moves through the async proxy and is
+// ordered by the transaction count, so no cluster-scope fence is needed here
+// (a cluster-scope release costs thousands of cycles per arrive).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
 // Arrive and add `bytes` to the expected transaction count of a cluster mbarrier.
 __device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar),
+  asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar),
                "r"(bytes)
                : "memory");
 }

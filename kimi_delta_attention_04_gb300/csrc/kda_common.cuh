@@ -141,6 +141,84 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// ---------------------------------------------------------------------------
+// 16x16 matrices held in registers in the mma.sync accumulator layout
+// ---------------------------------------------------------------------------
+// c[nt][e] = M[g + 8 (e >> 1)][8 nt + 2 t + (e & 1)], g = lane / 4, t = lane % 4.
+struct Frag16 {
+  float c[2][4];
+};
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+
+// A-operand fragments (m16 x k16) of M: the accumulator layout of two adjacent
+// n-tiles is exactly the A layout.
+template <typename Op>
+__device__ __forceinline__ void frag_as_a(const Frag16& m, uint32_t (&a)[4]) {
+  a[0] = Op::pack(m.c[0][0], m.c[0][1]);
+  a[1] = Op::pack(m.c[0][2], m.c[0][3]);
+  a[2] = Op::pack(m.c[1][0], m.c[1][1]);
+  a[3] = Op::pack(m.c[1][2], m.c[1][3]);
+}
+
+// B-operand fragments (k16 x n8, k = row of M) for both n-tiles: each packed
+// 8x8 block of the accumulator layout is transposed in registers.
+template <typename Op>
+__device__ __forceinline__ void frag_as_b(const Frag16& m, uint32_t (&b)[2][2]) {
+  b[0][0] = movmatrix_trans(Op::pack(m.c[0][0], m.c[0][1]));  // rows 0-7,  cols 0-7
+  b[0][1] = movmatrix_trans(Op::pack(m.c[0][2], m.c[0][3]));  // rows 8-15, cols 0-7
+  b[1][0] = movmatrix_trans(Op::pack(m.c[1][0], m.c[1][1]));  // rows 0-7,  cols 8-15
+  b[1][1] = movmatrix_trans(Op::pack(m.c[1][2], m.c[1][3]));  // rows 8-15, cols 8-15
+}
+
+template <typename Op>
+__device__ __forceinline__ Frag16 frag_mm(const Frag16& A, const Frag16& B) {
+  uint32_t a[4], b[2][2];
+  frag_as_a<Op>(A, a);
+  frag_as_b<Op>(B, b);
+  Frag16 C;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    C.c[nt][0] = C.c[nt][1] = C.c[nt][2] = C.c[nt][3] = 0.f;
+    mma16816<Op>(C.c[nt], a, b[nt][0], b[nt][1]);
+  }
+  return C;
+}
+
+__device__ __forceinline__ Frag16 frag_plus_identity(Frag16 m, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if ((e >> 1) == nt && g == 2 * t + (e & 1)) m.c[nt][e] += 1.f;
+  return m;
+}
+
+// (I + L)^{-1} for a strictly lower-triangular 16x16 L (row stride `ld` floats in
+// shared memory): the Neumann series of X = -L, which is exact because L^16 = 0,
+// summed as (I + X)(I + X^2)(I + X^4)(I + X^8). Independent products are paired
+// so the dependent chain is four products deep. One warp; operands rounded to Op.
+template <typename Op>
+__device__ __forceinline__ Frag16 neumann_inverse16(const float* L, int ld, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  Frag16 X;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) X.c[nt][e] = -L[(g + 8 * (e >> 1)) * ld + 8 * nt + 2 * t + (e & 1)];
+  const Frag16 X2 = frag_mm<Op>(X, X);
+  const Frag16 X4 = frag_mm<Op>(X2, X2);
+  const Frag16 P1 = frag_mm<Op>(frag_plus_identity(X, lane), frag_plus_identity(X2, lane));
+  const Frag16 X8 = frag_mm<Op>(X4, X4);
+  const Frag16 P2 = frag_mm<Op>(P1, frag_plus_identity(X4, lane));
+  return frag_mm<Op>(P2, frag_plus_identity(X8, lane));
+}
+
 // softplus with the usual linear branch above 20 (the two differ by < 2.1e-9 there).
 __device__ __forceinline__ float softplus_f(float x) { return x <= 20.f ? log1pf(expf(x)) : x; }
 

@@ -5,6 +5,7 @@
  *   kda_chunk_fwd             chunkwise KDA forward over one batch of sequences
  *   kda_chunk_workspace_size  scratch bytes kda_chunk_fwd needs for given arguments
  *   kda_decode_step           fused T=1 decode step on a packed q|k|v row with a slot pool
+ *   kda_chunk_fwd_noalloc     kda_chunk_fwd on a library-owned scratch buffer (no allocation)
  *   kda_version               library version string
  *
  * What is computed (per sequence n and head h; math state S is [dk, dv], stored
@@ -53,7 +54,8 @@ typedef enum {
   KDA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, bad index array */
   KDA_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement (e.g. dk = 96) */
   KDA_ERR_CUDA = 3,         /* a CUDA launch or runtime call failed */
-  KDA_ERR_TIMEOUT = 4       /* a bounded device-side wait expired (reported through err) */
+  KDA_ERR_TIMEOUT = 4,      /* a bounded device-side wait expired (reported through err) */
+  KDA_ERR_TOO_LARGE = 5     /* needs more scratch than kda_chunk_fwd_noalloc's fixed buffer */
 } kda_status;
 
 typedef enum {
@@ -178,6 +180,40 @@ typedef struct kda_decode_args {
 
 /* Fused T=1 decode step. Returns KDA_OK once the work is enqueued. */
 kda_status kda_decode_step(const kda_decode_args* args, kda_stream_t stream);
+
+/*
+ * Chunk forward for callers that cannot allocate device memory.
+ *
+ * No counterpart in the method's description: this is a deployment aid. Some
+ * callers may not call cudaMalloc (or any allocating routine) at the point
+ * where they run the attention: code recording a CUDA graph or replaying a
+ * fixed memory plan, runtimes that hand out every device byte at start-up and
+ * forbid allocation afterwards, and bindings with no device allocator of their
+ * own. kda_chunk_fwd needs a caller-provided workspace; this entry point uses
+ * instead a scratch buffer of KDA_NOALLOC_SCRATCH_BYTES that the library owns:
+ * a file-scope __device__ array, present on every GPU that loads the library
+ * until the process exits.
+ *
+ * Arguments and results are those of kda_chunk_fwd; inputs and outputs are
+ * still caller-owned device memory. The call allocates nothing (no cudaMalloc,
+ * no cudaFree, no allocating library routine).
+ *
+ * Returns KDA_ERR_TOO_LARGE, launching nothing, when the arguments need more
+ * than KDA_NOALLOC_SCRATCH_BYTES of scratch (kda_chunk_workspace_size(args)
+ * tells how much they need; bf16 with dk = dv = 128 needs only a small
+ * per-sequence header). Other argument errors as for kda_chunk_fwd.
+ *
+ * The first call on each device looks up the address of the device's copy of
+ * the buffer (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture. Later calls only read the cached address.
+ * The buffer's contents on entry do not matter (every byte a call reads is
+ * written earlier in the same call), and it keeps the last call's contents.
+ * All calls on a device share the one buffer: calls whose GPU work overlaps
+ * (different streams, or other threads) race and corrupt each other; order
+ * them on one stream or synchronise between them.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20) /* 16 MiB */
+kda_status kda_chunk_fwd_noalloc(const kda_chunk_args* args, kda_stream_t stream);
 
 /* Version string of the library, e.g. "kda-gb300 0.1.0 sm_103a". */
 const char* kda_version(void);

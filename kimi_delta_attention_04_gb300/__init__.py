@@ -10,6 +10,7 @@ from ._lib import (  # noqa: F401
     KdaError,
     chunk_workspace_size,
     kda_chunk_fwd,
+    kda_chunk_fwd_noalloc,
     kda_decode_step,
     lib_path,
     load,

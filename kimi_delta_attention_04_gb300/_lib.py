@@ -23,8 +23,10 @@ KDA_ERR_INVALID_ARG = 1
 KDA_ERR_UNSUPPORTED = 2
 KDA_ERR_CUDA = 3
 KDA_ERR_TIMEOUT = 4
+KDA_ERR_TOO_LARGE = 5
 STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_CUDA",
-                4: "KDA_ERR_TIMEOUT"}
+                4: "KDA_ERR_TIMEOUT", 5: "KDA_ERR_TOO_LARGE"}
+KDA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 KDA_DTYPE_BF16 = 0
 KDA_DTYPE_FP32 = 1
@@ -64,7 +66,8 @@ class DecodeArgs(ctypes.Structure):
     ]
 
 
-EXPORTS = ("kda_chunk_fwd", "kda_chunk_workspace_size", "kda_decode_step", "kda_version")
+EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_chunk_workspace_size", "kda_decode_step",
+           "kda_version")
 
 
 def lib_path() -> Path:
@@ -88,6 +91,8 @@ def load() -> ctypes.CDLL:
         lib.kda_chunk_workspace_size.argtypes = [ctypes.POINTER(ChunkArgs)]
         lib.kda_decode_step.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
+        lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
+        lib.kda_chunk_fwd_noalloc.argtypes = [ctypes.POINTER(ChunkArgs), ctypes.c_void_p]
         lib.kda_version.restype = ctypes.c_char_p
         lib.kda_version.argtypes = []
         _lib = lib
@@ -191,6 +196,30 @@ def kda_chunk_fwd(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None, b
     st = lib.kda_chunk_fwd(ctypes.byref(args), ctypes.c_void_p(_ptr(workspace)), need, _stream_ptr(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_chunk_fwd")
+    return o, hT
+
+
+def kda_chunk_fwd_noalloc(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None, beta=None, b=None,
+                          h0=None, cu_seqlens=None, l2norm_qk=False, delta=True, o=None, hT=None,
+                          output_final_state=True, err=None, stream=None):
+    """kda_chunk_fwd on the library's own scratch buffer: the C call allocates
+    nothing (for callers that may not allocate device memory; see
+    include/kda.h). Outputs o / hT are allocated here with torch unless given.
+    Raises KdaError(KDA_ERR_TOO_LARGE) when the request needs more than
+    KDA_NOALLOC_SCRATCH_BYTES of scratch."""
+    lib = load()
+    B, T, H, _ = q.shape
+    if o is None:
+        o = torch.empty(B, T, H, v.shape[-1], dtype=q.dtype, device=q.device)
+    N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else B
+    if hT is None and output_final_state:
+        hT = torch.empty(N, H, v.shape[-1], q.shape[-1], dtype=torch.float32, device=q.device)
+    args = make_chunk_args(q, k, v, scale=scale, g=g, a=a, dt_bias=dt_bias, A_log=A_log, beta=beta, b=b,
+                           h0=h0, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk, delta=delta, o=o, hT=hT,
+                           err=err)
+    st = lib.kda_chunk_fwd_noalloc(ctypes.byref(args), _stream_ptr(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_fwd_noalloc")
     return o, hT
 
 

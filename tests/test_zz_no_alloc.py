@@ -1,0 +1,81 @@
+"""kda_chunk_fwd_noalloc: the chunk forward on the library's own scratch buffer.
+
+Callers that may not allocate device memory when they run attention (graph
+recording or a fixed memory plan, runtimes that own every device byte, bindings
+without an allocator) use this entry point instead of kda_chunk_fwd with a
+workspace. These tests call it through the C ABI (via the ctypes binding) and
+check, on two calls in a row, that it gives what kda_chunk_fwd gives, within
+the tolerances of the parity tests. The file is named so that pytest collects
+it last; it also passes on its own in a fresh process.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import kimi_delta_attention_04_gb300 as kda
+from kimi_delta_attention_04_gb300 import _lib
+from kimi_delta_attention_04_gb300 import workloads as W
+
+from kda_cases import BF16_MAX_ABS, BF16_REL_F, FP32_MAX_ABS, max_abs, np64, rel_f, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from kimi_delta_attention_04_gb300 import build
+    build.build()
+    kda.load()
+
+
+def _kwargs(d):
+    return dict(scale=d["scale"], g=d["g"], a=d["a"], dt_bias=d["dt_bias"], A_log=d["A_log"], beta=d["beta"],
+                b=d["b"], h0=d["h0"], cu_seqlens=d["cu_seqlens"], l2norm_qk=d["l2norm"], delta=d["delta"])
+
+
+def _close(x, ref, dtype):
+    x, ref = np64(x), np64(ref)
+    if dtype == torch.float32:
+        assert max_abs(x, ref) <= FP32_MAX_ABS
+    else:
+        assert rel_f(x, ref) <= BF16_REL_F and max_abs(x, ref) <= BF16_MAX_ABS
+
+
+CASES = {
+    "fp32_gate_inputs": lambda: W.fp32_small(),
+    "fp32_d64x128_ragged": lambda: W.chunk_workload(seed=101, B=2, T=77, H=2, K=64, V=128, dtype=torch.float32,
+                                                    h0_std=0.1),
+    "bf16_d64": lambda: W.chunk_workload(seed=102, B=3, T=90, H=2, K=64, V=64),
+    "bf16_d128_varlen": lambda: W.chunk_workload(seed=103, lengths=[40, 0, 130, 17], H=3),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_noalloc_matches_workspace_entry_point(name):
+    wl = CASES[name]()
+    d = to_dev(wl)
+    o_ref, h_ref = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], **_kwargs(d))
+    torch.cuda.synchronize()
+    for _ in range(2):  # two calls in a row share (and reuse) the one scratch buffer
+        o, h = kda.kda_chunk_fwd_noalloc(d["q"], d["k"], d["v"], **_kwargs(d))
+        torch.cuda.synchronize()
+        _close(o, o_ref, wl["dtype"])
+        _close(h, h_ref, wl["dtype"])
+        assert torch.isfinite(o.float()).all()
+
+
+def test_noalloc_rejects_requests_beyond_its_buffer():
+    lib = _lib.load()
+    a = _lib.ChunkArgs()
+    # fp32, dk = dv = 128, 8 heads, 8192 tokens: far more than 16 MiB of records
+    a.dtype, a.B, a.T, a.H, a.dk, a.dv, a.N = _lib.KDA_DTYPE_FP32, 1, 8192, 8, 128, 128, 1
+    a.gate_mode, a.beta_mode, a.flags, a.scale = _lib.KDA_GATE_NONE, _lib.KDA_BETA_VALUES, 0, 1.0
+    fake = 0x10000  # never dereferenced: the request is refused before any launch
+    a.q = a.k = a.v = a.beta = a.o = fake
+    assert lib.kda_chunk_workspace_size(ctypes.byref(a)) > _lib.KDA_NOALLOC_SCRATCH_BYTES
+    assert lib.kda_chunk_fwd_noalloc(ctypes.byref(a), None) == _lib.KDA_ERR_TOO_LARGE
+    a.q = None  # argument errors still come back as for kda_chunk_fwd
+    assert lib.kda_chunk_fwd_noalloc(ctypes.byref(a), None) == _lib.KDA_ERR_INVALID_ARG

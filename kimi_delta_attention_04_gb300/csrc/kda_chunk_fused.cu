@@ -28,6 +28,7 @@
 
 #include "kda_cluster.cuh"
 #include "kda_common.cuh"
+#include "kda_tma.h"
 
 namespace kda {
 namespace {
@@ -96,6 +97,7 @@ struct __align__(128) FusedSmem {
   RecScratch rs;
   uint64_t full[kRing];
   uint64_t empty[kRing];
+  uint64_t pinbar[2];  // input tile buffer b loaded (TMA -> prep)
   uint64_t pfull[2];   // prep output buffer b written (prep -> mover)
   uint64_t pempty[2];  // prep output buffer b read by the pushes (mover -> prep)
   int failed;
@@ -104,34 +106,23 @@ struct __align__(128) FusedSmem {
 __device__ __forceinline__ int row_tok_f(int s, int r) { return (r / s) * 2 * s + s + (r % s); }
 __device__ __forceinline__ int col_tok_f(int s, int r) { return (r / s) * 2 * s + (r % s); }
 
-// Issue the loads of one chunk's inputs into a PrepIn buffer (prep threads).
-__device__ __forceinline__ void prefetch_inputs(const ChunkCall& p, PrepIn& in, int h, int tok0, int ntok, int pt) {
-  const int H = p.geo.H;
-  // q, k, v: 16 rows x 16 vectors of 16 B each
-  for (int i = pt; i < 3 * 16 * 16; i += 128) {
-    const int which = i >> 8, row = (i >> 4) & 15, vec = i & 15;
-    const __nv_bfloat16* src = which == 0 ? reinterpret_cast<const __nv_bfloat16*>(p.q)
-                             : which == 1 ? reinterpret_cast<const __nv_bfloat16*>(p.k)
-                                          : reinterpret_cast<const __nv_bfloat16*>(p.v);
-    __nv_bfloat16* dst = which == 0 ? &in.q[row][vec * 8] : which == 1 ? &in.k[row][vec * 8] : &in.v[row][vec * 8];
-    const bool valid = row < ntok;
-    const __nv_bfloat16* s = src + (valid ? (static_cast<size_t>(tok0 + row) * H + h) * FD + vec * 8 : 0);
-    cp_async16_zfill(dst, s, valid ? 16u : 0u);
-  }
-  if (p.gate_mode != 0) {
-    const float* src = p.gate_mode == 1 ? p.g : p.a;  // both [tokens, H * FD] fp32
-    for (int i = pt; i < 16 * 32; i += 128) {
-      const int row = i >> 5, vec = i & 31;
-      const bool valid = row < ntok;
-      const float* s = src + (valid ? (static_cast<size_t>(tok0 + row) * H + h) * FD + vec * 4 : 0);
-      cp_async16_zfill(&in.a[row][vec * 4], s, valid ? 16u : 0u);
-    }
-  }
+// One thread issues the TMA loads of one chunk's input tiles (16 tokens x 128
+// channels of q, k, v and, with a gate, a or g) into a PrepIn buffer; the bytes
+// are counted on that buffer's mbarrier. Tokens past the end read as zero;
+// tokens of the next sequence are masked by the reader.
+__device__ __forceinline__ void issue_inputs(const TmaInputMaps& m, PrepIn& in, uint64_t* bar, int h, int tok0,
+                                             int gate_mode) {
+  const uint32_t bytes = 3 * sizeof(in.q) + (gate_mode != 0 ? sizeof(in.a) : 0);
+  mbar_arrive_expect_tx_local(bar, bytes);
+  tma_load_3d(&in.q[0][0], &m.q, 0, h, tok0, bar);
+  tma_load_3d(&in.k[0][0], &m.k, 0, h, tok0, bar);
+  tma_load_3d(&in.v[0][0], &m.v, 0, h, tok0, bar);
+  if (gate_mode != 0) tma_load_3d(&in.a[0][0], &m.a, 0, h, tok0, bar);
 }
 
 template <bool DELTA, bool L2N>
 __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1)
-    kda_chunk_fused_kernel(const ChunkCall p) {
+    kda_chunk_fused_kernel(const ChunkCall p, const __grid_constant__ TmaInputMaps maps) {
   using QK = std::conditional_t<L2N, F16, Bf16>;
   using ST2 = std::conditional_t<DELTA, F16, Bf16>;
   using Q = typename QK::T;
@@ -155,6 +146,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       mbar_init(&sm.empty[s], kCtas * 4);
     }
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.pinbar[b], 1);
       mbar_init(&sm.pfull[b], 1);
       mbar_init(&sm.pempty[b], 1);
     }
@@ -335,8 +327,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       return raw;
     };
     if (c < nch) {
-      prefetch_inputs(p, sm.pin[0], h, ts + c * kChunk, min(kChunk, te - (ts + c * kChunk)), pt);
-      cp_async_commit();
+      if (pt == 0) issue_inputs(maps, sm.pin[0], &sm.pinbar[0], h, ts + c * kChunk, p.gate_mode);
       beta_next = load_beta(c);
     }
     for (int j = 0; c < nch; ++j, c += kCtas) {
@@ -345,13 +336,14 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       const int ntok = min(kChunk, te - tok0);
       const float beta_cur = beta_next;
       if (c + kCtas < nch) {
-        const int t1 = ts + (c + kCtas) * kChunk;
-        prefetch_inputs(p, sm.pin[buf ^ 1], h, t1, min(kChunk, te - t1), pt);
-        cp_async_commit();
+        // buffer buf ^ 1 was last read in the previous iteration, before its closing barrier
+        if (pt == 0) issue_inputs(maps, sm.pin[buf ^ 1], &sm.pinbar[buf ^ 1], h, ts + (c + kCtas) * kChunk, p.gate_mode);
         beta_next = load_beta(c + kCtas);
-        cp_async_wait<1>();
-      } else {
-        cp_async_wait<0>();
+      }
+      if (!failed && !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pinbar[buf])),
+                                        static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs)) {
+        failed = true;
+        if (pt == 0) set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
       }
       PrepOut& po = sm.pout[buf];
       if (j >= 2 && pt == 0 && !failed &&
@@ -372,10 +364,10 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       const PrepIn& in = sm.pin[buf];
       float qv[16], kv[16], al[16], vv[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        qv[i] = __bfloat162float(in.q[i][pt]);
-        kv[i] = __bfloat162float(in.k[i][pt]);
-        vv[i] = __bfloat162float(in.v[i][pt]);
+      for (int i = 0; i < 16; ++i) {  // rows past the sequence end belong to another sequence: zero them
+        qv[i] = i < ntok ? __bfloat162float(in.q[i][pt]) : 0.f;
+        kv[i] = i < ntok ? __bfloat162float(in.k[i][pt]) : 0.f;
+        vv[i] = i < ntok ? __bfloat162float(in.v[i][pt]) : 0.f;
       }
       // One branch for the gate mode around the whole token loop, so the 16
       // independent exp/log chains interleave; padded tokens select alpha = 1.
@@ -620,7 +612,10 @@ cudaError_t launch_fused_t(const ChunkCall& c, cudaStream_t s) {
   }
   const unsigned grid = static_cast<unsigned>(c.geo.N) * static_cast<unsigned>(c.geo.H) * kCtas;
   if (grid == 0) return cudaSuccess;
-  kda_chunk_fused_kernel<DELTA, L2N><<<grid, kFusedThreads, smem, s>>>(c);
+  TmaInputMaps maps;
+  cudaError_t e = encode_input_maps(c, &maps);
+  if (e != cudaSuccess) return e;
+  kda_chunk_fused_kernel<DELTA, L2N><<<grid, kFusedThreads, smem, s>>>(c, maps);
   return cudaGetLastError();
 }
 

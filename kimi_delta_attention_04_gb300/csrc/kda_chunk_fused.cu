@@ -326,20 +326,13 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         raw = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.beta)[static_cast<size_t>(tk0 + pt) * H + h]);
       return raw;
     };
-    if (c < nch) {
-      if (pt == 0) issue_inputs(maps, sm.pin[0], &sm.pinbar[0], h, ts + c * kChunk, p.gate_mode);
-      beta_next = load_beta(c);
-    }
+    if (c < nch) beta_next = load_beta(c);
     for (int j = 0; c < nch; ++j, c += kCtas) {
       const int buf = j & 1;
       const int tok0 = ts + c * kChunk;
       const int ntok = min(kChunk, te - tok0);
       const float beta_cur = beta_next;
-      if (c + kCtas < nch) {
-        // buffer buf ^ 1 was last read in the previous iteration, before its closing barrier
-        if (pt == 0) issue_inputs(maps, sm.pin[buf ^ 1], &sm.pinbar[buf ^ 1], h, ts + (c + kCtas) * kChunk, p.gate_mode);
-        beta_next = load_beta(c + kCtas);
-      }
+      if (c + kCtas < nch) beta_next = load_beta(c + kCtas);
       if (!failed && !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pinbar[buf])),
                                         static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs)) {
         failed = true;
@@ -372,17 +365,23 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       // One branch for the gate mode around the whole token loop, so the 16
       // independent exp/log chains interleave; padded tokens select alpha = 1.
       if (p.gate_mode == 2) {
+        // alpha = e^{-A softplus(x)} = 2^{-A log2(1 + 2^{x log2 e})}, branch free:
+        // the exponent is clamped and x itself selected above the threshold 20.
+        constexpr float kLog2e = 1.4426950408889634f;
+        const float nA = -Aexp;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float x = in.a[i][pt] + dtb;
-          const float sp = x <= 20.f ? __logf(1.f + __expf(x)) : x;
-          const float a = __expf(-Aexp * sp);
+          const float l2 = __log2f(1.f + exp2f(fminf(x, 20.f) * kLog2e));
+          const float sp2 = x > 20.f ? x * kLog2e : l2;  // softplus(x) in log2 units
+          const float a = exp2f(nA * sp2);
           al[i] = i < ntok ? a : 1.f;
         }
       } else if (p.gate_mode == 1) {
+        constexpr float kLog2e = 1.4426950408889634f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float a = __expf(in.a[i][pt]);
+          const float a = exp2f(in.a[i][pt] * kLog2e);
           al[i] = i < ntok ? a : 1.f;
         }
       } else {
@@ -562,7 +561,17 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     // ===================== mover warp =====================
     // Pushes each prepared chunk into stage (c mod 4) of all four CTAs once the
     // consumers have released that stage, so prep never blocks on the ring.
+    // It also loads the input tiles: those of this CTA's chunk j + 2 go into
+    // buffer j mod 2 as soon as the prep warps have finished chunk j.
     if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.q) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.k) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.v) : "memory");
+      if (p.gate_mode != 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.a) : "memory");
+      for (int jj = 0; jj < 2; ++jj) {
+        const int cc = static_cast<int>(rank) + jj * kCtas;
+        if (cc < nch) issue_inputs(maps, sm.pin[jj], &sm.pinbar[jj], h, ts + cc * kChunk, p.gate_mode);
+      }
       bool failed = false;
       const uint32_t s = rank;  // every chunk this CTA prepares goes to stage rank
       const uint32_t dst_local = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.ring[s]));
@@ -574,6 +583,8 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           failed = true;
           set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
         }
+        if (c + 2 * kCtas < nch)  // prep has finished reading buffer b (chunk c)
+          issue_inputs(maps, sm.pin[b], &sm.pinbar[b], h, ts + (c + 2 * kCtas) * kChunk, p.gate_mode);
         if (j >= 1 && !failed &&
             !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.empty[s])),
                                static_cast<uint32_t>(j - 1) & 1u, kWaitLimitNs)) {

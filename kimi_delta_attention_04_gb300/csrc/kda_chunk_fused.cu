@@ -98,6 +98,7 @@ struct __align__(128) FusedSmem {
   uint64_t full[kRing];
   uint64_t empty[kRing];
   uint64_t pinbar[2];  // input tile buffer b loaded (TMA -> prep)
+  uint64_t pinfree[2]; // input tile buffer b read into registers (prep -> mover)
   uint64_t pfull[2];   // prep output buffer b written (prep -> mover)
   uint64_t pempty[2];  // prep output buffer b read by the pushes (mover -> prep)
   int failed;
@@ -147,6 +148,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.pinbar[b], 1);
+      mbar_init(&sm.pinfree[b], 1);
       mbar_init(&sm.pfull[b], 1);
       mbar_init(&sm.pempty[b], 1);
     }
@@ -406,7 +408,9 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           sm.ps.red[pw][32 + jj] = t3;
         }
       }
+      fence_proxy_async_smem();  // the reads of pin[buf] precede the next TMA write into it
       prep_bar();
+      if (pt == 0) mbar_arrive_local(&sm.pinfree[buf]);
       if (pt < 16) {
         float sq = 0.f, sk = 0.f, sqk = 0.f;
 #pragma unroll
@@ -578,13 +582,19 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       const uint32_t bar_local = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.full[s]));
       for (int j = 0, c = static_cast<int>(rank); c < nch; ++j, c += kCtas) {
         const int b = j & 1;
+        if (c + 2 * kCtas < nch) {  // once prep has read chunk c's tiles, load chunk c + 8's into the buffer
+          if (!failed && !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pinfree[b])),
+                                            static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs)) {
+            failed = true;
+            set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
+          }
+          issue_inputs(maps, sm.pin[b], &sm.pinbar[b], h, ts + (c + 2 * kCtas) * kChunk, p.gate_mode);
+        }
         if (!failed && !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pfull[b])),
                                           static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs)) {
           failed = true;
           set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
         }
-        if (c + 2 * kCtas < nch)  // prep has finished reading buffer b (chunk c)
-          issue_inputs(maps, sm.pin[b], &sm.pinbar[b], h, ts + (c + 2 * kCtas) * kChunk, p.gate_mode);
         if (j >= 1 && !failed &&
             !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.empty[s])),
                                static_cast<uint32_t>(j - 1) & 1u, kWaitLimitNs)) {

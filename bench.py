@@ -67,6 +67,14 @@ def decode_algorithmic_bytes(n_valid, H=32, HV=32, K=128, V=128, B=256):
     return state + io + params + B * HV * V * 2                         # + o
 
 
+# Sources of the kernels the roofline objects describe (a stored ncu traffic
+# figure is only reported while these files are unchanged).
+CHUNK_KERNEL_SOURCES = ["kda_chunk_fused.cu", "kda_common.cuh", "kda_cluster.cuh", "kda_tma.h", "kda_tma.cpp"]
+DECODE_KERNEL_SOURCES = ["kda_decode.cu", "kda_common.cuh"]
+CHUNK_LAUNCHES_PER_STEP = 1   # kda_chunk_fused_kernel (bf16, d = 128, no cu_seqlens)
+DECODE_LAUNCHES_PER_STEP = 1  # kda_decode_kernel
+
+
 def load_peaks():
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
@@ -82,16 +90,23 @@ def kernel_sources_sha(names):
     return h.hexdigest()[:16]
 
 
-def stored_traffic(kernel_key, sha):
-    """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel source; otherwise None."""
-    p = ROOT / "profiles" / "traffic.json"
+def stored_traffic(kernel_key, sha, units=1.0):
+    """DRAM bytes (read + write) per launch from the committed ncu summary
+    profiles/traffic.txt, if it was taken on the current kernel source, scaled
+    by `units` (the ratio of this launch's work to the captured launch's);
+    otherwise None. Lines: <kernel> source_sha=<sha> dram_bytes=<n> units=<u> ..."""
+    p = ROOT / "profiles" / "traffic.txt"
     if not p.exists():
         return None
-    d = json.loads(p.read_text()).get(kernel_key)
-    if not d or d.get("source_sha") != sha:
-        return None
-    return d.get("dram_bytes_per_launch")
+    for line in p.read_text().splitlines():
+        parts = line.split()
+        if not parts or parts[0] != kernel_key:
+            continue
+        kv = dict(x.split("=", 1) for x in parts[1:] if "=" in x)
+        if kv.get("source_sha") != sha:
+            return None
+        return float(kv["dram_bytes"]) * units / float(kv.get("units", "1"))
+    return None
 
 
 class ClockSampler:
@@ -324,8 +339,8 @@ def run_gpu(args):
     t_roof = max(abytes / (hbm * 1e9), aflops / (tflops * 1e12))
     dbytes = decode_algorithmic_bytes(n_valid)
     dach = dbytes / dec_avg / 1e9 if dec_avg > 0 else 0.0
-    chunk_sha = kernel_sources_sha(["kda_chunk_tc.cu", "kda_common.cuh"])
-    dec_sha = kernel_sources_sha(["kda_decode.cu", "kda_common.cuh"])
+    chunk_sha = kernel_sources_sha(CHUNK_KERNEL_SOURCES)
+    dec_sha = kernel_sources_sha(DECODE_KERNEL_SOURCES)
     clk = clocks.summary()
 
     if rank == 0:
@@ -342,13 +357,14 @@ def run_gpu(args):
             "decode": {"us_per_step": 1e6 * dec_avg, "n_valid_rows": n_valid,
                        "roofline": {"bound": "hbm", "achieved": dach, "peak": hbm, "unit": "GB/s",
                                     "frac": dach / hbm, "algorithmic_bytes": dbytes,
-                                    "traffic": stored_traffic("kda_decode", dec_sha), "peak_kind": peak_kind}},
+                                    "traffic": stored_traffic("kda_decode_kernel", dec_sha, n_valid), "peak_kind": peak_kind}},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": stored_traffic("kda_chunk_fwd", chunk_sha), "kernel": "chunk forward (prep + recurrence launches)",
+                         "traffic": stored_traffic("kda_chunk_fused_kernel", chunk_sha, T), "kernel": "kda_chunk_fused_kernel (prep + recurrence in one launch)",
                          "algorithmic_bytes": abytes, "peak_kind": peak_kind},
             "e2e": {"value": T * world / e2e_s if e2e_steps else None, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
-            "gpu_launches": (2 if args.only != "decode" else 0) * K + (1 if args.only != "chunk" else 0) * K,
+            "gpu_launches": (CHUNK_LAUNCHES_PER_STEP if args.only != "decode" else 0) * K
+                            + (DECODE_LAUNCHES_PER_STEP if args.only != "chunk" else 0) * K,
             "clocks": clk,
         }
         if args.only != "all" or T != PREFILL_T:

@@ -84,7 +84,8 @@ struct __align__(16) PrepScratch {
 };
 
 struct __align__(16) RecScratch {
-  float xch[2][2][2][32][16];        // [chunk parity][row block][key half][lane][8 U + 8 O]
+  float xch[2][2][2][32][8];         // [chunk parity][row block][key half][lane]: U^T partials
+  float oxch[2][2][32][8];           // [chunk parity][row block][lane]: second half's O^T partial
   __nv_bfloat16 ost[2][16][16];      // per row block: [token][value row]
 };
 
@@ -177,6 +178,35 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       for (int nt = 0; nt < 8; ++nt) S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.f;
     }
     bool failed = false;
+    float o_prev[2][4];  // first-half warp: its O^T partial of the previous chunk
+    // First-half warp only: add the second half's O^T partial of chunk cc (posted
+    // before the pair barrier that preceded this call) and store chunk cc's rows.
+    auto finish_output = [&](int cc) {
+      const float* op = sm.rs.oxch[cc & 1][dvb][lane];
+      const float4 b0 = *reinterpret_cast<const float4*>(op + 0);
+      const float4 b1 = *reinterpret_cast<const float4*>(op + 4);
+      o_prev[0][0] += b0.x; o_prev[0][1] += b0.y; o_prev[0][2] += b0.z; o_prev[0][3] += b0.w;
+      o_prev[1][0] += b1.x; o_prev[1][1] += b1.y; o_prev[1][2] += b1.z; o_prev[1][3] += b1.w;
+      __nv_bfloat16 (&ost)[16][16] = sm.rs.ost[dvb];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int tok = 8 * nt + 2 * t;
+        ost[tok][g] = __float2bfloat16_rn(o_prev[nt][0]);
+        ost[tok + 1][g] = __float2bfloat16_rn(o_prev[nt][1]);
+        ost[tok][g + 8] = __float2bfloat16_rn(o_prev[nt][2]);
+        ost[tok + 1][g + 8] = __float2bfloat16_rn(o_prev[nt][3]);
+      }
+      __syncwarp();
+      const int tok0 = ts + cc * kChunk;
+      const int ntok = min(kChunk, te - tok0);
+      const int row = lane >> 1, hv = lane & 1;
+      if (row < ntok) {
+        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.o) +
+                             (static_cast<size_t>(tok0 + row) * H + h) * FD + row0 + hv * 8;
+        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&ost[row][hv * 8]);
+      }
+      __syncwarp();
+    };
     for (int c = 0; c < nch; ++c) {
       const int s = c & (kRing - 1);
       const uint32_t par = static_cast<uint32_t>(c / kRing) & 1u;
@@ -194,7 +224,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         sa[kk][2] = Bf16::pack(S[2 * kk + 1][0], S[2 * kk + 1][1]);
         sa[kk][3] = Bf16::pack(S[2 * kk + 1][2], S[2 * kk + 1][3]);
       }
-      float u[2][4], o[2][4];
+      float u[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         if (dkh == 0) {
@@ -204,11 +234,10 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         } else {
           u[nt][0] = u[nt][1] = u[nt][2] = u[nt][3] = 0.f;
         }
-        o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
       }
       const int brow = ((lane >> 4) << 3) + (lane & 7);
       const int bcol = ((lane >> 3) & 1) * 8;
-      if (DELTA) {  // U first: it is on the serial path; two chains per n-tile
+      if (DELTA) {  // U^T partial over this key half: the serial path; two chains per n-tile
         float u2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         uint32_t b[4][4];
 #pragma unroll
@@ -224,35 +253,20 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
 #pragma unroll
           for (int e = 0; e < 4; ++e) u[nt][e] += u2[nt][e];
       }
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        uint32_t b[4];
-        ldsm_x4(b, &st.qd[brow][kc0 + 16 * kk + bcol]);
-        mma16816<Bf16>(o[0], sa[kk], b[0], b[1]);
-        mma16816<Bf16>(o[1], sa[kk], b[2], b[3]);
-      }
-      // exchange the key-half partial sums of U^T (and O^T) within the warp pair
+      // Exchange the two key halves' U^T partial sums (split-K). The same barrier
+      // also hands the first-half warp the second half's O^T partial of chunk c - 1.
       {
         float* mine = sm.rs.xch[c & 1][dvb][dkh][lane];
         *reinterpret_cast<float4*>(mine + 0) = make_float4(u[0][0], u[0][1], u[0][2], u[0][3]);
         *reinterpret_cast<float4*>(mine + 4) = make_float4(u[1][0], u[1][1], u[1][2], u[1][3]);
-        if (dkh == 1) {
-          *reinterpret_cast<float4*>(mine + 8) = make_float4(o[0][0], o[0][1], o[0][2], o[0][3]);
-          *reinterpret_cast<float4*>(mine + 12) = make_float4(o[1][0], o[1][1], o[1][2], o[1][3]);
-        }
         named_bar_sync(2 + dvb, 64);
         const float* other = sm.rs.xch[c & 1][dvb][dkh ^ 1][lane];
         const float4 a0 = *reinterpret_cast<const float4*>(other + 0);
         const float4 a1 = *reinterpret_cast<const float4*>(other + 4);
         u[0][0] += a0.x; u[0][1] += a0.y; u[0][2] += a0.z; u[0][3] += a0.w;
         u[1][0] += a1.x; u[1][1] += a1.y; u[1][2] += a1.z; u[1][3] += a1.w;
-        if (dkh == 0) {
-          const float4 b0 = *reinterpret_cast<const float4*>(other + 8);
-          const float4 b1 = *reinterpret_cast<const float4*>(other + 12);
-          o[0][0] += b0.x; o[0][1] += b0.y; o[0][2] += b0.z; o[0][3] += b0.w;
-          o[1][0] += b1.x; o[1][1] += b1.y; o[1][2] += b1.z; o[1][3] += b1.w;
-        }
       }
+      if (dkh == 0 && c > 0) finish_output(c - 1);
       uint32_t ua[4];
       ua[0] = ST2::pack(u[0][0], u[0][1]);
       ua[1] = ST2::pack(u[0][2], u[0][3]);
@@ -271,34 +285,40 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           mma16816<ST2>(S[nt], ua, b[2 * half], b[2 * half + 1]);
         }
       }
-      if (dkh == 0) {
-        uint32_t b[4];
-        ldsm_x4(b, &st.mqk[brow][bcol]);
-        mma16816<ST2>(o[0], ua, b[0], b[1]);
-        mma16816<ST2>(o[1], ua, b[2], b[3]);
-        __nv_bfloat16 (&ost)[16][16] = sm.rs.ost[dvb];
+      // O^T of this chunk, off the serial path: q_dec S_old over this key half
+      // (S_old is still in sa), plus U^T Mqk^T on the first half.
+      {
+        float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          const int tok = 8 * nt + 2 * t;
-          ost[tok][g] = __float2bfloat16_rn(o[nt][0]);
-          ost[tok + 1][g] = __float2bfloat16_rn(o[nt][1]);
-          ost[tok][g + 8] = __float2bfloat16_rn(o[nt][2]);
-          ost[tok + 1][g + 8] = __float2bfloat16_rn(o[nt][3]);
+        for (int kk = 0; kk < 4; ++kk) {
+          uint32_t b[4];
+          ldsm_x4(b, &st.qd[brow][kc0 + 16 * kk + bcol]);
+          mma16816<Bf16>(o[0], sa[kk], b[0], b[1]);
+          mma16816<Bf16>(o[1], sa[kk], b[2], b[3]);
         }
-        __syncwarp();
-        const int tok0 = ts + c * kChunk;
-        const int ntok = min(kChunk, te - tok0);
-        const int row = lane >> 1, hv = lane & 1;
-        if (row < ntok) {
-          __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.o) +
-                               (static_cast<size_t>(tok0 + row) * H + h) * FD + row0 + hv * 8;
-          *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&ost[row][hv * 8]);
+        if (dkh == 0) {
+          uint32_t b[4];
+          ldsm_x4(b, &st.mqk[brow][bcol]);
+          mma16816<ST2>(o[0], ua, b[0], b[1]);
+          mma16816<ST2>(o[1], ua, b[2], b[3]);
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o_prev[nt][e] = o[nt][e];
+        } else {
+          float* dst = sm.rs.oxch[c & 1][dvb][lane];
+          *reinterpret_cast<float4*>(dst + 0) = make_float4(o[0][0], o[0][1], o[0][2], o[0][3]);
+          *reinterpret_cast<float4*>(dst + 4) = make_float4(o[1][0], o[1][1], o[1][2], o[1][3]);
         }
       }
       __syncwarp();
       if (lane == 0)
         mbar_arrive_cluster(mapa_shared(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.empty[s])),
                                         static_cast<uint32_t>(s)));
+    }
+    if (nch > 0) {  // the last chunk's O^T partial from the second half
+      named_bar_sync(2 + dvb, 64);
+      if (dkh == 0) finish_output(nch - 1);
     }
     if (ok && p.hT != nullptr) {
       float* dst = p.hT + (static_cast<size_t>(n) * H + h) * FD * FD;

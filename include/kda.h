@@ -130,7 +130,10 @@ typedef struct kda_chunk_args {
 /*
  * Bytes of device scratch memory kda_chunk_fwd needs for these arguments
  * (0 when the arguments are invalid). The workspace is caller-owned; its
- * contents on entry do not matter and are garbage on exit.
+ * contents on entry do not matter and are garbage on exit. For bf16 with
+ * dk = dv = 128 it is a fixed ~14 MB (a pool of L2-resident rings through
+ * which the kernel hands prepared chunks between the CTAs of a cluster) plus a
+ * small per-sequence header; other shapes need per-(chunk, head) records.
  */
 size_t kda_chunk_workspace_size(const kda_chunk_args* args);
 
@@ -200,8 +203,8 @@ kda_status kda_decode_step(const kda_decode_args* args, kda_stream_t stream);
  *
  * Returns KDA_ERR_TOO_LARGE, launching nothing, when the arguments need more
  * than KDA_NOALLOC_SCRATCH_BYTES of scratch (kda_chunk_workspace_size(args)
- * tells how much they need; bf16 with dk = dv = 128 needs only a small
- * per-sequence header). Other argument errors as for kda_chunk_fwd.
+ * tells how much they need; bf16 with dk = dv = 128 needs a fixed ~14 MB plus
+ * 4 bytes per sequence). Other argument errors as for kda_chunk_fwd.
  *
  * The first call on each device looks up the address of the device's copy of
  * the buffer (cudaGetSymbolAddress, with that device current); make that first

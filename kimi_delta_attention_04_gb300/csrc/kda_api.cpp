@@ -68,7 +68,7 @@ kda_status check_chunk(const kda_chunk_args* a, kda::ChunkGeom* geo, size_t* rec
     geo->max_chunks = geo->chunks_per_seq + a->N;  // each sequence adds at most one partial chunk
   }
   if (uses_fused(*a)) {
-    *rec_bytes = 0;  // prep and recurrence exchange chunks on chip: no records
+    *rec_bytes = 0;  // no per-chunk records: a fixed pool of rings instead
     return KDA_OK;
   }
   *rec_bytes = a->dtype == KDA_DTYPE_BF16 ? kda::record_bytes_tc(a->dk) : kda::record_bytes_f32(a->dk, a->dv);
@@ -76,7 +76,8 @@ kda_status check_chunk(const kda_chunk_args* a, kda::ChunkGeom* geo, size_t* rec
   return KDA_OK;
 }
 
-size_t workspace_bytes(const kda::ChunkGeom& geo, size_t rec_bytes) {
+size_t workspace_bytes(const kda_chunk_args& a, const kda::ChunkGeom& geo, size_t rec_bytes) {
+  if (uses_fused(a)) return kda::plan_header_bytes(geo.N) + kda::fused_workspace_bytes();
   return kda::plan_header_bytes(geo.N) + static_cast<size_t>(geo.max_chunks) * geo.H * rec_bytes;
 }
 
@@ -88,7 +89,7 @@ size_t kda_chunk_workspace_size(const kda_chunk_args* args) {
   kda::ChunkGeom geo;
   size_t rec = 0;
   if (check_chunk(args, &geo, &rec) != KDA_OK) return 0;
-  return workspace_bytes(geo, rec);
+  return workspace_bytes(*args, geo, rec);
 }
 
 kda_status kda_chunk_fwd(const kda_chunk_args* args, void* workspace, size_t ws_bytes, kda_stream_t stream) {
@@ -96,7 +97,7 @@ kda_status kda_chunk_fwd(const kda_chunk_args* args, void* workspace, size_t ws_
   size_t rec = 0;
   kda_status st = check_chunk(args, &geo, &rec);
   if (st != KDA_OK) return st;
-  const size_t need = workspace_bytes(geo, rec);
+  const size_t need = workspace_bytes(*args, geo, rec);
   if (workspace == nullptr || ws_bytes < need || !aligned(workspace, 256)) return KDA_ERR_INVALID_ARG;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 

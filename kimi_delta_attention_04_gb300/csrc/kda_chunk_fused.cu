@@ -13,14 +13,17 @@
 //    chunk (split-K), which halves the serial MMA chain per warp.
 //  * The same CTA's four prep warps prepare every 4th chunk (chunks c = r mod 4):
 //    gate, beta, L2 norm, decay products, L / Mqk, Neumann inverse, W and U~.
-//    Inputs for the producer's next chunk are prefetched with cp.async while the
-//    current one is computed.
-//  * A prepared chunk is pushed from the producer's shared memory into stage
-//    c mod 4 of all four CTAs' rings with cp.async.bulk over distributed shared
-//    memory (the shared operands to every CTA, each CTA's 32 rows of U~ to it),
-//    counted on the destination's "full" mbarrier. Consumers release a stage by
-//    arriving on the producer's "empty" mbarrier. Nothing goes through global
-//    memory between prep and recurrence.
+//    A helper warp loads their input tiles with TMA two chunks ahead.
+//  * Prepared chunks travel through a ring of kGRing slots in global memory
+//    (L2-resident; one ring per cluster, taken from a pool in the workspace):
+//    the prep warps copy the chunk from shared memory into slot c mod kGRing
+//    with 16-byte stores; the helper warp then publishes it at cluster scope
+//    (fence.acq_rel.cluster) and arrives on the slot's "ready" mbarrier in all
+//    four CTAs. Each CTA's mover warp bulk-loads the shared operands and its
+//    own 32 rows of U~ into local stage c mod kRing and, when its recurrence
+//    warps release that stage, hands the global slot back to the producer
+//    ("gfree"). On GB300 an L2 bulk load delivers ~50 B/clk per SM against
+//    ~15-25 B/clk for a push over distributed shared memory.
 //  * Every mbarrier wait is bounded (KDA_ERR_TIMEOUT in err on expiry); loop trip
 //    counts never depend on a wait, so named barriers stay matched and every CTA
 //    reaches the closing cluster barrier.
@@ -36,8 +39,10 @@ namespace {
 constexpr int FD = 128;              // dk = dv
 constexpr int kCtas = 4;             // cluster size
 constexpr int kRows = FD / kCtas;    // value rows per CTA
-constexpr int kRing = 4;             // ring stages (= cluster size: stage s is produced by CTA s)
-constexpr int kFusedThreads = 288;   // 4 recurrence warps + 4 prep warps + 1 mover warp
+constexpr int kRing = 4;             // local stages per CTA
+constexpr int kGRing = 16;           // global ring slots per cluster (a multiple of kCtas)
+constexpr int kPool = 40;            // cluster rings in the workspace pool (> clusters resident at once)
+constexpr int kFusedThreads = 480;   // 4 recurrence warps, 2 x 4 prep warps, mover, publisher, loader
 constexpr int kPad = FD + 8;         // padded 16-bit row (conflict-free ldmatrix)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -63,6 +68,12 @@ struct __align__(16) PrepOut {
   float ut[FD][16];  // all value rows
 };
 static_assert(offsetof(PrepOut, ut) == kSharedBytes, "prep-out and stage share the layout");
+
+constexpr uint32_t kSlotBytes = sizeof(PrepOut);
+static_assert(kSlotBytes % 16 == 0, "slot size");
+constexpr size_t kPoolHeader = 256;  // bitmap of the pool's rings in use
+constexpr size_t kRingBytes = static_cast<size_t>(kGRing) * kSlotBytes;
+static_assert(kPool <= 64, "bitmap holds 64 rings");
 
 struct __align__(16) PrepIn {
   __nv_bfloat16 q[16][FD];
@@ -92,17 +103,17 @@ struct __align__(16) RecScratch {
 template <typename Q>
 struct __align__(128) FusedSmem {
   Stage ring[kRing];
-  PrepOut pout[2];
-  PrepIn pin[2];
-  PrepScratch<Q> ps;
+  PrepIn pin[2];                   // input tiles of prep group g
+  PrepScratch<Q> ps[2];            // scratch of prep group g
   RecScratch rs;
-  uint64_t full[kRing];
-  uint64_t empty[kRing];
-  uint64_t pinbar[2];  // input tile buffer b loaded (TMA -> prep)
-  uint64_t pinfree[2]; // input tile buffer b read into registers (prep -> mover)
-  uint64_t pfull[2];   // prep output buffer b written (prep -> mover)
-  uint64_t pempty[2];  // prep output buffer b read by the pushes (mover -> prep)
-  int failed;
+  uint64_t full[kRing];            // stage loaded (mover's bulk loads -> recurrence)
+  uint64_t empty[kRing];           // stage released by the 4 recurrence warps (-> mover)
+  uint64_t ready[kGRing];          // global slot written and published (producer's helper -> every mover)
+  uint64_t gfree[kGRing];          // global slot read by all 4 CTAs (movers -> producer's prep)
+  uint64_t sig[kGRing / kCtas];    // this CTA's slot written (prep -> publisher)
+  uint64_t pinbar[2];              // input tiles of group g loaded (TMA -> prep)
+  uint64_t pinfree[2];             // input tiles of group g read into registers (prep -> loader)
+  int ring_id;                     // pool ring of this cluster (CTA 0's copy is authoritative)
 };
 
 __device__ __forceinline__ int row_tok_f(int s, int r) { return (r / s) * 2 * s + s + (r % s); }
@@ -122,6 +133,37 @@ __device__ __forceinline__ void issue_inputs(const TmaInputMaps& m, PrepIn& in, 
   if (gate_mode != 0) tma_load_3d(&in.a[0][0], &m.a, 0, h, tok0, bar);
 }
 
+__device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+
+// Takes a free ring of the workspace pool (a 64-bit map, cleared before the
+// launch). At most ~38 clusters of this kernel are resident at once, fewer
+// than kPool, so a ring frees up at the latest when a running cluster ends; the
+// wait is bounded all the same. Returns -1 (and reports a timeout) on failure.
+__device__ int claim_ring(unsigned char* pool, int32_t* err) {
+  unsigned int* bits = reinterpret_cast<unsigned int*>(pool);
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+#pragma unroll 1
+    for (int w = 0; w < 2; ++w) {
+      const unsigned int valid = (w == 0) ? 0xffffffffu : ((1u << (kPool - 32)) - 1u);
+      unsigned int free_bits = ~atomicOr(&bits[w], 0u) & valid;
+      while (free_bits != 0u) {
+        const int b = __ffs(free_bits) - 1;
+        const unsigned int old = atomicOr(&bits[w], 1u << b);
+        if ((old & (1u << b)) == 0u) return 32 * w + b;
+        free_bits = ~old & valid;
+      }
+    }
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      set_err(err, 4 /* KDA_ERR_TIMEOUT */);
+      return -1;
+    }
+    __nanosleep(1000);
+  }
+}
+
 template <bool DELTA, bool L2N>
 __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1)
     kda_chunk_fused_kernel(const ChunkCall p, const __grid_constant__ TmaInputMaps maps) {
@@ -139,24 +181,34 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
   const int h = unit - n * H;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int ts = 0, te = 0, cb = 0;
-  const bool ok = locate_seq(p.geo, n, ts, te, cb);
-  const int nch = ok ? (te - ts + kChunk - 1) / kChunk : 0;
+  const bool located = locate_seq(p.geo, n, ts, te, cb);
+  const int nch0 = located ? (te - ts + kChunk - 1) / kChunk : 0;
 
   if (tid == 0) {
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], kCtas * 4);
+      mbar_init(&sm.empty[s], 4);
     }
+    for (int i = 0; i < kGRing; ++i) {
+      mbar_init(&sm.ready[i], 1);
+      mbar_init(&sm.gfree[i], kCtas);
+    }
+    for (int i = 0; i < kGRing / kCtas; ++i) mbar_init(&sm.sig[i], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.pinbar[b], 1);
       mbar_init(&sm.pinfree[b], 1);
-      mbar_init(&sm.pfull[b], 1);
-      mbar_init(&sm.pempty[b], 1);
     }
-    sm.failed = 0;
+    sm.ring_id = (rank == 0 && nch0 > 0) ? claim_ring(p.records, p.err) : -1;
     fence_mbarrier_init_cluster();
   }
   cluster_sync_all();
+  // every CTA works on CTA 0's ring; without one (nothing to do, or no ring
+  // could be had) the cluster does nothing
+  const int ring_id = ld_shared_cluster_s32(mapa_shared(smem_u32(&sm.ring_id), 0));
+  const bool ok = located && (nch0 == 0 || ring_id >= 0);
+  const int nch = ring_id >= 0 ? nch0 : 0;
+  unsigned char* const gring =
+      p.records + kPoolHeader + static_cast<size_t>(ring_id >= 0 ? ring_id : 0) * kRingBytes;
 
   if (warp < 4) {
     // ===================== recurrence warps =====================
@@ -253,6 +305,16 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
 #pragma unroll
           for (int e = 0; e < 4; ++e) u[nt][e] += u2[nt][e];
       }
+      // O^T = q_dec S_old over this key half, issued behind the U^T MMAs so it
+      // fills their latency; its result is only used after the state update.
+      float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t b[4];
+        ldsm_x4(b, &st.qd[brow][kc0 + 16 * kk + bcol]);
+        mma16816<Bf16>(o[0], sa[kk], b[0], b[1]);
+        mma16816<Bf16>(o[1], sa[kk], b[2], b[3]);
+      }
       // Exchange the two key halves' U^T partial sums (split-K). The same barrier
       // also hands the first-half warp the second half's O^T partial of chunk c - 1.
       {
@@ -285,17 +347,9 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           mma16816<ST2>(S[nt], ua, b[2 * half], b[2 * half + 1]);
         }
       }
-      // O^T of this chunk, off the serial path: q_dec S_old over this key half
-      // (S_old is still in sa), plus U^T Mqk^T on the first half.
+      // finish this chunk's O^T off the serial path: U^T Mqk^T on the first half;
+      // the second half posts its partial for the first half's next barrier.
       {
-        float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          uint32_t b[4];
-          ldsm_x4(b, &st.qd[brow][kc0 + 16 * kk + bcol]);
-          mma16816<Bf16>(o[0], sa[kk], b[0], b[1]);
-          mma16816<Bf16>(o[1], sa[kk], b[2], b[3]);
-        }
         if (dkh == 0) {
           uint32_t b[4];
           ldsm_x4(b, &st.mqk[brow][bcol]);
@@ -312,9 +366,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         }
       }
       __syncwarp();
-      if (lane == 0)
-        mbar_arrive_cluster(mapa_shared(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.empty[s])),
-                                        static_cast<uint32_t>(s)));
+      if (lane == 0) mbar_arrive_local(&sm.empty[s]);
     }
     if (nch > 0) {  // the last chunk's O^T partial from the second half
       named_bar_sync(2 + dvb, 64);
@@ -329,15 +381,23 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
             make_float2(S[nt][2], S[nt][3]);
       }
     }
-  } else if (warp < 8) {
+  } else if (warp < 12) {
     // ===================== prep warps =====================
-    const int pt = tid - 128;  // key / value channel owned by this thread
-    const int pw = pt >> 5;    // prep warp index 0..3
-    auto prep_bar = [] { named_bar_sync(1, 128); };
+    // Chunk c is prepared in shared memory (pout), then copied into global slot
+    // c mod kGRing once all four CTAs have loaded that slot's previous chunk.
+    // Two groups of four warps; group g prepares this CTA's chunks j = g mod 2
+    // (c = rank + 4 j), so two chunks are in flight and each group's latency
+    // hides behind the other's.
+    const int grp = (warp - 4) >> 2;
+    const int pt = tid - 128 * (1 + grp);  // key / value channel owned by this thread
+    const int pw = pt >> 5;                // warp index 0..3 within the group
+    const uint32_t bar_id = grp == 0 ? 1u : 4u;
+    auto prep_bar = [bar_id] { named_bar_sync(bar_id, 128); };
+    PrepScratch<Q>& ps = sm.ps[grp];
     const float Aexp = (p.gate_mode == 2) ? expf(p.A_log[h]) : 0.f;
     const float dtb = (p.gate_mode == 2) ? p.dt_bias[h * FD + pt] : 0.f;
     bool failed = false;
-    int c = static_cast<int>(rank);
+    int c = static_cast<int>(rank) + kCtas * grp;
     // beta is loaded raw one producer step ahead; its sigmoid is taken when it
     // is stored, so the load latency never sits on the prep's critical path.
     float beta_next = 0.f;
@@ -349,31 +409,33 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       return raw;
     };
     if (c < nch) beta_next = load_beta(c);
-    for (int j = 0; c < nch; ++j, c += kCtas) {
-      const int buf = j & 1;
+    for (int j = grp; c < nch; j += 2, c += 2 * kCtas) {
+      const int buf = grp;
       const int tok0 = ts + c * kChunk;
       const int ntok = min(kChunk, te - tok0);
       const float beta_cur = beta_next;
-      if (c + kCtas < nch) beta_next = load_beta(c + kCtas);
+      if (c + 2 * kCtas < nch) beta_next = load_beta(c + 2 * kCtas);
       if (!failed && !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pinbar[buf])),
                                         static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs)) {
         failed = true;
         if (pt == 0) set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
       }
-      PrepOut& po = sm.pout[buf];
-      if (j >= 2 && pt == 0 && !failed &&
-          !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pempty[buf])),
-                             static_cast<uint32_t>((j >> 1) - 1) & 1u, kWaitLimitNs)) {
-        failed = true;  // the pushes of chunk c - 8 have not read this buffer yet
+      // the chunk is written straight into global slot c mod kGRing, once all
+      // four CTAs have loaded that slot's previous chunk
+      const int gs = c % kGRing;
+      if (c >= kGRing && pt == 0 && !failed &&
+          !mbar_wait_bounded(smem_u32(&sm.gfree[gs]), static_cast<uint32_t>(c / kGRing - 1) & 1u, kWaitLimitNs)) {
+        failed = true;
         set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
       }
+      PrepOut& po = *reinterpret_cast<PrepOut*>(gring + static_cast<size_t>(gs) * kSlotBytes);
       for (int i = pt; i < 16 * 17; i += 128) {
-        (&sm.ps.Lm[0][0])[i] = 0.f;
-        (&sm.ps.Mq[0][0])[i] = 0.f;
+        (&ps.Lm[0][0])[i] = 0.f;
+        (&ps.Mq[0][0])[i] = 0.f;
       }
       if (pt < 16) {
         const float bt = (p.beta_mode == 1) ? sigmoid_f(beta_cur) : beta_cur;
-        sm.ps.beta[pt] = (DELTA && pt < ntok) ? bt : 0.f;
+        ps.beta[pt] = (DELTA && pt < ntok) ? bt : 0.f;
       }
       prep_bar();
       const PrepIn& in = sm.pin[buf];
@@ -423,9 +485,9 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         const float t3 = warp_transpose_reduce16(red, lane);
         if ((lane & 1) == 0) {
           const int jj = lane >> 1;
-          sm.ps.red[pw][jj] = t1;
-          sm.ps.red[pw][16 + jj] = t2;
-          sm.ps.red[pw][32 + jj] = t3;
+          ps.red[pw][jj] = t1;
+          ps.red[pw][16 + jj] = t2;
+          ps.red[pw][32 + jj] = t3;
         }
       }
       fence_proxy_async_smem();  // the reads of pin[buf] precede the next TMA write into it
@@ -435,21 +497,21 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         float sq = 0.f, sk = 0.f, sqk = 0.f;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-          sq += sm.ps.red[w][pt];
-          sk += sm.ps.red[w][16 + pt];
-          sqk += sm.ps.red[w][32 + pt];
+          sq += ps.red[w][pt];
+          sk += ps.red[w][16 + pt];
+          sqk += ps.red[w][32 + pt];
         }
         const float rq = L2N ? rsqrtf(sq + 1e-6f) : 1.f;
         const float rk = L2N ? rsqrtf(sk + 1e-6f) : 1.f;
-        sm.ps.rnq[pt] = rq;
-        sm.ps.rnk[pt] = rk;
-        sm.ps.Mq[pt][pt] = p.scale * sqk * rq * rk;
+        ps.rnq[pt] = rq;
+        ps.rnk[pt] = rk;
+        ps.Mq[pt][pt] = p.scale * sqk * rq * rk;
       }
       prep_bar();
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        qv[i] *= sm.ps.rnq[i];
-        kv[i] *= sm.ps.rnk[i];
+        qv[i] *= ps.rnq[i];
+        kv[i] *= ps.rnk[i];
       }
       float P[16], Rs[16];
       P[0] = al[0];
@@ -466,8 +528,8 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           const typename ST2::T kr = ST2::cvt(kv[i] * Rs[i]);
           po.kr[i][pt] = *reinterpret_cast<const uint16_t*>(&kr);
           if (DELTA) {
-            sm.ps.kdec[i][pt] = QK::cvt(kv[i] * P[i]);
-            sm.ps.vs[i][pt] = __float2bfloat16_rn(vv[i]);
+            ps.kdec[i][pt] = QK::cvt(kv[i] * P[i]);
+            ps.vs[i][pt] = __float2bfloat16_rn(vv[i]);
           }
         }
         po.gamma[pt] = P[15];
@@ -487,14 +549,14 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
             for (int i = m; i < m + s; ++i) {
               if (i > m) f *= al[i];
               const int r = blk * s + (i - m);
-              if (DELTA) sm.ps.A_lv[lv][r][pt] = QK::cvt(kv[i] * f);
-              sm.ps.A_lv[lv][8 + r][pt] = QK::cvt(qv[i] * f);
+              if (DELTA) ps.A_lv[lv][r][pt] = QK::cvt(kv[i] * f);
+              ps.A_lv[lv][8 + r][pt] = QK::cvt(qv[i] * f);
             }
             f = 1.f;
 #pragma unroll
             for (int i = m - 1; i >= m - s; --i) {
               f *= al[i + 1];
-              sm.ps.B_lv[lv][blk * s + (i - (m - s))][pt] = QK::cvt(kv[i] * f);
+              ps.B_lv[lv][blk * s + (i - (m - s))][pt] = QK::cvt(kv[i] * f);
             }
           }
         }
@@ -507,8 +569,8 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
 #pragma unroll
         for (int kk = 0; kk < FD / 16; ++kk) {
           uint32_t a[4], b[2];
-          ldsm_x4(a, &sm.ps.A_lv[lv][lane & 15][16 * kk + (lane >> 4) * 8]);
-          ldsm_x2(b, &sm.ps.B_lv[lv][lane & 7][16 * kk + ((lane >> 3) & 1) * 8]);
+          ldsm_x4(a, &ps.A_lv[lv][lane & 15][16 * kk + (lane >> 4) * 8]);
+          ldsm_x2(b, &ps.B_lv[lv][lane & 7][16 * kk + ((lane >> 3) & 1) * 8]);
           mma16816<QK>(acc, a, b[0], b[1]);
         }
         const int g = lane >> 2, t = lane & 3;
@@ -520,27 +582,27 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           if (rr / s != cidx / s) continue;
           const int i = row_tok_f(s, rr), jx = col_tok_f(s, cidx);
           if (r < 8) {
-            if (DELTA) sm.ps.Lm[i][jx] = sm.ps.beta[i] * acc[e];
+            if (DELTA) ps.Lm[i][jx] = ps.beta[i] * acc[e];
           } else {
-            sm.ps.Mq[i][jx] = p.scale * acc[e];
+            ps.Mq[i][jx] = p.scale * acc[e];
           }
         }
       }
       prep_bar();
       for (int e = pt; e < 256; e += 128) {
-        const typename ST2::T v = ST2::cvt(sm.ps.Mq[e >> 4][e & 15]);
+        const typename ST2::T v = ST2::cvt(ps.Mq[e >> 4][e & 15]);
         po.mqk[e >> 4][e & 15] = *reinterpret_cast<const uint16_t*>(&v);
       }
       if (DELTA) {
         // every prep warp forms INV' = (I + L)^{-1} diag(beta) in registers
         const int g = lane >> 2, t = lane & 3;
-        Frag16 inv = neumann_inverse16<QK>(&sm.ps.Lm[0][0], 17, lane);
+        Frag16 inv = neumann_inverse16<QK>(&ps.Lm[0][0], 17, lane);
         Frag16 ihi, ilo;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const float v = inv.c[nt][e] * sm.ps.beta[8 * nt + 2 * t + (e & 1)];
+            const float v = inv.c[nt][e] * ps.beta[8 * nt + 2 * t + (e & 1)];
             inv.c[nt][e] = v;
             ihi.c[nt][e] = __bfloat162float(__float2bfloat16_rn(v));
             ilo.c[nt][e] = v - ihi.c[nt][e];
@@ -553,7 +615,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         for (int pp = 0; pp < 2; ++pp) {
           const int n0 = pw * 32 + 16 * pp;
           uint32_t b[4];
-          ldsm_x4_trans(b, &sm.ps.kdec[lane & 15][n0 + (lane >> 4) * 8]);
+          ldsm_x4_trans(b, &ps.kdec[lane & 15][n0 + (lane >> 4) * 8]);
           float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
           mma16816<QK>(c0, a, b[0], b[1]);
           mma16816<QK>(c1, a, b[2], b[3]);
@@ -561,7 +623,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           *reinterpret_cast<uint32_t*>(&po.W[g + 8][n0 + 2 * t]) = Bf16::pack(-c0[2], -c0[3]);
           *reinterpret_cast<uint32_t*>(&po.W[g][n0 + 8 + 2 * t]) = Bf16::pack(-c1[0], -c1[1]);
           *reinterpret_cast<uint32_t*>(&po.W[g + 8][n0 + 8 + 2 * t]) = Bf16::pack(-c1[2], -c1[3]);
-          ldsm_x4_trans(b, &sm.ps.vs[lane & 15][n0 + (lane >> 4) * 8]);
+          ldsm_x4_trans(b, &ps.vs[lane & 15][n0 + (lane >> 4) * 8]);
           float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};
           mma16816<Bf16>(u0, ahi, b[0], b[1]);
           mma16816<Bf16>(u0, alo, b[0], b[1]);
@@ -577,16 +639,72 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           po.ut[n0 + 8 + 2 * t + 1][g + 8] = u1[3];
         }
       }
-      fence_proxy_async_smem();  // make po visible to the bulk-copy (async) proxy
-      prep_bar();
-      if (pt == 0) mbar_arrive_local(&sm.pfull[buf]);
+      prep_bar();  // every store into the slot precedes the hand-off
+      if (pt == 0) mbar_arrive_local(&sm.sig[j % (kGRing / kCtas)]);
+    }
+  } else if (warp == 12) {
+    // ===================== mover warp =====================
+    // Loads chunk c from its global slot into local stage c mod kRing once the
+    // slot is published and the recurrence warps have released the stage; a
+    // released stage also returns its chunk's global slot to the producer.
+    if (lane == 0) {
+      bool failed = false;
+      for (int c = 0; c < nch; ++c) {
+        const int s = c & (kRing - 1);
+        const int gs = c % kGRing;
+        if (c >= kRing) {
+          if (!failed && !mbar_wait_bounded(smem_u32(&sm.empty[s]), static_cast<uint32_t>(c / kRing - 1) & 1u,
+                                            kWaitLimitNs)) {
+            failed = true;
+            set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
+          }
+          const int cp = c - kRing;
+          mbar_arrive_cluster(mapa_shared(smem_u32(&sm.gfree[cp % kGRing]), static_cast<uint32_t>(cp % kCtas)));
+        }
+        if (!failed && !mbar_wait_acq_cluster_bounded(smem_u32(&sm.ready[gs]), static_cast<uint32_t>(c / kGRing) & 1u,
+                                                      kWaitLimitNs)) {
+          failed = true;
+          set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
+        }
+        fence_proxy_async_global();  // the bulk loads below read what the acquire made visible
+        const unsigned char* slot = gring + static_cast<size_t>(gs) * kSlotBytes;
+        unsigned char* stage = reinterpret_cast<unsigned char*>(&sm.ring[s]);
+        mbar_arrive_expect_tx_local(&sm.full[s], kStageTx);
+        bulk_load_g2s(stage, slot, kSharedBytes, &sm.full[s]);
+        bulk_load_g2s(stage + kSharedBytes, slot + kSharedBytes + rank * kUtSliceBytes, kUtSliceBytes, &sm.full[s]);
+      }
+      // no load may still be landing in this CTA's shared memory when it exits
+      for (int c = max(0, nch - kRing); c < nch; ++c)
+        if (!failed && !mbar_wait_bounded(smem_u32(&sm.full[c & (kRing - 1)]), static_cast<uint32_t>(c / kRing) & 1u,
+                                          kWaitLimitNs)) {
+          failed = true;
+          set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
+        }
+    }
+    __syncwarp();
+  } else if (warp == 13) {
+    // ===================== publisher warp =====================
+    // Publishes each chunk the prep groups wrote into the global ring: lanes
+    // 0-3 each make the group's stores visible at cluster scope and arrive on
+    // the slot's "ready" mbarrier in CTA `lane`.
+    bool failed = false;
+    for (int j = 0, c = static_cast<int>(rank); c < nch; ++j, c += kCtas) {
+      if (lane < kCtas) {
+        if (!failed && !mbar_wait_bounded(smem_u32(&sm.sig[j % (kGRing / kCtas)]),
+                                          static_cast<uint32_t>(j / (kGRing / kCtas)) & 1u, kWaitLimitNs)) {
+          failed = true;
+          set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
+        }
+        fence_acq_rel_cluster();
+        mbar_arrive_relaxed_cluster(mapa_shared(smem_u32(&sm.ready[c % kGRing]), static_cast<uint32_t>(lane)));
+      }
+      __syncwarp();
     }
   } else {
-    // ===================== mover warp =====================
-    // Pushes each prepared chunk into stage (c mod 4) of all four CTAs once the
-    // consumers have released that stage, so prep never blocks on the ring.
-    // It also loads the input tiles: those of this CTA's chunk j + 2 go into
-    // buffer j mod 2 as soon as the prep warps have finished chunk j.
+    // ===================== loader warp =====================
+    // TMA loads of the prep groups' input tiles: chunk j + 2 of this CTA goes
+    // into group (j mod 2)'s buffer as soon as that group holds chunk j's tiles
+    // in registers.
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.q) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.k) : "memory");
@@ -597,47 +715,23 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         if (cc < nch) issue_inputs(maps, sm.pin[jj], &sm.pinbar[jj], h, ts + cc * kChunk, p.gate_mode);
       }
       bool failed = false;
-      const uint32_t s = rank;  // every chunk this CTA prepares goes to stage rank
-      const uint32_t dst_local = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.ring[s]));
-      const uint32_t bar_local = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.full[s]));
-      for (int j = 0, c = static_cast<int>(rank); c < nch; ++j, c += kCtas) {
-        const int b = j & 1;
-        if (c + 2 * kCtas < nch) {  // once prep has read chunk c's tiles, load chunk c + 8's into the buffer
-          if (!failed && !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pinfree[b])),
-                                            static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs)) {
-            failed = true;
-            set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
-          }
-          issue_inputs(maps, sm.pin[b], &sm.pinbar[b], h, ts + (c + 2 * kCtas) * kChunk, p.gate_mode);
-        }
-        if (!failed && !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pfull[b])),
-                                          static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs)) {
+      for (int j = 0, c = static_cast<int>(rank); c + 2 * kCtas < nch; ++j, c += kCtas) {
+        const int g = j & 1;
+        if (!failed && !mbar_wait_bounded(smem_u32(&sm.pinfree[g]), static_cast<uint32_t>(j >> 1) & 1u,
+                                          kWaitLimitNs)) {
           failed = true;
           set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
         }
-        if (j >= 1 && !failed &&
-            !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.empty[s])),
-                               static_cast<uint32_t>(j - 1) & 1u, kWaitLimitNs)) {
-          failed = true;
-          set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
-        }
-        const uint32_t src = static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pout[b]));
-#pragma unroll
-        for (uint32_t r2 = 0; r2 < kCtas; ++r2) {
-          const uint32_t dst = mapa_shared(dst_local, r2);
-          const uint32_t bar = mapa_shared(bar_local, r2);
-          mbar_arrive_expect_tx_cluster(bar, kStageTx);
-          bulk_copy_s2s(dst, src, kSharedBytes, bar);
-          bulk_copy_s2s(dst + kSharedBytes, src + kSharedBytes + r2 * kUtSliceBytes, kUtSliceBytes, bar);
-        }
-        bulk_commit();
-        bulk_wait_read_all();
-        mbar_arrive_local(&sm.pempty[b]);
+        issue_inputs(maps, sm.pin[g], &sm.pinbar[g], h, ts + (c + 2 * kCtas) * kChunk, p.gate_mode);
       }
     }
     __syncwarp();
   }
   cluster_sync_all();
+  if (rank == 0 && tid == 0 && ring_id >= 0) {  // hand the ring back to the pool
+    __threadfence();
+    atomicAnd(reinterpret_cast<unsigned int*>(p.records) + ring_id / 32, ~(1u << (ring_id % 32)));
+  }
 }
 
 template <bool DELTA, bool L2N>
@@ -656,13 +750,20 @@ cudaError_t launch_fused_t(const ChunkCall& c, cudaStream_t s) {
   TmaInputMaps maps;
   cudaError_t e = encode_input_maps(c, &maps);
   if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(c.records, 0, kPoolHeader, s);  // every pool ring free
+  if (e != cudaSuccess) return e;
   kda_chunk_fused_kernel<DELTA, L2N><<<grid, kFusedThreads, smem, s>>>(c, maps);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+static_assert(sizeof(FusedSmem<__half>) <= 227 * 1024 && sizeof(FusedSmem<__nv_bfloat16>) <= 227 * 1024,
+              "fused kernel shared memory");
+
 size_t fused_smem_bytes() { return sizeof(FusedSmem<__half>); }
+
+size_t fused_workspace_bytes() { return kPoolHeader + static_cast<size_t>(kPool) * kRingBytes; }
 
 cudaError_t launch_chunk_fused(const ChunkCall& c, cudaStream_t s) {
   if (c.dk != FD || c.dv != FD) return cudaErrorInvalidValue;

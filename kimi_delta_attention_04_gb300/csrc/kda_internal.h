@@ -39,7 +39,8 @@ struct ChunkCall {
   void* o;
   float* hT;
   int32_t* err;
-  unsigned char* records;  // per (chunk, head) prep records in the workspace
+  unsigned char* records;  // workspace after the plan header: per (chunk, head) prep records,
+                           // or the fused kernel's pool of global rings
 };
 
 struct DecodeCall {
@@ -72,6 +73,7 @@ cudaError_t launch_chunk_tc(const ChunkCall& c, cudaStream_t s);
 cudaError_t launch_chunk_f32(const ChunkCall& c, cudaStream_t s);
 cudaError_t launch_chunk_fused(const ChunkCall& c, cudaStream_t s);  // bf16, dk = dv = 128
 size_t fused_smem_bytes();
+size_t fused_workspace_bytes();  // pool of per-cluster global rings (fixed size)
 cudaError_t launch_decode(const DecodeCall& c, cudaStream_t s);
 
 }  // namespace kda

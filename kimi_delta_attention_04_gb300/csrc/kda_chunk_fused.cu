@@ -10,7 +10,10 @@
 //    recurrence warps are (16-row block) x (half of the key channels): each holds
 //    S^T[16 x 64] fp32 in registers as mma.sync accumulators. The U^T partial
 //    sums of the two key halves are exchanged through shared memory once per
-//    chunk (split-K), which halves the serial MMA chain per warp.
+//    chunk (split-K), which halves the serial MMA chain per warp. Each warp's
+//    O^T partial (q_dec S over its key half, plus U^T Mqk^T on the first half)
+//    is computed behind the state update and staged in shared memory; an
+//    output warp adds the halves and stores o, off the serial path.
 //  * The same CTA's four prep warps prepare every 4th chunk (chunks c = r mod 4):
 //    gate, beta, L2 norm, decay products, L / Mqk, Neumann inverse, W and U~.
 //    A helper warp loads their input tiles with TMA two chunks ahead.
@@ -42,7 +45,7 @@ constexpr int kRows = FD / kCtas;    // value rows per CTA
 constexpr int kRing = 4;             // local stages per CTA
 constexpr int kGRing = 16;           // global ring slots per cluster (a multiple of kCtas)
 constexpr int kPool = 40;            // cluster rings in the workspace pool (> clusters resident at once)
-constexpr int kFusedThreads = 480;   // 4 recurrence warps, 2 x 4 prep warps, mover, publisher, loader
+constexpr int kFusedThreads = 512;   // 4 recurrence warps, 2 x 4 prep warps, mover, publisher, loader, output
 constexpr int kPad = FD + 8;         // padded 16-bit row (conflict-free ldmatrix)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -94,10 +97,11 @@ struct __align__(16) PrepScratch {
   float rnq[16], rnk[16], beta[16];
 };
 
+constexpr int kOPitch = kRows + 4;  // padded row of an output partial (conflict-free both ways)
+
 struct __align__(16) RecScratch {
-  float xch[2][2][2][32][8];         // [chunk parity][row block][key half][lane]: U^T partials
-  float oxch[2][2][32][8];           // [chunk parity][row block][lane]: second half's O^T partial
-  __nv_bfloat16 ost[2][16][16];      // per row block: [token][value row]
+  float xch[2][2][2][32][8];              // [chunk parity][row block][key half][lane]: U^T partials
+  float opart[kRing][2][16][kOPitch];     // [stage][key half][token][value row]: O partials
 };
 
 template <typename Q>
@@ -107,7 +111,8 @@ struct __align__(128) FusedSmem {
   PrepScratch<Q> ps[2];            // scratch of prep group g
   RecScratch rs;
   uint64_t full[kRing];            // stage loaded (mover's bulk loads -> recurrence)
-  uint64_t empty[kRing];           // stage released by the 4 recurrence warps (-> mover)
+  uint64_t empty[kRing];           // stage released by the 4 recurrence warps and the output warp (-> mover)
+  uint64_t ofull[kRing];           // O partials of the stage's chunk written (recurrence -> output warp)
   uint64_t ready[kGRing];          // global slot written and published (producer's helper -> every mover)
   uint64_t gfree[kGRing];          // global slot read by all 4 CTAs (movers -> producer's prep)
   uint64_t sig[kGRing / kCtas];    // this CTA's slot written (prep -> publisher)
@@ -187,7 +192,8 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
   if (tid == 0) {
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 4);
+      mbar_init(&sm.empty[s], 5);
+      mbar_init(&sm.ofull[s], 4);
     }
     for (int i = 0; i < kGRing; ++i) {
       mbar_init(&sm.ready[i], 1);
@@ -230,45 +236,27 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       for (int nt = 0; nt < 8; ++nt) S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.f;
     }
     bool failed = false;
-    float o_prev[2][4];  // first-half warp: its O^T partial of the previous chunk
-    // First-half warp only: add the second half's O^T partial of chunk cc (posted
-    // before the pair barrier that preceded this call) and store chunk cc's rows.
-    auto finish_output = [&](int cc) {
-      const float* op = sm.rs.oxch[cc & 1][dvb][lane];
-      const float4 b0 = *reinterpret_cast<const float4*>(op + 0);
-      const float4 b1 = *reinterpret_cast<const float4*>(op + 4);
-      o_prev[0][0] += b0.x; o_prev[0][1] += b0.y; o_prev[0][2] += b0.z; o_prev[0][3] += b0.w;
-      o_prev[1][0] += b1.x; o_prev[1][1] += b1.y; o_prev[1][2] += b1.z; o_prev[1][3] += b1.w;
-      __nv_bfloat16 (&ost)[16][16] = sm.rs.ost[dvb];
+    // O^T partial of the previous chunk, handed to the output warp once the
+    // next chunk's U^T MMAs are issued (its MMAs have completed by then)
+    float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    auto post_output = [&](int cc) {
+      float (*op)[kOPitch] = sm.rs.opart[cc & (kRing - 1)][dkh];
+      const int r = dvb * 16 + g;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         const int tok = 8 * nt + 2 * t;
-        ost[tok][g] = __float2bfloat16_rn(o_prev[nt][0]);
-        ost[tok + 1][g] = __float2bfloat16_rn(o_prev[nt][1]);
-        ost[tok][g + 8] = __float2bfloat16_rn(o_prev[nt][2]);
-        ost[tok + 1][g + 8] = __float2bfloat16_rn(o_prev[nt][3]);
+        op[tok][r] = o[nt][0];
+        op[tok + 1][r] = o[nt][1];
+        op[tok][r + 8] = o[nt][2];
+        op[tok + 1][r + 8] = o[nt][3];
       }
       __syncwarp();
-      const int tok0 = ts + cc * kChunk;
-      const int ntok = min(kChunk, te - tok0);
-      const int row = lane >> 1, hv = lane & 1;
-      if (row < ntok) {
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.o) +
-                             (static_cast<size_t>(tok0 + row) * H + h) * FD + row0 + hv * 8;
-        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&ost[row][hv * 8]);
-      }
-      __syncwarp();
+      if (lane == 0) mbar_arrive_local(&sm.ofull[cc & (kRing - 1)]);
     };
-    for (int c = 0; c < nch; ++c) {
-      const int s = c & (kRing - 1);
-      const uint32_t par = static_cast<uint32_t>(c / kRing) & 1u;
-      if (!failed && !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.full[s])), par,
-                                        kWaitLimitNs)) {
-        failed = true;
-        if (lane == 0) set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
-      }
-      const Stage& st = sm.ring[s];
-      uint32_t sa[4][4];
+    const int brow = ((lane >> 4) << 3) + (lane & 7);
+    const int bcol = ((lane >> 3) & 1) * 8;
+    uint32_t sa[4][4];  // S^T of this warp in bf16 A fragments
+    auto pack_state = [&] {
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         sa[kk][0] = Bf16::pack(S[2 * kk][0], S[2 * kk][1]);
@@ -276,6 +264,16 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         sa[kk][2] = Bf16::pack(S[2 * kk + 1][0], S[2 * kk + 1][1]);
         sa[kk][3] = Bf16::pack(S[2 * kk + 1][2], S[2 * kk + 1][3]);
       }
+    };
+    pack_state();
+    for (int c = 0; c < nch; ++c) {
+      const int s = c & (kRing - 1);
+      const uint32_t par = static_cast<uint32_t>(c / kRing) & 1u;
+      if (!failed && !mbar_wait_bounded(smem_u32(&sm.full[s]), par, kWaitLimitNs)) {
+        failed = true;
+        if (lane == 0) set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
+      }
+      const Stage& st = sm.ring[s];
       float u[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
@@ -287,8 +285,6 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           u[nt][0] = u[nt][1] = u[nt][2] = u[nt][3] = 0.f;
         }
       }
-      const int brow = ((lane >> 4) << 3) + (lane & 7);
-      const int bcol = ((lane >> 3) & 1) * 8;
       if (DELTA) {  // U^T partial over this key half: the serial path; two chains per n-tile
         float u2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         uint32_t b[4][4];
@@ -305,18 +301,12 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
 #pragma unroll
           for (int e = 0; e < 4; ++e) u[nt][e] += u2[nt][e];
       }
-      // O^T = q_dec S_old over this key half, issued behind the U^T MMAs so it
-      // fills their latency; its result is only used after the state update.
-      float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      if (c > 0) post_output(c - 1);
+      // operands of the state update, independent of U: loaded while U settles
+      uint32_t krb[4][4];
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        uint32_t b[4];
-        ldsm_x4(b, &st.qd[brow][kc0 + 16 * kk + bcol]);
-        mma16816<Bf16>(o[0], sa[kk], b[0], b[1]);
-        mma16816<Bf16>(o[1], sa[kk], b[2], b[3]);
-      }
-      // Exchange the two key halves' U^T partial sums (split-K). The same barrier
-      // also hands the first-half warp the second half's O^T partial of chunk c - 1.
+      for (int np = 0; np < 4; ++np) ldsm_x4_trans(krb[np], &st.kr[lane & 15][kc0 + 16 * np + (lane >> 4) * 8]);
+      // Exchange the two key halves' U^T partial sums (split-K).
       {
         float* mine = sm.rs.xch[c & 1][dvb][dkh][lane];
         *reinterpret_cast<float4*>(mine + 0) = make_float4(u[0][0], u[0][1], u[0][2], u[0][3]);
@@ -328,7 +318,6 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         u[0][0] += a0.x; u[0][1] += a0.y; u[0][2] += a0.z; u[0][3] += a0.w;
         u[1][0] += a1.x; u[1][1] += a1.y; u[1][2] += a1.z; u[1][3] += a1.w;
       }
-      if (dkh == 0 && c > 0) finish_output(c - 1);
       uint32_t ua[4];
       ua[0] = ST2::pack(u[0][0], u[0][1]);
       ua[1] = ST2::pack(u[0][2], u[0][3]);
@@ -337,41 +326,36 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       // state update on this warp's key half: S^T = S^T diag(gamma) + U^T k_res
 #pragma unroll
       for (int np = 0; np < 4; ++np) {
-        uint32_t b[4];
-        ldsm_x4_trans(b, &st.kr[lane & 15][kc0 + 16 * np + (lane >> 4) * 8]);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const int nt = 2 * np + half;
           const float2 gm = *reinterpret_cast<const float2*>(&st.gamma[kc0 + 8 * nt + 2 * t]);
           S[nt][0] *= gm.x; S[nt][1] *= gm.y; S[nt][2] *= gm.x; S[nt][3] *= gm.y;
-          mma16816<ST2>(S[nt], ua, b[2 * half], b[2 * half + 1]);
+          mma16816<ST2>(S[nt], ua, krb[np][2 * half], krb[np][2 * half + 1]);
         }
       }
-      // finish this chunk's O^T off the serial path: U^T Mqk^T on the first half;
-      // the second half posts its partial for the first half's next barrier.
-      {
-        if (dkh == 0) {
-          uint32_t b[4];
-          ldsm_x4(b, &st.mqk[brow][bcol]);
-          mma16816<ST2>(o[0], ua, b[0], b[1]);
-          mma16816<ST2>(o[1], ua, b[2], b[3]);
+      // O^T of this chunk behind the state update in the tensor pipe: q_dec S_old
+      // over this key half (S_old is still in sa), plus U^T Mqk^T on the first half
 #pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 2; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) o_prev[nt][e] = o[nt][e];
-        } else {
-          float* dst = sm.rs.oxch[c & 1][dvb][lane];
-          *reinterpret_cast<float4*>(dst + 0) = make_float4(o[0][0], o[0][1], o[0][2], o[0][3]);
-          *reinterpret_cast<float4*>(dst + 4) = make_float4(o[1][0], o[1][1], o[1][2], o[1][3]);
-        }
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t b[4];
+        ldsm_x4(b, &st.qd[brow][kc0 + 16 * kk + bcol]);
+        mma16816<Bf16>(o[0], sa[kk], b[0], b[1]);
+        mma16816<Bf16>(o[1], sa[kk], b[2], b[3]);
       }
+      if (dkh == 0) {
+        uint32_t b[4];
+        ldsm_x4(b, &st.mqk[brow][bcol]);
+        mma16816<ST2>(o[0], ua, b[0], b[1]);
+        mma16816<ST2>(o[1], ua, b[2], b[3]);
+      }
+      pack_state();
       __syncwarp();
       if (lane == 0) mbar_arrive_local(&sm.empty[s]);
     }
-    if (nch > 0) {  // the last chunk's O^T partial from the second half
-      named_bar_sync(2 + dvb, 64);
-      if (dkh == 0) finish_output(nch - 1);
-    }
+    if (nch > 0) post_output(nch - 1);
     if (ok && p.hT != nullptr) {
       float* dst = p.hT + (static_cast<size_t>(n) * H + h) * FD * FD;
 #pragma unroll
@@ -700,7 +684,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       }
       __syncwarp();
     }
-  } else {
+  } else if (warp == 14) {
     // ===================== loader warp =====================
     // TMA loads of the prep groups' input tiles: chunk j + 2 of this CTA goes
     // into group (j mod 2)'s buffer as soon as that group holds chunk j's tiles
@@ -726,6 +710,39 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       }
     }
     __syncwarp();
+  } else {
+    // ===================== output warp =====================
+    // Adds the two key halves' O partials of each chunk, stores the chunk's
+    // 16 x 32 block of o (lane: one token, 16 value rows) and releases the stage.
+    const int tok = lane >> 1, hv = lane & 1;
+    bool failed = false;
+    for (int c = 0; c < nch; ++c) {
+      const int s = c & (kRing - 1);
+      if (!failed &&
+          !mbar_wait_bounded(smem_u32(&sm.ofull[s]), static_cast<uint32_t>(c / kRing) & 1u, kWaitLimitNs)) {
+        failed = true;
+        if (lane == 0) set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
+      }
+      const float* p0 = &sm.rs.opart[s][0][tok][hv * 16];
+      const float* p1 = &sm.rs.opart[s][1][tok][hv * 16];
+      uint32_t pk[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 x = *reinterpret_cast<const float4*>(p0 + 4 * i);
+        const float4 y = *reinterpret_cast<const float4*>(p1 + 4 * i);
+        pk[2 * i] = Bf16::pack(x.x + y.x, x.y + y.y);
+        pk[2 * i + 1] = Bf16::pack(x.z + y.z, x.w + y.w);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_local(&sm.empty[s]);
+      const int tok0 = ts + c * kChunk;
+      if (tok < te - tok0) {  // rows past the sequence end belong to the next sequence
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
+                                              (static_cast<size_t>(tok0 + tok) * H + h) * FD + rank * kRows + hv * 16);
+        dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+      }
+    }
   }
   cluster_sync_all();
   if (rank == 0 && tid == 0 && ring_id >= 0) {  // hand the ring back to the pool

@@ -46,13 +46,18 @@ constexpr int kRing = 4;             // local stages per CTA
 constexpr int kGRing = 16;           // global ring slots per cluster (a multiple of kCtas)
 constexpr int kPool = 40;            // cluster rings in the workspace pool (> clusters resident at once)
 constexpr int kFusedThreads = 512;   // 4 recurrence warps, 2 x 4 prep warps, mover, publisher, loader, output
-constexpr int kPad = FD + 8;         // padded 16-bit row (conflict-free ldmatrix)
+// Channel-major 16-bit tiles [channel][16 tokens]: one channel's 16 tokens are
+// one 32-byte row, so the thread that owns a channel writes it with two 16-byte
+// stores. The two 16-byte halves (tokens 0-7, 8-15) are swapped on rows whose
+// bit 2 is set, so the eight rows one ldmatrix 8x8 load reads fall on distinct
+// banks. cm_off gives the element offset of half `half` of row `row`.
+__device__ __forceinline__ int cm_off(int row, int half) { return row * 16 + ((half ^ (row >> 2)) & 1) * 8; }
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 struct __align__(16) Stage {
-  uint16_t W[16][kPad];    // bf16, -W = -INV diag(beta) k_dec
-  uint16_t qd[16][kPad];   // bf16, scale q e^{G}
-  uint16_t kr[16][kPad];   // st2, k e^{G_last - G}
+  uint16_t W[FD][16];      // bf16, -W^T = -(INV diag(beta) k_dec)^T, channel-major
+  uint16_t qd[FD][16];     // bf16, (scale q e^{G})^T, channel-major
+  uint16_t kr[FD][16];     // st2, (k e^{G_last - G})^T, channel-major
   uint16_t mqk[16][24];    // st2
   float gamma[FD];         // e^{G_last}
   float ut[kRows][16];     // U~ rows of this CTA (transposed)
@@ -63,9 +68,9 @@ constexpr uint32_t kStageTx = kSharedBytes + kUtSliceBytes;
 static_assert(kSharedBytes % 16 == 0 && kStageTx == sizeof(Stage), "stage layout");
 
 struct __align__(16) PrepOut {
-  uint16_t W[16][kPad];
-  uint16_t qd[16][kPad];
-  uint16_t kr[16][kPad];
+  uint16_t W[FD][16];
+  uint16_t qd[FD][16];
+  uint16_t kr[FD][16];
   uint16_t mqk[16][24];
   float gamma[FD];
   float ut[FD][16];  // all value rows
@@ -87,10 +92,10 @@ struct __align__(16) PrepIn {
 
 template <typename Q>
 struct __align__(16) PrepScratch {
-  Q A_lv[4][16][kPad];
-  Q B_lv[4][8][kPad];
-  Q kdec[16][kPad];
-  __nv_bfloat16 vs[16][kPad];
+  Q A_lv[4][FD][16];          // per level: [channel][row], channel-major
+  Q B_lv[4][FD][8];           // per level: [channel][column]
+  Q kdec[FD][16];             // channel-major
+  __nv_bfloat16 vs[FD][16];   // channel-major
   float Lm[16][17];
   float Mq[16][17];
   float red[4][48];
@@ -255,6 +260,12 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     };
     const int brow = ((lane >> 4) << 3) + (lane & 7);
     const int bcol = ((lane >> 3) & 1) * 8;
+    // ldmatrix rows of the channel-major tiles. B fragments of a [K][N]-stored
+    // operand (W^T, q_dec^T: K = channel) come from .trans loads, lane matrix m =
+    // (n-tile m >> 1, k half m & 1); those of an [N][K]-stored one (k_res^T:
+    // N = channel) from plain loads, m = (n-tile m >> 1, token half m & 1).
+    const int tm_row = ((lane >> 3) & 1) * 8 + (lane & 7), tm_half = lane >> 4;
+    const int nm_row = (lane >> 4) * 8 + (lane & 7), nm_half = (lane >> 3) & 1;
     uint32_t sa[4][4];  // S^T of this warp in bf16 A fragments
     auto pack_state = [&] {
 #pragma unroll
@@ -289,7 +300,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         float u2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         uint32_t b[4][4];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) ldsm_x4(b[kk], &st.W[brow][kc0 + 16 * kk + bcol]);
+        for (int kk = 0; kk < 4; ++kk) ldsm_x4_trans(b[kk], &st.W[0][0] + cm_off(kc0 + 16 * kk + tm_row, tm_half));
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           float (&acc)[2][4] = (kk & 1) ? u2 : u;
@@ -305,7 +316,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       // operands of the state update, independent of U: loaded while U settles
       uint32_t krb[4][4];
 #pragma unroll
-      for (int np = 0; np < 4; ++np) ldsm_x4_trans(krb[np], &st.kr[lane & 15][kc0 + 16 * np + (lane >> 4) * 8]);
+      for (int np = 0; np < 4; ++np) ldsm_x4(krb[np], &st.kr[0][0] + cm_off(kc0 + 16 * np + nm_row, nm_half));
       // Exchange the two key halves' U^T partial sums (split-K).
       {
         float* mine = sm.rs.xch[c & 1][dvb][dkh][lane];
@@ -341,7 +352,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) {
         uint32_t b[4];
-        ldsm_x4(b, &st.qd[brow][kc0 + 16 * kk + bcol]);
+        ldsm_x4_trans(b, &st.qd[0][0] + cm_off(kc0 + 16 * kk + tm_row, tm_half));
         mma16816<Bf16>(o[0], sa[kk], b[0], b[1]);
         mma16816<Bf16>(o[1], sa[kk], b[2], b[3]);
       }
@@ -382,14 +393,15 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     const float dtb = (p.gate_mode == 2) ? p.dt_bias[h * FD + pt] : 0.f;
     bool failed = false;
     int c = static_cast<int>(rank) + kCtas * grp;
-    // beta is loaded raw one producer step ahead; its sigmoid is taken when it
-    // is stored, so the load latency never sits on the prep's critical path.
-    float beta_next = 0.f;
+    // beta is loaded one step of this group ahead and kept as raw bits until
+    // it is used (converting right after the load would wait for it there);
+    // its sigmoid is taken when it is stored, off the load's latency.
+    unsigned short beta_next = 0;
     auto load_beta = [&](int cc) {
-      float raw = 0.f;
+      unsigned short raw = 0;
       const int tk0 = ts + cc * kChunk;
       if (DELTA && pt < 16 && tk0 + pt < te)
-        raw = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.beta)[static_cast<size_t>(tk0 + pt) * H + h]);
+        raw = reinterpret_cast<const unsigned short*>(p.beta)[static_cast<size_t>(tk0 + pt) * H + h];
       return raw;
     };
     if (c < nch) beta_next = load_beta(c);
@@ -397,7 +409,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       const int buf = grp;
       const int tok0 = ts + c * kChunk;
       const int ntok = min(kChunk, te - tok0);
-      const float beta_cur = beta_next;
+      const float beta_cur = __bfloat162float(__ushort_as_bfloat16(beta_next));
       if (c + 2 * kCtas < nch) beta_next = load_beta(c + 2 * kCtas);
       if (!failed && !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pinbar[buf])),
                                         static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs)) {
@@ -505,16 +517,26 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
 #pragma unroll
       for (int i = 14; i >= 0; --i) Rs[i] = Rs[i + 1] * al[i + 1];
       {
+        // channel pt's 16 tokens of each channel-major tile, two 16-byte stores each
+        auto put16 = [&](uint16_t* tile, const uint32_t (&w)[8]) {
+          *reinterpret_cast<uint4*>(tile + cm_off(pt, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(tile + cm_off(pt, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+        };
+        uint32_t w[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const __nv_bfloat16 qd = __float2bfloat16_rn(p.scale * qv[i] * P[i]);
-          po.qd[i][pt] = *reinterpret_cast<const uint16_t*>(&qd);
-          const typename ST2::T kr = ST2::cvt(kv[i] * Rs[i]);
-          po.kr[i][pt] = *reinterpret_cast<const uint16_t*>(&kr);
-          if (DELTA) {
-            ps.kdec[i][pt] = QK::cvt(kv[i] * P[i]);
-            ps.vs[i][pt] = __float2bfloat16_rn(vv[i]);
-          }
+        for (int i = 0; i < 8; ++i)
+          w[i] = Bf16::pack(p.scale * qv[2 * i] * P[2 * i], p.scale * qv[2 * i + 1] * P[2 * i + 1]);
+        put16(&po.qd[0][0], w);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = ST2::pack(kv[2 * i] * Rs[2 * i], kv[2 * i + 1] * Rs[2 * i + 1]);
+        put16(&po.kr[0][0], w);
+        if (DELTA) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[i] = QK::pack(kv[2 * i] * P[2 * i], kv[2 * i + 1] * P[2 * i + 1]);
+          put16(reinterpret_cast<uint16_t*>(&ps.kdec[0][0]), w);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[i] = Bf16::pack(vv[2 * i], vv[2 * i + 1]);
+          put16(reinterpret_cast<uint16_t*>(&ps.vs[0][0]), w);
         }
         po.gamma[pt] = P[15];
         if (!DELTA) {
@@ -525,6 +547,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
 #pragma unroll
         for (int lv = 0; lv < 4; ++lv) {
           const int s = 8 >> lv;
+          float ar[16], bc[8];  // this channel's row (k rows 0-7, q rows 8-15) and column operands
 #pragma unroll
           for (int blk = 0; blk < 8 / s; ++blk) {
             const int m = blk * 2 * s + s;
@@ -533,16 +556,21 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
             for (int i = m; i < m + s; ++i) {
               if (i > m) f *= al[i];
               const int r = blk * s + (i - m);
-              if (DELTA) ps.A_lv[lv][r][pt] = QK::cvt(kv[i] * f);
-              ps.A_lv[lv][8 + r][pt] = QK::cvt(qv[i] * f);
+              ar[r] = DELTA ? kv[i] * f : 0.f;
+              ar[8 + r] = qv[i] * f;
             }
             f = 1.f;
 #pragma unroll
             for (int i = m - 1; i >= m - s; --i) {
               f *= al[i + 1];
-              ps.B_lv[lv][blk * s + (i - (m - s))][pt] = QK::cvt(kv[i] * f);
+              bc[blk * s + (i - (m - s))] = kv[i] * f;
             }
           }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) w[i] = QK::pack(ar[2 * i], ar[2 * i + 1]);
+          put16(reinterpret_cast<uint16_t*>(&ps.A_lv[lv][0][0]), w);
+          *reinterpret_cast<uint4*>(&ps.B_lv[lv][pt][0]) =
+              make_uint4(QK::pack(bc[0], bc[1]), QK::pack(bc[2], bc[3]), QK::pack(bc[4], bc[5]), QK::pack(bc[6], bc[7]));
         }
       }
       prep_bar();
@@ -553,8 +581,10 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
 #pragma unroll
         for (int kk = 0; kk < FD / 16; ++kk) {
           uint32_t a[4], b[2];
-          ldsm_x4(a, &ps.A_lv[lv][lane & 15][16 * kk + (lane >> 4) * 8]);
-          ldsm_x2(b, &ps.B_lv[lv][lane & 7][16 * kk + ((lane >> 3) & 1) * 8]);
+          // A^T and B^T are stored [channel][row]: .trans loads; lane matrix m of
+          // A = (row half m & 1, channel half m >> 1)
+          ldsm_x4_trans(a, &ps.A_lv[lv][0][0] + cm_off(16 * kk + (lane >> 4) * 8 + (lane & 7), (lane >> 3) & 1));
+          ldsm_x2_trans(b, &ps.B_lv[lv][16 * kk + (lane & 15)][0]);
           mma16816<QK>(acc, a, b[0], b[1]);
         }
         const int g = lane >> 2, t = lane & 3;
@@ -599,15 +629,17 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         for (int pp = 0; pp < 2; ++pp) {
           const int n0 = pw * 32 + 16 * pp;
           uint32_t b[4];
-          ldsm_x4_trans(b, &ps.kdec[lane & 15][n0 + (lane >> 4) * 8]);
+          ldsm_x4(b, &ps.kdec[0][0] + cm_off(n0 + (lane >> 4) * 8 + (lane & 7), (lane >> 3) & 1));
           float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
           mma16816<QK>(c0, a, b[0], b[1]);
           mma16816<QK>(c1, a, b[2], b[3]);
-          *reinterpret_cast<uint32_t*>(&po.W[g][n0 + 2 * t]) = Bf16::pack(-c0[0], -c0[1]);
-          *reinterpret_cast<uint32_t*>(&po.W[g + 8][n0 + 2 * t]) = Bf16::pack(-c0[2], -c0[3]);
-          *reinterpret_cast<uint32_t*>(&po.W[g][n0 + 8 + 2 * t]) = Bf16::pack(-c1[0], -c1[1]);
-          *reinterpret_cast<uint32_t*>(&po.W[g + 8][n0 + 8 + 2 * t]) = Bf16::pack(-c1[2], -c1[3]);
-          ldsm_x4_trans(b, &ps.vs[lane & 15][n0 + (lane >> 4) * 8]);
+          // -W blocks (tokens x 8 channels) transposed in registers into -W^T rows
+          uint16_t* wt = &po.W[0][0];
+          *reinterpret_cast<uint32_t*>(wt + cm_off(n0 + g, 0) + 2 * t) = movmatrix_trans(Bf16::pack(-c0[0], -c0[1]));
+          *reinterpret_cast<uint32_t*>(wt + cm_off(n0 + g, 1) + 2 * t) = movmatrix_trans(Bf16::pack(-c0[2], -c0[3]));
+          *reinterpret_cast<uint32_t*>(wt + cm_off(n0 + 8 + g, 0) + 2 * t) = movmatrix_trans(Bf16::pack(-c1[0], -c1[1]));
+          *reinterpret_cast<uint32_t*>(wt + cm_off(n0 + 8 + g, 1) + 2 * t) = movmatrix_trans(Bf16::pack(-c1[2], -c1[3]));
+          ldsm_x4(b, &ps.vs[0][0] + cm_off(n0 + (lane >> 4) * 8 + (lane & 7), (lane >> 3) & 1));
           float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};
           mma16816<Bf16>(u0, ahi, b[0], b[1]);
           mma16816<Bf16>(u0, alo, b[0], b[1]);

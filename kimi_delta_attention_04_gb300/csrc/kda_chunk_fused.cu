@@ -14,15 +14,16 @@
 //    O^T partial (q_dec S over its key half, plus U^T Mqk^T on the first half)
 //    is computed behind the state update and staged in shared memory; an
 //    output warp adds the halves and stores o, off the serial path.
-//  * The same CTA's four prep warps prepare every 4th chunk (chunks c = r mod 4):
+//  * The same CTA's prep warps prepare every 4th chunk (chunks c = r mod 4):
 //    gate, beta, L2 norm, decay products, L / Mqk, Neumann inverse, W and U~.
-//    A helper warp loads their input tiles with TMA two chunks ahead.
+//    Two groups of four warps take alternate ones, each loading its next
+//    chunk's input tiles with TMA as soon as the current ones are in registers.
 //  * Prepared chunks travel through a ring of kGRing slots in global memory
 //    (L2-resident; one ring per cluster, taken from a pool in the workspace):
-//    the prep warps copy the chunk from shared memory into slot c mod kGRing
-//    with 16-byte stores; the helper warp then publishes it at cluster scope
-//    (fence.acq_rel.cluster) and arrives on the slot's "ready" mbarrier in all
-//    four CTAs. Each CTA's mover warp bulk-loads the shared operands and its
+//    the prep warps write the chunk straight into slot c mod kGRing (mostly
+//    16-byte stores of channel-major tiles); the publisher warp then makes it
+//    visible at cluster scope (fence.acq_rel.cluster) and arrives on the
+//    slot's "ready" mbarrier in all four CTAs. Each CTA's mover warp bulk-loads the shared operands and its
 //    own 32 rows of U~ into local stage c mod kRing and, when its recurrence
 //    warps release that stage, hands the global slot back to the producer
 //    ("gfree"). On GB300 an L2 bulk load delivers ~50 B/clk per SM against
@@ -45,7 +46,7 @@ constexpr int kRows = FD / kCtas;    // value rows per CTA
 constexpr int kRing = 4;             // local stages per CTA
 constexpr int kGRing = 16;           // global ring slots per cluster (a multiple of kCtas)
 constexpr int kPool = 40;            // cluster rings in the workspace pool (> clusters resident at once)
-constexpr int kFusedThreads = 512;   // 4 recurrence warps, 2 x 4 prep warps, mover, publisher, loader, output
+constexpr int kFusedThreads = 480;   // 4 recurrence warps, 2 x 4 prep warps, mover, publisher, output
 // Channel-major 16-bit tiles [channel][16 tokens]: one channel's 16 tokens are
 // one 32-byte row, so the thread that owns a channel writes it with two 16-byte
 // stores. The two 16-byte halves (tokens 0-7, 8-15) are swapped on rows whose
@@ -118,11 +119,10 @@ struct __align__(128) FusedSmem {
   uint64_t full[kRing];            // stage loaded (mover's bulk loads -> recurrence)
   uint64_t empty[kRing];           // stage released by the 4 recurrence warps and the output warp (-> mover)
   uint64_t ofull[kRing];           // O partials of the stage's chunk written (recurrence -> output warp)
-  uint64_t ready[kGRing];          // global slot written and published (producer's helper -> every mover)
+  uint64_t ready[kGRing];          // global slot written and published (producer's publisher -> every mover)
   uint64_t gfree[kGRing];          // global slot read by all 4 CTAs (movers -> producer's prep)
   uint64_t sig[kGRing / kCtas];    // this CTA's slot written (prep -> publisher)
   uint64_t pinbar[2];              // input tiles of group g loaded (TMA -> prep)
-  uint64_t pinfree[2];             // input tiles of group g read into registers (prep -> loader)
   int ring_id;                     // pool ring of this cluster (CTA 0's copy is authoritative)
 };
 
@@ -207,7 +207,6 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     for (int i = 0; i < kGRing / kCtas; ++i) mbar_init(&sm.sig[i], 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.pinbar[b], 1);
-      mbar_init(&sm.pinfree[b], 1);
     }
     sm.ring_id = (rank == 0 && nch0 > 0) ? claim_ring(p.records, p.err) : -1;
     fence_mbarrier_init_cluster();
@@ -405,6 +404,23 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       return raw;
     };
     if (c < nch) beta_next = load_beta(c);
+    // Each group loads its own input tiles with TMA: the first chunk's now,
+    // chunk c + 8's as soon as chunk c's are in registers.
+    if (pt == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.q) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.k) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.v) : "memory");
+      if (p.gate_mode != 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.a) : "memory");
+      if (c < nch) issue_inputs(maps, sm.pin[grp], &sm.pinbar[grp], h, ts + c * kChunk, p.gate_mode);
+    }
+    // The hand-off of a written chunk to the publisher (a release at CTA scope)
+    // is made after the next chunk's first barrier: right after the slot
+    // stores it would wait for their L2 acknowledgements.
+    int sig_pending = -1;
+    auto signal_written = [&] {
+      if (pt == 0 && sig_pending >= 0) mbar_arrive_local(&sm.sig[sig_pending % (kGRing / kCtas)]);
+      sig_pending = -1;
+    };
     for (int j = grp; c < nch; j += 2, c += 2 * kCtas) {
       const int buf = grp;
       const int tok0 = ts + c * kChunk;
@@ -434,6 +450,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         ps.beta[pt] = (DELTA && pt < ntok) ? bt : 0.f;
       }
       prep_bar();
+      signal_written();
       const PrepIn& in = sm.pin[buf];
       float qv[16], kv[16], al[16], vv[16];
 #pragma unroll
@@ -488,7 +505,8 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       }
       fence_proxy_async_smem();  // the reads of pin[buf] precede the next TMA write into it
       prep_bar();
-      if (pt == 0) mbar_arrive_local(&sm.pinfree[buf]);
+      if (pt == 0 && c + 2 * kCtas < nch)
+        issue_inputs(maps, sm.pin[buf], &sm.pinbar[buf], h, ts + (c + 2 * kCtas) * kChunk, p.gate_mode);
       if (pt < 16) {
         float sq = 0.f, sk = 0.f, sqk = 0.f;
 #pragma unroll
@@ -656,8 +674,9 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         }
       }
       prep_bar();  // every store into the slot precedes the hand-off
-      if (pt == 0) mbar_arrive_local(&sm.sig[j % (kGRing / kCtas)]);
+      sig_pending = j;
     }
+    signal_written();
   } else if (warp == 12) {
     // ===================== mover warp =====================
     // Loads chunk c from its global slot into local stage c mod kRing once the
@@ -716,32 +735,6 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       }
       __syncwarp();
     }
-  } else if (warp == 14) {
-    // ===================== loader warp =====================
-    // TMA loads of the prep groups' input tiles: chunk j + 2 of this CTA goes
-    // into group (j mod 2)'s buffer as soon as that group holds chunk j's tiles
-    // in registers.
-    if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.q) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.k) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.v) : "memory");
-      if (p.gate_mode != 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.a) : "memory");
-      for (int jj = 0; jj < 2; ++jj) {
-        const int cc = static_cast<int>(rank) + jj * kCtas;
-        if (cc < nch) issue_inputs(maps, sm.pin[jj], &sm.pinbar[jj], h, ts + cc * kChunk, p.gate_mode);
-      }
-      bool failed = false;
-      for (int j = 0, c = static_cast<int>(rank); c + 2 * kCtas < nch; ++j, c += kCtas) {
-        const int g = j & 1;
-        if (!failed && !mbar_wait_bounded(smem_u32(&sm.pinfree[g]), static_cast<uint32_t>(j >> 1) & 1u,
-                                          kWaitLimitNs)) {
-          failed = true;
-          set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
-        }
-        issue_inputs(maps, sm.pin[g], &sm.pinbar[g], h, ts + (c + 2 * kCtas) * kChunk, p.gate_mode);
-      }
-    }
-    __syncwarp();
   } else {
     // ===================== output warp =====================
     // Adds the two key halves' O partials of each chunk, stores the chunk's

@@ -469,16 +469,16 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float x = in.a[i][pt] + dtb;
-          const float l2 = __log2f(1.f + exp2f(fminf(x, 20.f) * kLog2e));
+          const float l2 = lg2_approx(1.f + ex2_approx(fminf(x, 20.f) * kLog2e));
           const float sp2 = x > 20.f ? x * kLog2e : l2;  // softplus(x) in log2 units
-          const float a = exp2f(nA * sp2);
+          const float a = ex2_approx(nA * sp2);
           al[i] = i < ntok ? a : 1.f;
         }
       } else if (p.gate_mode == 1) {
         constexpr float kLog2e = 1.4426950408889634f;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float a = exp2f(in.a[i][pt] * kLog2e);
+          const float a = ex2_approx(in.a[i][pt] * kLog2e);
           al[i] = i < ntok ? a : 1.f;
         }
       } else {

@@ -225,6 +225,21 @@ __device__ __forceinline__ Frag16 neumann_inverse16(const float* L, int ld, int 
   return frag_mm<Op>(P2, frag_plus_identity(X8, lane));
 }
 
+// 2^x and log2(x) straight from the special-function unit (PTX ex2.approx /
+// lg2.approx: relative error about 2^-22; ftz: results below 2^-126 become 0).
+// The decay factors need absolute accuracy near 1e-7 only, which these give in
+// one instruction each.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // softplus with the usual linear branch above 20 (the two differ by < 2.1e-9 there).
 __device__ __forceinline__ float softplus_f(float x) { return x <= 20.f ? log1pf(expf(x)) : x; }
 

@@ -1,4 +1,5 @@
-"""Plain fp64 CPU oracle for the KDA chunk forward and the fused T=1 decode step.
+"""Plain fp64 CPU oracle for the KDA chunk forward, the fused T=1 decode step and
+the short-T recurrent step on a state pool.
 
 TEST INFRASTRUCTURE ONLY: imported by tests/, __graft_entry__.smoke() and the
 CPU-baseline legs of bench.py, never by the CUDA path (and it imports nothing
@@ -350,6 +351,55 @@ def kda_decode(packed_qkv, a, b, A_log, dt_bias, state_pool, indices, *,
             k = l2_normalize(k)
         S = pool[s].transpose(0, 2, 1)                         # [HV, K, V]
         S, o[row] = _token_step(S, q, k, v_all[row], g_all[row], beta_all[row], scale, True)
+        pool[s] = S.transpose(0, 2, 1)
+    return o, pool
+
+
+def kda_recurrent_pool(q, k, v, a, b, A_log, dt_bias, state_pool, indices, *,
+                       scale, l2norm_qk=True):
+    """T tokens per batch row on a state-slot pool: the general fused recurrent
+    step that the packed decode specialises ([PR] 功能与动机 and 实现拆解: the
+    packed kernel replaces the generic path for one token per row; speculative
+    and extend steps run several). Same recurrence, gate, beta, L2 norm, head
+    grouping and pad convention as kda_decode.
+
+    q, k: [B, T, H, K]; v: [B, T, HV, V]; a: [B, T, HV*K]; b: [B, T, HV] (beta
+    logits); A_log: [HV]; dt_bias: [HV*K]; state_pool: [num_slots, HV, V, K]
+    (stored layout); indices: [B] int, -1 = pad. Value head hv reads query/key
+    head hv // (HV // H). Tokens of a row are applied in order to its slot's
+    state. Returns (o [B, T, HV, V], new_pool); the input pool is not modified.
+    Pad rows get o = 0 and touch no state. Valid indices must be distinct.
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    pool = np.array(np.asarray(state_pool, np.float64))
+    idx = np.asarray(indices).astype(np.int64)
+    Bn, T, H, K = q.shape
+    HV, V = v.shape[2], v.shape[3]
+    valid = idx[idx >= 0]
+    if len(set(valid.tolist())) != len(valid):
+        raise ValueError("valid slot indices must be distinct")
+    if HV % H:
+        raise ValueError("HV must be a multiple of H")
+    heads = np.arange(HV) // (HV // H)
+    g_all = kda_gate(a.reshape(Bn, T, HV, K), np.asarray(dt_bias, np.float64).reshape(HV, K), A_log)
+    beta_all = sigmoid(b)
+    o = np.zeros((Bn, T, HV, V))
+    for row in range(Bn):
+        s = int(idx[row])
+        if s < 0:
+            continue
+        S = pool[s].transpose(0, 2, 1)                         # [HV, K, V]
+        for t in range(T):
+            qt = q[row, t][heads]
+            kt = k[row, t][heads]
+            if l2norm_qk:
+                qt = l2_normalize(qt)
+                kt = l2_normalize(kt)
+            S, o[row, t] = _token_step(S, qt, kt, v[row, t], g_all[row, t], beta_all[row, t], scale, True)
         pool[s] = S.transpose(0, 2, 1)
     return o, pool
 

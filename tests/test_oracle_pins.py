@@ -355,12 +355,56 @@ def pin_value_split_invariance():
         np.testing.assert_allclose(h2, h[:, cols], rtol=1e-14, atol=1e-15)
 
 
+def pin_recurrent_pool_is_repeated_decode():
+    """T tokens per row on the pool equal T successive packed decode steps, each
+    fed the pool the previous one returned (the recurrent step is the decode
+    step applied token by token), with HV = 2 H grouping and a pad row."""
+    r = _rng(16)
+    B, T, H, HV, K, V = 3, 4, 2, 4, 4, 3
+    q = r.standard_normal((B, T, H, K))
+    k = r.standard_normal((B, T, H, K))
+    v = r.standard_normal((B, T, HV, V))
+    a = r.standard_normal((B, T, HV * K))
+    bb = r.standard_normal((B, T, HV))
+    A_log = r.uniform(0, 1, HV)
+    dt = r.uniform(-1, 1, HV * K)
+    pool = r.standard_normal((5, HV, V, K))
+    idx = np.array([3, -1, 0])
+    o, newp = ko.kda_recurrent_pool(q, k, v, a, bb, A_log, dt, pool, idx, scale=0.5)
+    p = pool
+    for t in range(T):
+        packed = np.concatenate([q[:, t].reshape(B, -1), k[:, t].reshape(B, -1), v[:, t].reshape(B, -1)], axis=1)
+        ot, p = ko.kda_decode(packed, a[:, t], bb[:, t], A_log, dt, p, idx, H=H, HV=HV, K=K, V=V, scale=0.5)
+        np.testing.assert_allclose(o[:, t], ot, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(newp, p, rtol=1e-13, atol=1e-14)
+    assert np.all(o[1] == 0.0) and np.array_equal(newp[1], pool[1])
+
+
+def pin_recurrent_pool_tokens_matter():
+    """Swapping two tokens of a row changes the result (the steps do not
+    commute), and a one-token call equals the decode golden's row layout."""
+    r = _rng(17)
+    B, T, H, K, V = 1, 3, 1, 4, 4
+    q = r.standard_normal((B, T, H, K))
+    k = r.standard_normal((B, T, H, K))
+    v = r.standard_normal((B, T, H, V))
+    a = r.standard_normal((B, T, H * K))
+    bb = r.standard_normal((B, T, H))
+    pool = r.standard_normal((2, H, V, K))
+    args = (r.uniform(0, 1, H), r.uniform(-1, 1, H * K), pool, np.array([1]))
+    o, p = ko.kda_recurrent_pool(q, k, v, a, bb, *args, scale=0.5)
+    perm = [1, 0, 2]
+    o2, p2 = ko.kda_recurrent_pool(q[:, perm], k[:, perm], v[:, perm], a[:, perm], bb[:, perm], *args, scale=0.5)
+    assert _rel(p2, p) > 1e-3 and _rel(o2[:, 2], o[:, 2]) > 1e-3
+
+
 PINS = [
     pin_hand_worked_chunk, pin_level1_quadratic_form, pin_level1_chunk_identity,
     pin_gla_parallel_form, pin_retnet_scalar_decay, pin_chunked_equals_recurrent,
     pin_L_nilpotent_and_inverse, pin_chunk_matrices_brute_force, pin_delta_exact_write,
     pin_beta_zero_pure_decay, pin_orthonormal_keys, pin_gate_sigmoid_l2norm,
     pin_decode_golden, pin_decode_head_grouping, pin_split_sequence, pin_value_split_invariance,
+    pin_recurrent_pool_is_repeated_decode, pin_recurrent_pool_tokens_matter,
 ]
 
 
@@ -483,6 +527,29 @@ def _cm_no_beta(q, k, g, beta, scale):
 
 
 _orig_chunk_matrices = ko.chunk_matrices
+_orig_recurrent_pool = ko.kda_recurrent_pool
+
+
+def _rp_reversed_tokens(q, k, v, a, b, *args, **kw):
+    return _orig_recurrent_pool(q[:, ::-1], k[:, ::-1], v[:, ::-1], a[:, ::-1], b[:, ::-1], *args, **kw)
+
+
+def _rp_group_by_modulo(q, k, v, a, b, A_log, dt_bias, state_pool, indices, *, scale, l2norm_qk=True):
+    H, HV = q.shape[2], v.shape[2]
+    qm = np.asarray(q)[:, :, np.arange(HV) % H]
+    km = np.asarray(k)[:, :, np.arange(HV) % H]
+    return _orig_recurrent_pool(qm, km, v, a, b, A_log, dt_bias, state_pool, indices, scale=scale,
+                                l2norm_qk=l2norm_qk)
+
+
+def _rp_state_not_carried(q, k, v, a, b, A_log, dt_bias, state_pool, indices, *, scale, l2norm_qk=True):
+    outs = []
+    for t in range(np.asarray(q).shape[1]):
+        ot, newp = _orig_recurrent_pool(q[:, t:t + 1], k[:, t:t + 1], v[:, t:t + 1], a[:, t:t + 1], b[:, t:t + 1],
+                                        A_log, dt_bias, state_pool, indices, scale=scale, l2norm_qk=l2norm_qk)
+        outs.append(ot)
+    return np.concatenate(outs, axis=1), newp
+
 
 MUTANTS = [
     ("_token_step", _step_decay_after_write),
@@ -501,6 +568,9 @@ MUTANTS = [
     ("chunk_matrices", _cm_exclusive_cumsum),
     ("chunk_matrices", _cm_diag_in_L),
     ("chunk_matrices", _cm_no_beta),
+    ("kda_recurrent_pool", _rp_reversed_tokens),
+    ("kda_recurrent_pool", _rp_group_by_modulo),
+    ("kda_recurrent_pool", _rp_state_not_carried),
 ]
 
 

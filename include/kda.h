@@ -5,6 +5,7 @@
  *   kda_chunk_fwd             chunkwise KDA forward over one batch of sequences
  *   kda_chunk_workspace_size  scratch bytes kda_chunk_fwd needs for given arguments
  *   kda_decode_step           fused T=1 decode step on a packed q|k|v row with a slot pool
+ *   kda_recurrent_step        T tokens per row (T <= 64) on a slot pool: speculative / extend steps
  *   kda_chunk_fwd_noalloc     kda_chunk_fwd on a library-owned scratch buffer (no allocation)
  *   kda_version               library version string
  *
@@ -183,6 +184,54 @@ typedef struct kda_decode_args {
 
 /* Fused T=1 decode step. Returns KDA_OK once the work is enqueued. */
 kda_status kda_decode_step(const kda_decode_args* args, kda_stream_t stream);
+
+/*
+ * Arguments of kda_recurrent_step: T tokens per batch row on a state-slot pool.
+ * This is the general fused recurrent step that the packed decode specialises
+ * (sglang PR #26586 summary, 功能与动机 and 实现拆解: the packed kernel takes over
+ * the generic path for one token per row); several tokens per row occur in
+ * speculative and extend steps.
+ *
+ *   q, k       [B, T, H, K]          bf16
+ *   v          [B, T, HV, V]         bf16
+ *   a          [B, T, HV*K]          bf16  gate input
+ *   b          [B, T, HV]            bf16  beta logits (beta = sigmoid(b))
+ *   A_log      [HV]                  fp32
+ *   dt_bias    [HV*K]                fp32
+ *   state_pool [num_slots, HV, V, K] fp32, updated IN PLACE for the valid rows
+ *   indices    [B]                   int32 slot of each row; negative = padding row
+ *   o          [B, T, HV, V]         bf16
+ * The T tokens of a row are applied to its slot's state in order. Everything
+ * else is as for kda_decode_step: value head hv uses query/key head
+ * hv / (HV / H); the gate, beta, L2 norm (KDA_FLAG_L2NORM_QK) and scaling of q;
+ * a padding row writes o = 0 for all its tokens and touches no state; valid
+ * indices must be distinct; an index >= num_slots writes KDA_ERR_INVALID_ARG
+ * to err, zeroes that row's o and touches no state.
+ * Supported: K, V in {64, 128}; 1 <= T <= KDA_RECURRENT_MAX_T (longer
+ * sequences belong to kda_chunk_fwd). q, k, v, a, dt_bias, state_pool and o
+ * must be 16-byte aligned.
+ */
+#define KDA_RECURRENT_MAX_T 64
+typedef struct kda_recurrent_args {
+  int32_t B, T, H, HV, K, V;
+  int32_t num_slots;
+  uint32_t flags;      /* KDA_FLAG_L2NORM_QK */
+  float scale;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* a;
+  const void* b;
+  const float* A_log;
+  const float* dt_bias;
+  float* state_pool;
+  const int32_t* indices;
+  void* o;
+  int32_t* err;        /* optional device status word */
+} kda_recurrent_args;
+
+/* Short-T recurrent step. Returns KDA_OK once the work is enqueued. */
+kda_status kda_recurrent_step(const kda_recurrent_args* args, kda_stream_t stream);
 
 /*
  * Chunk forward for callers that cannot allocate device memory.

@@ -1,4 +1,5 @@
-"""GB300-native Kimi Delta Attention: chunkwise forward and fused T=1 decode.
+"""GB300-native Kimi Delta Attention: chunkwise forward, fused T=1 decode and the
+short-T recurrent step on a state pool.
 
 The computation lives in libkda.so (hand-written sm_103a CUDA behind the C ABI
 of include/kda.h); this package is its thin Python binding. Importing the
@@ -12,10 +13,12 @@ from ._lib import (  # noqa: F401
     kda_chunk_fwd,
     kda_chunk_fwd_noalloc,
     kda_decode_step,
+    kda_recurrent_step,
     lib_path,
     load,
     make_chunk_args,
     make_decode_args,
+    make_recurrent_args,
     version,
 )
 

@@ -66,8 +66,22 @@ class DecodeArgs(ctypes.Structure):
     ]
 
 
+class RecurrentArgs(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32), ("HV", ctypes.c_int32),
+        ("K", ctypes.c_int32), ("V", ctypes.c_int32), ("num_slots", ctypes.c_int32), ("flags", ctypes.c_uint32),
+        ("scale", ctypes.c_float),
+        ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("a", ctypes.c_void_p),
+        ("b", ctypes.c_void_p), ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
+        ("state_pool", ctypes.c_void_p), ("indices", ctypes.c_void_p), ("o", ctypes.c_void_p),
+        ("err", ctypes.c_void_p),
+    ]
+
+
+KDA_RECURRENT_MAX_T = 64
+
 EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_chunk_workspace_size", "kda_decode_step",
-           "kda_version")
+           "kda_recurrent_step", "kda_version")
 
 
 def lib_path() -> Path:
@@ -91,6 +105,8 @@ def load() -> ctypes.CDLL:
         lib.kda_chunk_workspace_size.argtypes = [ctypes.POINTER(ChunkArgs)]
         lib.kda_decode_step.restype = ctypes.c_int
         lib.kda_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
+        lib.kda_recurrent_step.restype = ctypes.c_int
+        lib.kda_recurrent_step.argtypes = [ctypes.POINTER(RecurrentArgs), ctypes.c_void_p]
         lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
         lib.kda_chunk_fwd_noalloc.argtypes = [ctypes.POINTER(ChunkArgs), ctypes.c_void_p]
         lib.kda_version.restype = ctypes.c_char_p
@@ -249,4 +265,34 @@ def kda_decode_step(packed_qkv, a, b, A_log, dt_bias, state_pool, indices, *, H,
     st = lib.kda_decode_step(ctypes.byref(args), _stream_ptr(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_decode_step")
+    return o
+
+
+def make_recurrent_args(q, k, v, a, b, A_log, dt_bias, state_pool, indices, *, scale, l2norm_qk=True,
+                        o=None, err=None):
+    args = RecurrentArgs()
+    args.B, args.T, args.H, args.K = (int(x) for x in q.shape)
+    args.HV, args.V = int(v.shape[2]), int(v.shape[3])
+    args.num_slots = state_pool.shape[0]
+    args.flags = KDA_FLAG_L2NORM_QK if l2norm_qk else 0
+    args.scale = float(scale)
+    args.q, args.k, args.v, args.a, args.b = _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b)
+    args.A_log, args.dt_bias = _ptr(A_log), _ptr(dt_bias)
+    args.state_pool, args.indices = _ptr(state_pool), _ptr(indices)
+    args.o, args.err = _ptr(o), _ptr(err)
+    return args
+
+
+def kda_recurrent_step(q, k, v, a, b, A_log, dt_bias, state_pool, indices, *, scale, l2norm_qk=True,
+                       o=None, err=None, stream=None):
+    """T tokens per row (q, k [B, T, H, K]; v [B, T, HV, V]; a [B, T, HV*K]; b [B, T, HV])
+    through libkda on the slot pool, updated in place. Returns o [B, T, HV, V] bf16."""
+    lib = load()
+    if o is None:
+        o = torch.empty(q.shape[0], q.shape[1], v.shape[2], v.shape[3], dtype=torch.bfloat16, device=q.device)
+    args = make_recurrent_args(q, k, v, a, b, A_log, dt_bias, state_pool, indices, scale=scale,
+                               l2norm_qk=l2norm_qk, o=o, err=err)
+    st = lib.kda_recurrent_step(ctypes.byref(args), _stream_ptr(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_recurrent_step")
     return o

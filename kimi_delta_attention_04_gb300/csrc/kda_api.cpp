@@ -172,6 +172,51 @@ kda_status kda_decode_step(const kda_decode_args* a, kda_stream_t stream) {
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status kda_recurrent_step(const kda_recurrent_args* a, kda_stream_t stream) {
+  if (a == nullptr) return KDA_ERR_INVALID_ARG;
+  if (a->B < 0 || a->T < 1 || a->H < 1 || a->HV < 1 || a->K < 1 || a->V < 1 || a->num_slots < 0)
+    return KDA_ERR_INVALID_ARG;
+  if (a->HV % a->H != 0) return KDA_ERR_INVALID_ARG;
+  if (a->flags & ~KDA_FLAG_L2NORM_QK) return KDA_ERR_INVALID_ARG;
+  if (!((a->K == 64 || a->K == 128) && (a->V == 64 || a->V == 128))) return KDA_ERR_UNSUPPORTED;
+  if (a->T > KDA_RECURRENT_MAX_T) return KDA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(a->B) * a->HV > INT32_MAX ||
+      static_cast<int64_t>(a->B) * a->T * a->HV * (a->K > a->V ? a->K : a->V) > INT32_MAX)
+    return KDA_ERR_INVALID_ARG;
+  if (a->B > 0) {
+    if (!a->q || !a->k || !a->v || !a->a || !a->b || !a->A_log || !a->dt_bias || !a->indices || !a->o)
+      return KDA_ERR_INVALID_ARG;
+    if (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->a, 16) || !aligned(a->b, 2) ||
+        !aligned(a->A_log, 4) || !aligned(a->dt_bias, 16) || !aligned(a->indices, 4) || !aligned(a->o, 16))
+      return KDA_ERR_INVALID_ARG;
+    if (a->num_slots > 0 && (!a->state_pool || !aligned(a->state_pool, 16))) return KDA_ERR_INVALID_ARG;
+  }
+  if (a->err && !aligned(a->err, 4)) return KDA_ERR_INVALID_ARG;
+  kda::RecurrentCall c;
+  c.B = a->B;
+  c.T = a->T;
+  c.H = a->H;
+  c.HV = a->HV;
+  c.K = a->K;
+  c.V = a->V;
+  c.num_slots = a->num_slots;
+  c.l2norm = (a->flags & KDA_FLAG_L2NORM_QK) != 0;
+  c.scale = a->scale;
+  c.q = a->q;
+  c.k = a->k;
+  c.v = a->v;
+  c.a = a->a;
+  c.b = a->b;
+  c.A_log = a->A_log;
+  c.dt_bias = a->dt_bias;
+  c.state_pool = a->state_pool;
+  c.indices = a->indices;
+  c.o = a->o;
+  c.err = a->err;
+  const cudaError_t e = kda::launch_recurrent(c, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 const char* kda_version(void) { return "kda-gb300 0.1.0 sm_103a"; }
 
 }  // extern "C"

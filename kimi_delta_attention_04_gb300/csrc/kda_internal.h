@@ -64,6 +64,23 @@ inline size_t plan_header_bytes(int N) {
   return (b + 255) & ~static_cast<size_t>(255);
 }
 
+struct RecurrentCall {
+  int B, T, H, HV, K, V, num_slots;
+  bool l2norm;
+  float scale;
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* a;
+  const void* b;
+  const float* A_log;
+  const float* dt_bias;
+  float* state_pool;
+  const int32_t* indices;
+  void* o;
+  int32_t* err;
+};
+
 // Bytes of one (chunk, head) prep record.
 size_t record_bytes_tc(int d);           // bf16 tensor-core path, dk = dv = d
 size_t record_bytes_f32(int dk, int dv);  // fp32 path
@@ -75,5 +92,6 @@ cudaError_t launch_chunk_fused(const ChunkCall& c, cudaStream_t s);  // bf16, dk
 size_t fused_smem_bytes();
 size_t fused_workspace_bytes();  // pool of per-cluster global rings (fixed size)
 cudaError_t launch_decode(const DecodeCall& c, cudaStream_t s);
+cudaError_t launch_recurrent(const RecurrentCall& c, cudaStream_t s);
 
 }  // namespace kda

@@ -130,6 +130,37 @@ def decode_workload(*, seed=4, B=256, H=32, HV=32, K=128, V=128, num_slots=512,
                 scale=(1.0 / math.sqrt(K)) if scale is None else float(scale))
 
 
+def recurrent_workload(*, seed=5, B=64, T=8, H=32, HV=32, K=128, V=128, num_slots=128,
+                       pad_frac=0.1, state_std=0.1, scale=None):
+    """Inputs of one short-T recurrent step (T tokens per row on a slot pool).
+
+    Draw order: q, k (bf16 [B, T, H, K] ~ N(0,1)), v (bf16 [B, T, HV, V] ~ N(0,1)),
+    a (bf16 [B, T, HV*K] ~ N(0,1)), b (bf16 [B, T, HV] ~ N(0,1)), A_log (fp32 [HV]
+    ~ U(0,2)), dt_bias (fp32 [HV*K] ~ U(-1,1)), state pool (fp32 [num_slots, HV,
+    V, K] ~ state_std N(0,1)), slot indices (randperm(num_slots)[:B]), pad
+    positions (randperm(B)[:round(pad_frac*B + 0.5)] set to -1).
+    """
+    gen = _gen(seed)
+    q = _randn(gen, (B, T, H, K), torch.bfloat16)
+    k = _randn(gen, (B, T, H, K), torch.bfloat16)
+    v = _randn(gen, (B, T, HV, V), torch.bfloat16)
+    a = _randn(gen, (B, T, HV * K), torch.bfloat16)
+    b = _randn(gen, (B, T, HV), torch.bfloat16)
+    A_log = _uniform(gen, (HV,), 0.0, 2.0)
+    dt_bias = _uniform(gen, (HV * K,), -1.0, 1.0)
+    pool = _randn(gen, (num_slots, HV, V, K), torch.float32, state_std)
+    if B > num_slots:
+        raise ValueError("recurrent workload needs B <= num_slots (distinct slots)")
+    idx = torch.randperm(num_slots, generator=gen)[:B].to(torch.int32)
+    n_pad = int(math.floor(pad_frac * B + 0.5)) if pad_frac > 0 else 0
+    if n_pad:
+        pads = torch.randperm(B, generator=gen)[:n_pad]
+        idx[pads] = -1
+    return dict(q=q, k=k, v=v, a=a, b=b, A_log=A_log, dt_bias=dt_bias, state_pool=pool, indices=idx,
+                B=B, T=T, H=H, HV=HV, K=K, V=V, num_slots=num_slots,
+                scale=(1.0 / math.sqrt(K)) if scale is None else float(scale))
+
+
 # The five benchmark settings, by name.
 def fp32_small(seed=0, **kw):
     return chunk_workload(seed=seed, B=1, T=128, H=2, K=64, V=64, dtype=torch.float32,

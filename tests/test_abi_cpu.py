@@ -50,6 +50,7 @@ def test_struct_layout_matches_c(tmp_path):
     src = tmp_path / "layout.c"
     fields_c = [f for f, _ in _lib.ChunkArgs._fields_]
     fields_d = [f for f, _ in _lib.DecodeArgs._fields_]
+    fields_r = [f for f, _ in _lib.RecurrentArgs._fields_]
     lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void){"]
     lines.append('printf("chunk %zu\\n", sizeof(kda_chunk_args));')
     for f in fields_c:
@@ -57,6 +58,10 @@ def test_struct_layout_matches_c(tmp_path):
     lines.append('printf("decode %zu\\n", sizeof(kda_decode_args));')
     for f in fields_d:
         lines.append(f'printf("d.{f} %zu\\n", offsetof(kda_decode_args, {f}));')
+    lines.append('printf("recurrent %zu\\n", sizeof(kda_recurrent_args));')
+    for f in fields_r:
+        lines.append(f'printf("r.{f} %zu\\n", offsetof(kda_recurrent_args, {f}));')
+    lines.append('printf("maxT %d\\n", KDA_RECURRENT_MAX_T);')
     lines.append("return 0;}")
     src.write_text("\n".join(lines))
     exe = tmp_path / "layout"
@@ -69,6 +74,10 @@ def test_struct_layout_matches_c(tmp_path):
         assert int(got[f"c.{f}"]) == getattr(_lib.ChunkArgs, f).offset, f
     for f in fields_d:
         assert int(got[f"d.{f}"]) == getattr(_lib.DecodeArgs, f).offset, f
+    assert int(got["recurrent"]) == ctypes.sizeof(_lib.RecurrentArgs)
+    for f in fields_r:
+        assert int(got[f"r.{f}"]) == getattr(_lib.RecurrentArgs, f).offset, f
+    assert int(got["maxT"]) == _lib.KDA_RECURRENT_MAX_T
 
 
 # --- host-side validation, exercised with fake (never dereferenced) pointers ---
@@ -172,6 +181,35 @@ def _dec(**over):
 def test_decode_validation_rejects(lib, over, status):
     a = _dec(**over)
     assert lib.kda_decode_step(ctypes.byref(a), None) == status
+
+
+def _rec(**over):
+    a = _lib.RecurrentArgs()
+    a.B, a.T, a.H, a.HV, a.K, a.V, a.num_slots = 4, 8, 2, 4, 128, 128, 8
+    a.flags, a.scale = _lib.KDA_FLAG_L2NORM_QK, 0.1
+    a.q = a.k = a.v = a.a = a.b = a.A_log = a.dt_bias = a.state_pool = a.indices = a.o = FAKE
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(HV=3), _lib.KDA_ERR_INVALID_ARG),                   # HV not a multiple of H
+    (dict(T=0), _lib.KDA_ERR_INVALID_ARG),
+    (dict(T=_lib.KDA_RECURRENT_MAX_T + 1), _lib.KDA_ERR_UNSUPPORTED),  # long sequences: chunk forward
+    (dict(K=96), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(V=32), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(q=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(indices=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(state_pool=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(v=FAKE + 4), _lib.KDA_ERR_INVALID_ARG),              # misaligned
+    (dict(flags=0x2), _lib.KDA_ERR_INVALID_ARG),
+    (dict(B=-1), _lib.KDA_ERR_INVALID_ARG),
+])
+def test_recurrent_validation_rejects(lib, over, status):
+    a = _rec(**over)
+    assert lib.kda_recurrent_step(ctypes.byref(a), None) == status
+    assert lib.kda_recurrent_step(None, None) == _lib.KDA_ERR_INVALID_ARG
 
 
 def test_python_binding_refuses_cpu_tensors():

@@ -1,0 +1,112 @@
+"""GPU parity of kda_recurrent_step (T tokens per row on a state-slot pool)
+against the fp64 oracle, through the C ABI (ctypes binding) on the same
+bf16-rounded inputs. Tolerances as for decode: rel-Frobenius <= 5e-3 and
+max-abs <= 2e-2 for o and the updated slots; padding rows and slots no row
+indexes are bit-exact."""
+
+import pytest
+import torch
+
+import kimi_delta_attention_04_gb300 as kda
+from kimi_delta_attention_04_gb300 import workloads as W
+from oracle import kda_oracle as ko
+
+from kda_cases import assert_close, np64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from kimi_delta_attention_04_gb300 import build
+    build.build()
+    kda.load()
+
+
+def _run(wl, err=None):
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in wl.items()}
+    pool = d["state_pool"].clone()
+    o = kda.kda_recurrent_step(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], pool, d["indices"],
+                               scale=wl["scale"], err=err)
+    torch.cuda.synchronize()
+    return o, pool
+
+
+def _oracle(wl):
+    return ko.kda_recurrent_pool(np64(wl["q"]), np64(wl["k"]), np64(wl["v"]), np64(wl["a"]), np64(wl["b"]),
+                                 np64(wl["A_log"]), np64(wl["dt_bias"]), np64(wl["state_pool"]),
+                                 wl["indices"].numpy(), scale=wl["scale"])
+
+
+def _check(wl):
+    o, pool = _run(wl)
+    o_ref, pool_ref = _oracle(wl)
+    idx = wl["indices"]
+    valid = idx[idx >= 0].long()
+    assert_close("recurrent o", np64(o), o_ref, torch.bfloat16)
+    assert_close("recurrent state", np64(pool[valid.cuda()]), pool_ref[valid.numpy()], torch.bfloat16)
+    pads = (idx < 0).nonzero().flatten().cuda()
+    assert torch.equal(o[pads], torch.zeros_like(o[pads]))
+    untouched = torch.ones(wl["num_slots"], dtype=torch.bool)
+    untouched[valid] = False
+    ut = untouched.nonzero().flatten().cuda()
+    assert torch.equal(pool[ut], wl["state_pool"].cuda()[ut])
+    return o, pool
+
+
+@pytest.mark.parametrize("B,T,H,HV,K,V", [
+    (4, 3, 2, 4, 64, 64),      # value-head grouping, ragged T
+    (5, 8, 2, 2, 128, 128),
+    (3, 33, 1, 2, 128, 64),    # more tokens than one warp's share, HV = 2H
+    (6, 1, 2, 4, 64, 128),     # T = 1
+    (2, 64, 1, 1, 128, 128),   # the longest T the entry point takes
+])
+def test_recurrent_small(B, T, H, HV, K, V):
+    wl = W.recurrent_workload(seed=90 + B + T, B=B, T=T, H=H, HV=HV, K=K, V=V, num_slots=2 * B + 3, pad_frac=0.25)
+    _check(wl)
+
+
+def test_recurrent_full_size():
+    """B=64 rows of T=8 tokens, H=HV=32, K=V=128, fp32 pool [128, 32, 128, 128], 6 padded rows."""
+    _check(W.recurrent_workload())
+
+
+def test_recurrent_t1_matches_decode_kernel():
+    """One token per row through both entry points (decode reads a packed row)."""
+    wl = W.recurrent_workload(seed=97, B=9, T=1, H=2, HV=4, K=128, V=128, num_slots=12, pad_frac=0.2)
+    o, pool = _run(wl)
+    B, H, HV, K, V = wl["B"], wl["H"], wl["HV"], wl["K"], wl["V"]
+    packed = torch.cat([wl["q"].reshape(B, H * K), wl["k"].reshape(B, H * K), wl["v"].reshape(B, HV * V)], dim=1)
+    pool2 = wl["state_pool"].cuda().clone()
+    o2 = kda.kda_decode_step(packed.cuda().contiguous(), wl["a"].reshape(B, HV * K).cuda().contiguous(),
+                             wl["b"].reshape(B, HV).cuda().contiguous(), wl["A_log"].cuda(), wl["dt_bias"].cuda(),
+                             pool2, wl["indices"].cuda(), H=H, HV=HV, K=K, V=V, scale=wl["scale"])
+    torch.cuda.synchronize()
+    assert_close("o vs decode", np64(o[:, 0]), np64(o2), torch.bfloat16)
+    assert_close("state vs decode", np64(pool), np64(pool2), torch.bfloat16)
+
+
+def test_recurrent_bad_slot_and_padding():
+    wl = W.recurrent_workload(seed=98, B=5, T=4, H=2, HV=2, K=64, V=64, num_slots=6, pad_frac=0.0)
+    wl["indices"] = torch.tensor([-1, 4, 77, 0, -1], dtype=torch.int32)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, pool = _run(wl, err=err)
+    assert int(err.item()) == 1  # KDA_ERR_INVALID_ARG from the out-of-range slot
+    assert torch.equal(o[[0, 2, 4]], torch.zeros_like(o[[0, 2, 4]]))
+    assert torch.equal(pool[[1, 2, 3, 5]], wl["state_pool"].cuda()[[1, 2, 3, 5]])
+    o_ref, pool_ref = _oracle(dict(wl, indices=torch.tensor([-1, 4, -1, 0, -1], dtype=torch.int32)))
+    assert_close("recurrent o", np64(o), o_ref, torch.bfloat16)
+    assert_close("recurrent state", np64(pool[[0, 4]]), pool_ref[[0, 4]], torch.bfloat16)
+
+
+def test_recurrent_split_tokens_equals_one_call():
+    """T tokens in one call equal T1 then T - T1 tokens in two calls on the same pool."""
+    wl = W.recurrent_workload(seed=99, B=4, T=10, H=2, HV=4, K=128, V=128, num_slots=8, pad_frac=0.25)
+    o, pool = _run(wl)
+    first = {k: (v[:, :6].contiguous() if k in ("q", "k", "v", "a", "b") else v) for k, v in wl.items()}
+    o1, pool1 = _run(first)
+    second = {k: (v[:, 6:].contiguous() if k in ("q", "k", "v", "a", "b") else v) for k, v in wl.items()}
+    second["state_pool"] = pool1.cpu()
+    o2, pool2 = _run(second)
+    assert_close("o split", np64(torch.cat([o1, o2], dim=1)), np64(o), torch.bfloat16)
+    assert_close("state split", np64(pool2), np64(pool), torch.bfloat16)

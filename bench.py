@@ -60,6 +60,15 @@ def prefill_algorithmic_flops(T=PREFILL_T):
     return T * PREFILL_H * per
 
 
+def recurrent_algorithmic_bytes(n_valid, B, T, H=32, HV=32, K=128, V=128):
+    """Short-T recurrent step: each valid row's slot read and written once for
+    its T tokens, the valid rows' q, k, v, a, b, every row's o, the parameters."""
+    state = n_valid * HV * V * K * 4 * 2
+    io = n_valid * T * (2 * H * K * 2 + HV * V * 2 + HV * K * 2 + HV * 2)
+    params = HV * 4 + HV * K * 4 + B * 4
+    return state + io + params + B * T * HV * V * 2
+
+
 def decode_algorithmic_bytes(n_valid, H=32, HV=32, K=128, V=128, B=256):
     state = n_valid * HV * V * K * 4 * 2                            # read + write of each valid slot
     io = n_valid * (2 * H * K * 2 + HV * V * 2 + HV * K * 2 + HV * 2)  # packed q,k,v + a + b of valid rows
@@ -71,6 +80,7 @@ def decode_algorithmic_bytes(n_valid, H=32, HV=32, K=128, V=128, B=256):
 # figure is only reported while these files are unchanged).
 CHUNK_KERNEL_SOURCES = ["kda_chunk_fused.cu", "kda_common.cuh", "kda_cluster.cuh", "kda_tma.h", "kda_tma.cpp"]
 DECODE_KERNEL_SOURCES = ["kda_decode.cu", "kda_common.cuh"]
+RECURRENT_B, RECURRENT_T, RECURRENT_SLOTS = 128, 8, 256  # speculative-style step: 128 rows x 8 tokens
 CHUNK_LAUNCHES_PER_STEP = 1   # kda_chunk_fused_kernel (bf16, d = 128, no cu_seqlens)
 DECODE_LAUNCHES_PER_STEP = 1  # kda_decode_kernel
 
@@ -319,6 +329,33 @@ def run_gpu(args):
         torch.cuda.synchronize(dev)
     e2e_s = (time.perf_counter() - t0) / max(e2e_steps, 1)
 
+    # --- short-T recurrent step (its own timed region, not part of the step) ---
+    rec = None
+    if args.only == "all":
+        rw = W.recurrent_workload(seed=5 + 100 * rank, B=RECURRENT_B, T=RECURRENT_T, num_slots=RECURRENT_SLOTS)
+        rd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in rw.items()}
+        orr = torch.empty(rw["B"], rw["T"], rw["HV"], rw["V"], dtype=torch.bfloat16, device=dev)
+
+        def rec_step():
+            kda.kda_recurrent_step(rd["q"], rd["k"], rd["v"], rd["a"], rd["b"], rd["A_log"], rd["dt_bias"],
+                                   rd["state_pool"], rd["indices"], scale=rw["scale"], o=orr, stream=stream)
+        for _ in range(args.warmup):
+            rec_step()
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        r0.record(stream)
+        for _ in range(K):
+            rec_step()
+        r1.record(stream)
+        torch.cuda.synchronize(dev)
+        r_avg = r0.elapsed_time(r1) / 1000.0 / K
+        r_valid = int((rw["indices"] >= 0).sum())
+        rbytes = recurrent_algorithmic_bytes(r_valid, rw["B"], rw["T"])
+        rec = {"us_per_step": 1e6 * r_avg, "rows": rw["B"], "tokens_per_row": rw["T"], "n_valid_rows": r_valid,
+               "tokens_per_s": rw["B"] * rw["T"] / r_avg,
+               "roofline": {"bound": "hbm", "achieved": rbytes / r_avg / 1e9, "unit": "GB/s",
+                            "algorithmic_bytes": rbytes, "kernel": "kda_recurrent_kernel"}}
+
     # --- reduce over ranks: max time ---
     t_chunk = sum(chunk_ms) / 1000.0
     t_dec = sum(dec_ms) / 1000.0
@@ -354,6 +391,7 @@ def run_gpu(args):
                        "step": "one chunk forward (prefill) then one decode step (B=256)"},
             "chunk_fwd": {"ms": 1000.0 * chunk_avg, "tokens_per_s": value,
                           "roofline_time_us": 1e6 * t_roof, "frac_of_roofline": t_roof / chunk_avg if chunk_avg > 0 else 0.0},
+            "recurrent": rec,
             "decode": {"us_per_step": 1e6 * dec_avg, "n_valid_rows": n_valid,
                        "roofline": {"bound": "hbm", "achieved": dach, "peak": hbm, "unit": "GB/s",
                                     "frac": dach / hbm, "algorithmic_bytes": dbytes,
@@ -367,6 +405,10 @@ def run_gpu(args):
                             + (DECODE_LAUNCHES_PER_STEP if args.only != "chunk" else 0) * K,
             "clocks": clk,
         }
+        if rec is not None:
+            rec["roofline"]["peak"] = hbm
+            rec["roofline"]["frac"] = rec["roofline"]["achieved"] / hbm
+            rec["roofline"]["peak_kind"] = peak_kind
         if args.only != "all" or T != PREFILL_T:
             line["config"]["partial"] = f"only={args.only}, seq_len={T}: a profiling run, not the benchmark line"
         if world == 1 and not args.no_cpu_baseline:

@@ -329,6 +329,39 @@ def run_gpu(args):
         torch.cuda.synchronize(dev)
     e2e_s = (time.perf_counter() - t0) / max(e2e_steps, 1)
 
+    # --- varlen prefill: 16 packed sequences (its own timed region) ---
+    var = None
+    if args.only == "all":
+        vw = W.varlen(seed=3 + 100 * rank)
+        vd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in vw.items()}
+        n_seq = int(vd["cu_seqlens"].numel()) - 1
+        t_tot = int(vw["q"].shape[1])
+        vo = torch.empty_like(vd["v"])
+        vhT = torch.empty(n_seq, PREFILL_H, D, D, dtype=torch.float32, device=dev)
+        vargs = kda.make_chunk_args(vd["q"], vd["k"], vd["v"], scale=vd["scale"], a=vd["a"], dt_bias=vd["dt_bias"],
+                                    A_log=vd["A_log"], b=vd["b"], h0=vd["h0"], cu_seqlens=vd["cu_seqlens"],
+                                    l2norm_qk=True, o=vo, hT=vhT)
+        vws = torch.empty(kda.chunk_workspace_size(vargs), dtype=torch.uint8, device=dev)
+
+        def var_step():
+            kda.kda_chunk_fwd(vd["q"], vd["k"], vd["v"], scale=vd["scale"], a=vd["a"], dt_bias=vd["dt_bias"],
+                              A_log=vd["A_log"], b=vd["b"], h0=vd["h0"], cu_seqlens=vd["cu_seqlens"],
+                              l2norm_qk=True, o=vo, hT=vhT, workspace=vws, stream=stream)
+        for _ in range(args.warmup):
+            var_step()
+        v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        v0.record(stream)
+        for _ in range(K):
+            var_step()
+        v1.record(stream)
+        torch.cuda.synchronize(dev)
+        v_avg = v0.elapsed_time(v1) / 1000.0 / K
+        vbytes = t_tot * BYTES_PER_TOKEN + 2 * n_seq * STATE_BYTES + PARAM_BYTES
+        var = {"ms": 1000.0 * v_avg, "sequences": n_seq, "tokens": t_tot, "tokens_per_s": t_tot / v_avg,
+               "algorithmic_bytes": vbytes, "achieved_gbs": vbytes / v_avg / 1e9,
+               "launches_per_call": 2, "note": "kda_plan_kernel + kda_chunk_fused_kernel"}
+
     # --- short-T recurrent step (its own timed region, not part of the step) ---
     rec = None
     if args.only == "all":
@@ -391,6 +424,7 @@ def run_gpu(args):
                        "step": "one chunk forward (prefill) then one decode step (B=256)"},
             "chunk_fwd": {"ms": 1000.0 * chunk_avg, "tokens_per_s": value,
                           "roofline_time_us": 1e6 * t_roof, "frac_of_roofline": t_roof / chunk_avg if chunk_avg > 0 else 0.0},
+            "varlen": var,
             "recurrent": rec,
             "decode": {"us_per_step": 1e6 * dec_avg, "n_valid_rows": n_valid,
                        "roofline": {"bound": "hbm", "achieved": dach, "peak": hbm, "unit": "GB/s",
@@ -405,6 +439,8 @@ def run_gpu(args):
                             + (DECODE_LAUNCHES_PER_STEP if args.only != "chunk" else 0) * K,
             "clocks": clk,
         }
+        if var is not None:
+            var["frac_of_roofline"] = var["achieved_gbs"] / hbm
         if rec is not None:
             rec["roofline"]["peak"] = hbm
             rec["roofline"]["frac"] = rec["roofline"]["achieved"] / hbm

@@ -82,6 +82,15 @@ def kda_gate(a: np.ndarray, dt_bias: np.ndarray, A_log: np.ndarray) -> np.ndarra
     return -np.exp(A_log)[:, None] * softplus(a + dt_bias)
 
 
+def head_gate_to_channels(g_head: np.ndarray, K: int) -> np.ndarray:
+    """Gated DeltaNet's gate: one log-decay per token and head, the same for every
+    key channel ([TL] §1 ladder: Gated DeltaNet = scalar decay + delta rule, KDA
+    refines it to per-channel; [LA] model tree: Mamba-2 / SSD scalar alpha_t).
+    g_head [..., H] -> g [..., H, K]."""
+    g_head = np.asarray(g_head, dtype=np.float64)
+    return np.repeat(g_head[..., None], K, axis=-1)
+
+
 # ----------------------------------------------------------------------------
 # Token-by-token recurrence: the definition ([TL] §1, [FKDA] 背景)
 # ----------------------------------------------------------------------------
@@ -142,12 +151,13 @@ def _sequences(B, T, cu_seqlens):
 
 def kda_forward(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None,
                 beta=None, b=None, h0=None, cu_seqlens=None, l2norm_qk=False,
-                delta=True, chunk_size=None):
+                delta=True, chunk_size=None, g_head=None):
     """The chunk-forward operation as the C ABI exposes it, computed in fp64.
 
     q, k: [B, T, H, K]; v: [B, T, H, V]. The gate is given either as g
     [B, T, H, K], or as gate inputs a [B, T, H*K], dt_bias [H*K], A_log [H]
-    (g = -exp(A_log) * softplus(a + dt_bias)), or not at all (g = 0).
+    (g = -exp(A_log) * softplus(a + dt_bias)), or per head as g_head [B, T, H]
+    (Gated DeltaNet: the same decay on every key channel), or not at all (g = 0).
     beta [B, T, H] is given directly or as logits b (beta = sigmoid(b)).
     h0: [N, H, V, K] or None. cu_seqlens: [N+1] over a single row (B == 1) or None.
     chunk_size None runs the token recurrence; an integer runs kda_chunked.
@@ -163,6 +173,8 @@ def kda_forward(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None,
         k = l2_normalize(k)
     if g is not None:
         g = np.asarray(g, np.float64)
+    elif g_head is not None:
+        g = head_gate_to_channels(g_head, K)
     elif a is not None:
         g = kda_gate(np.asarray(a, np.float64).reshape(B, T, H, K),
                      np.asarray(dt_bias, np.float64).reshape(H, K), A_log)

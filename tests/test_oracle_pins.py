@@ -398,13 +398,44 @@ def pin_recurrent_pool_tokens_matter():
     assert _rel(p2, p) > 1e-3 and _rel(o2[:, 2], o[:, 2]) > 1e-3
 
 
+def pin_head_gate_semiseparable():
+    """Gated DeltaNet's scalar decay with the delta term off is the
+    semiseparable (Mamba-2 / SSD) form: o_t = scale [ (prod_{r<=t} a_r) S0^T q_t
+    + sum_{s<=t} (prod_{s<r<=t} a_r) (q_t . k_s) v_s ], a_r = e^{g_r}; brute force
+    over all (s, t) pairs. With the delta term on it must equal KDA whose
+    per-channel gate repeats the head's value on every channel."""
+    r = _rng(18)
+    T, H, K, V = 9, 2, 3, 2
+    q = r.standard_normal((1, T, H, K))
+    k = r.standard_normal((1, T, H, K))
+    v = r.standard_normal((1, T, H, V))
+    gh = -r.uniform(0.05, 1.0, (1, T, H))
+    h0 = r.standard_normal((1, H, V, K))
+    o, hT = ko.kda_forward(q, k, v, scale=0.7, g_head=gh, h0=h0, delta=False)
+    for h in range(H):
+        S = h0[0, h].T.copy()                       # math state [K, V]
+        for t in range(T):
+            want = math.exp(gh[0, :t + 1, h].sum()) * (h0[0, h] @ q[0, t, h])
+            for s in range(t + 1):
+                want = want + math.exp(gh[0, s + 1:t + 1, h].sum()) * (q[0, t, h] @ k[0, s, h]) * v[0, s, h]
+            np.testing.assert_allclose(o[0, t, h], 0.7 * want, rtol=1e-12, atol=1e-12)
+        S = math.exp(gh[0, :, h].sum()) * S + sum(math.exp(gh[0, s + 1:, h].sum()) * np.outer(k[0, s, h], v[0, s, h])
+                                                for s in range(T))
+        np.testing.assert_allclose(hT[0, h], S.T, rtol=1e-12, atol=1e-12)
+    bb = r.uniform(0, 1, (1, T, H))
+    o1, h1 = ko.kda_forward(q, k, v, scale=0.7, g_head=gh, h0=h0, beta=bb)
+    o2, h2 = ko.kda_forward(q, k, v, scale=0.7, g=np.repeat(gh[..., None], K, axis=-1), h0=h0, beta=bb)
+    np.testing.assert_allclose(o1, o2, rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(h1, h2, rtol=1e-14, atol=1e-14)
+
+
 PINS = [
     pin_hand_worked_chunk, pin_level1_quadratic_form, pin_level1_chunk_identity,
     pin_gla_parallel_form, pin_retnet_scalar_decay, pin_chunked_equals_recurrent,
     pin_L_nilpotent_and_inverse, pin_chunk_matrices_brute_force, pin_delta_exact_write,
     pin_beta_zero_pure_decay, pin_orthonormal_keys, pin_gate_sigmoid_l2norm,
     pin_decode_golden, pin_decode_head_grouping, pin_split_sequence, pin_value_split_invariance,
-    pin_recurrent_pool_is_repeated_decode, pin_recurrent_pool_tokens_matter,
+    pin_recurrent_pool_is_repeated_decode, pin_recurrent_pool_tokens_matter, pin_head_gate_semiseparable,
 ]
 
 
@@ -530,6 +561,17 @@ _orig_chunk_matrices = ko.chunk_matrices
 _orig_recurrent_pool = ko.kda_recurrent_pool
 
 
+def _hg_first_channel_only(g_head, K):
+    g = np.asarray(g_head, np.float64)
+    out = np.zeros(g.shape + (K,))
+    out[..., 0] = g
+    return out
+
+
+def _hg_exp_twice(g_head, K):
+    return np.repeat(np.exp(np.asarray(g_head, np.float64))[..., None] - 1.0, K, axis=-1)
+
+
 def _rp_reversed_tokens(q, k, v, a, b, *args, **kw):
     return _orig_recurrent_pool(q[:, ::-1], k[:, ::-1], v[:, ::-1], a[:, ::-1], b[:, ::-1], *args, **kw)
 
@@ -571,6 +613,8 @@ MUTANTS = [
     ("kda_recurrent_pool", _rp_reversed_tokens),
     ("kda_recurrent_pool", _rp_group_by_modulo),
     ("kda_recurrent_pool", _rp_state_not_carried),
+    ("head_gate_to_channels", _hg_first_channel_only),
+    ("head_gate_to_channels", _hg_exp_twice),
 ]
 
 

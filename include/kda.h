@@ -67,7 +67,9 @@ typedef enum {
 typedef enum {
   KDA_GATE_NONE = 0,    /* g = 0 (no decay) */
   KDA_GATE_G = 1,       /* log-decay g given: fp32 [B, T, H, dk] */
-  KDA_GATE_INPUTS = 2   /* g = -exp(A_log[h]) * softplus(a + dt_bias) computed in the kernel */
+  KDA_GATE_INPUTS = 2,  /* g = -exp(A_log[h]) * softplus(a + dt_bias) computed in the kernel */
+  KDA_GATE_HEAD_G = 3   /* Gated DeltaNet: one log-decay per token and head, g fp32 [B, T, H],
+                           applied to every key channel (TileLang 实战 §1 ladder) */
 } kda_gate_mode;
 
 typedef enum {
@@ -85,7 +87,7 @@ typedef enum {
  * Shapes (row-major, contiguous):
  *   q, k      [B, T, H, dk]        dtype
  *   v, o      [B, T, H, dv]        dtype
- *   g         [B, T, H, dk]        fp32   (KDA_GATE_G)
+ *   g         [B, T, H, dk]        fp32   (KDA_GATE_G), or [B, T, H] (KDA_GATE_HEAD_G)
  *   a         [B, T, H*dk]         fp32   (KDA_GATE_INPUTS)
  *   A_log     [H]                  fp32   (KDA_GATE_INPUTS)
  *   dt_bias   [H*dk]               fp32   (KDA_GATE_INPUTS)

@@ -30,7 +30,7 @@ KDA_NOALLOC_SCRATCH_BYTES = 16 << 20
 
 KDA_DTYPE_BF16 = 0
 KDA_DTYPE_FP32 = 1
-KDA_GATE_NONE, KDA_GATE_G, KDA_GATE_INPUTS = 0, 1, 2
+KDA_GATE_NONE, KDA_GATE_G, KDA_GATE_INPUTS, KDA_GATE_HEAD_G = 0, 1, 2, 3
 KDA_BETA_VALUES, KDA_BETA_LOGITS = 0, 1
 KDA_FLAG_L2NORM_QK = 0x1
 KDA_FLAG_DELTA_OFF = 0x2
@@ -146,7 +146,7 @@ def _dtype_code(dt: torch.dtype) -> int:
 
 
 def make_chunk_args(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None, beta=None, b=None,
-                    h0=None, cu_seqlens=None, l2norm_qk=False, delta=True, o=None, hT=None, err=None):
+                    h0=None, cu_seqlens=None, l2norm_qk=False, delta=True, o=None, hT=None, err=None, g_head=None):
     """Fill the C argument struct from tensors (no allocation, no launch)."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
@@ -156,6 +156,8 @@ def make_chunk_args(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None,
         N = B
     if g is not None:
         gate_mode = KDA_GATE_G
+    elif g_head is not None:
+        gate_mode, g = KDA_GATE_HEAD_G, g_head  # passed in the g field
     elif a is not None:
         gate_mode = KDA_GATE_INPUTS
     else:
@@ -184,12 +186,13 @@ def chunk_workspace_size(args: ChunkArgs) -> int:
 
 def kda_chunk_fwd(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None, beta=None, b=None,
                   h0=None, cu_seqlens=None, l2norm_qk=False, delta=True, o=None, hT=None,
-                  output_final_state=True, workspace=None, err=None, stream=None):
+                  output_final_state=True, workspace=None, err=None, stream=None, g_head=None):
     """Chunkwise KDA forward through libkda (see include/kda.h for the contract).
 
     q, k [B, T, H, dk]; v [B, T, H, dv] (bf16 or fp32, same dtype). The gate is
     g (fp32 [B, T, H, dk]) or gate inputs a (fp32 [B, T, H*dk]) + dt_bias
-    (fp32 [H*dk]) + A_log (fp32 [H]), or neither (g = 0). beta [B, T, H] is given
+    (fp32 [H*dk]) + A_log (fp32 [H]), or the Gated DeltaNet per-head gate g_head
+    (fp32 [B, T, H]), or none (g = 0). beta [B, T, H] is given
     as values (beta=) or logits (b=). h0 / returned hT are fp32 [N, H, dv, dk].
     Returns (o, hT) with hT None when output_final_state is False.
     """
@@ -202,7 +205,7 @@ def kda_chunk_fwd(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None, b
         hT = torch.empty(N, H, v.shape[-1], q.shape[-1], dtype=torch.float32, device=q.device)
     args = make_chunk_args(q, k, v, scale=scale, g=g, a=a, dt_bias=dt_bias, A_log=A_log, beta=beta, b=b,
                            h0=h0, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk, delta=delta, o=o, hT=hT,
-                           err=err)
+                           err=err, g_head=g_head)
     need = int(lib.kda_chunk_workspace_size(ctypes.byref(args)))
     if need == 0:
         st = lib.kda_chunk_fwd(ctypes.byref(args), None, 0, _stream_ptr(stream))
@@ -217,7 +220,7 @@ def kda_chunk_fwd(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None, b
 
 def kda_chunk_fwd_noalloc(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None, beta=None, b=None,
                           h0=None, cu_seqlens=None, l2norm_qk=False, delta=True, o=None, hT=None,
-                          output_final_state=True, err=None, stream=None):
+                          output_final_state=True, err=None, stream=None, g_head=None):
     """kda_chunk_fwd on the library's own scratch buffer: the C call allocates
     nothing (for callers that may not allocate device memory; see
     include/kda.h). Outputs o / hT are allocated here with torch unless given.
@@ -232,7 +235,7 @@ def kda_chunk_fwd_noalloc(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log
         hT = torch.empty(N, H, v.shape[-1], q.shape[-1], dtype=torch.float32, device=q.device)
     args = make_chunk_args(q, k, v, scale=scale, g=g, a=a, dt_bias=dt_bias, A_log=A_log, beta=beta, b=b,
                            h0=h0, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk, delta=delta, o=o, hT=hT,
-                           err=err)
+                           err=err, g_head=g_head)
     st = lib.kda_chunk_fwd_noalloc(ctypes.byref(args), _stream_ptr(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_chunk_fwd_noalloc")

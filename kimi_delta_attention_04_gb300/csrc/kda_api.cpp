@@ -26,7 +26,7 @@ kda_status check_chunk(const kda_chunk_args* a, kda::ChunkGeom* geo, size_t* rec
   if (a->dtype != KDA_DTYPE_BF16 && a->dtype != KDA_DTYPE_FP32) return KDA_ERR_INVALID_ARG;
   if (a->B < 1 || a->T < 0 || a->H < 1 || a->dk < 1 || a->dv < 1 || a->N < 1) return KDA_ERR_INVALID_ARG;
   if (a->flags & ~(KDA_FLAG_L2NORM_QK | KDA_FLAG_DELTA_OFF)) return KDA_ERR_INVALID_ARG;
-  if (a->gate_mode < KDA_GATE_NONE || a->gate_mode > KDA_GATE_INPUTS) return KDA_ERR_INVALID_ARG;
+  if (a->gate_mode < KDA_GATE_NONE || a->gate_mode > KDA_GATE_HEAD_G) return KDA_ERR_INVALID_ARG;
   const bool delta = !(a->flags & KDA_FLAG_DELTA_OFF);
   if (delta && a->beta_mode != KDA_BETA_VALUES && a->beta_mode != KDA_BETA_LOGITS) return KDA_ERR_INVALID_ARG;
   if (a->cu_seqlens == nullptr) {
@@ -43,6 +43,7 @@ kda_status check_chunk(const kda_chunk_args* a, kda::ChunkGeom* geo, size_t* rec
     if (!a->q || !a->k || !a->v || !a->o) return KDA_ERR_INVALID_ARG;
     if (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->o, 16)) return KDA_ERR_INVALID_ARG;
     if (a->gate_mode == KDA_GATE_G && (!a->g || !aligned(a->g, 16))) return KDA_ERR_INVALID_ARG;
+    if (a->gate_mode == KDA_GATE_HEAD_G && (!a->g || !aligned(a->g, 4))) return KDA_ERR_INVALID_ARG;
     if (a->gate_mode == KDA_GATE_INPUTS) {
       if (!a->a || !a->A_log || !a->dt_bias) return KDA_ERR_INVALID_ARG;
       if (!aligned(a->a, 16) || !aligned(a->A_log, 4) || !aligned(a->dt_bias, 4)) return KDA_ERR_INVALID_ARG;

@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kPrepThreads32) kda_prep_f32_kernel(const Chun
     if (vk) {
       if (p.gate_mode == 1) a = expf(p.g[kbase + i * kstride]);
       else if (p.gate_mode == 2) a = expf(-Aexp * softplus_f(p.a[kbase + i * kstride] + dtb));
+      else if (p.gate_mode == 3) a = expf(p.g[(static_cast<size_t>(pos.tok0) + i) * H + h]);
     }
     al[i] = a;
   }

@@ -101,6 +101,7 @@ struct __align__(16) PrepScratch {
   float Mq[16][17];
   float red[4][48];
   float rnq[16], rnk[16], beta[16];
+  float ghead[16];  // per-head log-decay of the chunk's tokens (KDA_GATE_HEAD_G)
 };
 
 constexpr int kOPitch = kRows + 4;  // padded row of an output partial (conflict-free both ways)
@@ -135,12 +136,13 @@ __device__ __forceinline__ int col_tok_f(int s, int r) { return (r / s) * 2 * s 
 // tokens of the next sequence are masked by the reader.
 __device__ __forceinline__ void issue_inputs(const TmaInputMaps& m, PrepIn& in, uint64_t* bar, int h, int tok0,
                                              int gate_mode) {
-  const uint32_t bytes = 3 * sizeof(in.q) + (gate_mode != 0 ? sizeof(in.a) : 0);
+  const bool gate_tile = gate_mode == 1 || gate_mode == 2;  // per-channel gate (not the per-head one)
+  const uint32_t bytes = 3 * sizeof(in.q) + (gate_tile ? sizeof(in.a) : 0);
   mbar_arrive_expect_tx_local(bar, bytes);
   tma_load_3d(&in.q[0][0], &m.q, 0, h, tok0, bar);
   tma_load_3d(&in.k[0][0], &m.k, 0, h, tok0, bar);
   tma_load_3d(&in.v[0][0], &m.v, 0, h, tok0, bar);
-  if (gate_mode != 0) tma_load_3d(&in.a[0][0], &m.a, 0, h, tok0, bar);
+  if (gate_tile) tma_load_3d(&in.a[0][0], &m.a, 0, h, tok0, bar);
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
@@ -404,13 +406,22 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       return raw;
     };
     if (c < nch) beta_next = load_beta(c);
+    // Per-head gate (Gated DeltaNet): one log-decay per token, prefetched like beta.
+    float gh_next = 0.f;
+    auto load_gh = [&](int cc) {
+      float x = 0.f;
+      const int tk0 = ts + cc * kChunk;
+      if (p.gate_mode == 3 && pt < 16 && tk0 + pt < te) x = p.g[static_cast<size_t>(tk0 + pt) * H + h];
+      return x;
+    };
+    if (c < nch) gh_next = load_gh(c);
     // Each group loads its own input tiles with TMA: the first chunk's now,
     // chunk c + 8's as soon as chunk c's are in registers.
     if (pt == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.q) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.k) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.v) : "memory");
-      if (p.gate_mode != 0) asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.a) : "memory");
+      if (p.gate_mode == 1 || p.gate_mode == 2) asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.a) : "memory");
       if (c < nch) issue_inputs(maps, sm.pin[grp], &sm.pinbar[grp], h, ts + c * kChunk, p.gate_mode);
     }
     // The hand-off of a written chunk to the publisher (a release at CTA scope)
@@ -427,6 +438,8 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       const int ntok = min(kChunk, te - tok0);
       const float beta_cur = __bfloat162float(__ushort_as_bfloat16(beta_next));
       if (c + 2 * kCtas < nch) beta_next = load_beta(c + 2 * kCtas);
+      const float gh_cur = gh_next;
+      if (c + 2 * kCtas < nch) gh_next = load_gh(c + 2 * kCtas);
       if (!failed && !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pinbar[buf])),
                                         static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs)) {
         failed = true;
@@ -448,6 +461,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       if (pt < 16) {
         const float bt = (p.beta_mode == 1) ? sigmoid_f(beta_cur) : beta_cur;
         ps.beta[pt] = (DELTA && pt < ntok) ? bt : 0.f;
+        ps.ghead[pt] = gh_cur;
       }
       prep_bar();
       signal_written();
@@ -474,6 +488,10 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           const float a = ex2_approx(nA * sp2);
           al[i] = i < ntok ? a : 1.f;
         }
+      } else if (p.gate_mode == 3) {
+        constexpr float kLog2e = 1.4426950408889634f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) al[i] = i < ntok ? ex2_approx(ps.ghead[i] * kLog2e) : 1.f;
       } else if (p.gate_mode == 1) {
         constexpr float kLog2e = 1.4426950408889634f;
 #pragma unroll

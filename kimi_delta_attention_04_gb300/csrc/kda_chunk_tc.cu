@@ -164,6 +164,8 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_tc_kernel(const ChunkCa
       } else if (p.gate_mode == 2) {
         const float x = p.a[base + i * row_stride] + dtb;
         a = expf(-Aexp * softplus_f(x));
+      } else if (p.gate_mode == 3) {  // one decay per token and head
+        a = expf(p.g[(static_cast<size_t>(pos.tok0) + i) * H + h]);
       }
     }
     al[i] = a;

@@ -44,7 +44,7 @@ cudaError_t encode_input_maps(const ChunkCall& c, TmaInputMaps* m) {
   bool ok = encode3d(&m->q, c.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, H, tokens) &&
             encode3d(&m->k, c.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, H, tokens) &&
             encode3d(&m->v, c.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, H, tokens);
-  if (ok && c.gate_mode != 0)
+  if (ok && (c.gate_mode == 1 || c.gate_mode == 2))  // per-channel gate tiles (not the per-head one)
     ok = encode3d(&m->a, c.gate_mode == 1 ? static_cast<const void*>(c.g) : static_cast<const void*>(c.a),
                   CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, D, H, tokens);
   return ok ? cudaSuccess : cudaErrorInvalidValue;

@@ -52,7 +52,8 @@ def chunk_workload(*, seed=2, B=1, T=8192, H=32, K=128, V=128, dtype=torch.bfloa
 
     gate: "inputs" (a ~ N(0,1) fp32 [B, T, H*K], dt_bias ~ U(-1,1) [H*K],
           A_log ~ U(0, A_log_hi) [H]), "g" (a log-decay g = -U(0.01, 3) fp32
-          [B, T, H, K], drawn directly), or "none".
+          [B, T, H, K], drawn directly), "head" (Gated DeltaNet: one log-decay
+          per token and head, g_head = -U(0.01, 3) fp32 [B, T, H]), or "none".
     beta: "logits" (b ~ N(0,1)), "values" (beta ~ U(0,1)), both in the input dtype.
     h0_std: standard deviation of the fp32 initial state, or None for no h0.
     scale: output scale; defaults to K^-0.5.
@@ -72,7 +73,7 @@ def chunk_workload(*, seed=2, B=1, T=8192, H=32, K=128, V=128, dtype=torch.bfloa
     q = _randn(gen, (B, T, H, K), dtype, qkv_std)
     k = _randn(gen, (B, T, H, K), dtype, qkv_std)
     v = _randn(gen, (B, T, H, V), dtype, qkv_std)
-    out = dict(q=q, k=k, v=v, g=None, a=None, dt_bias=None, A_log=None, beta=None, b=None,
+    out = dict(q=q, k=k, v=v, g=None, g_head=None, a=None, dt_bias=None, A_log=None, beta=None, b=None,
                h0=None, cu_seqlens=cu_seqlens, N=N, B=B, T=T, H=H, K=K, V=V, dtype=dtype,
                gate=gate, beta_mode=beta, l2norm=l2norm, delta=delta,
                scale=(1.0 / math.sqrt(K)) if scale is None else float(scale))
@@ -82,6 +83,8 @@ def chunk_workload(*, seed=2, B=1, T=8192, H=32, K=128, V=128, dtype=torch.bfloa
         out["A_log"] = _uniform(gen, (H,), 0.0, A_log_hi)
     elif gate == "g":
         out["g"] = -_uniform(gen, (B, T, H, K), 0.01, 3.0)
+    elif gate == "head":
+        out["g_head"] = -_uniform(gen, (B, T, H), 0.01, 3.0)
     elif gate != "none":
         raise ValueError(f"unknown gate mode {gate!r}")
     if beta == "logits":

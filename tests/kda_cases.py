@@ -23,7 +23,7 @@ def np64(t):
 
 def to_dev(wl, device="cuda"):
     out = dict(wl)
-    for key in ("q", "k", "v", "g", "a", "dt_bias", "A_log", "beta", "b", "h0", "cu_seqlens"):
+    for key in ("q", "k", "v", "g", "g_head", "a", "dt_bias", "A_log", "beta", "b", "h0", "cu_seqlens"):
         if out.get(key) is not None:
             out[key] = out[key].to(device).contiguous()
     return out
@@ -35,7 +35,7 @@ def gpu_chunk(wl, *, h0=True, final_state=True, err=None, workspace=None, o=None
         d["q"], d["k"], d["v"], scale=d["scale"], g=d["g"], a=d["a"], dt_bias=d["dt_bias"], A_log=d["A_log"],
         beta=d["beta"], b=d["b"], h0=d["h0"] if h0 else None, cu_seqlens=d["cu_seqlens"],
         l2norm_qk=d["l2norm"], delta=d["delta"], output_final_state=final_state, err=err, workspace=workspace,
-        o=o, hT=hT)
+        o=o, hT=hT, g_head=d.get("g_head"))
 
 
 def oracle_chunk(wl, *, h0=True, chunk_size=None):
@@ -43,7 +43,7 @@ def oracle_chunk(wl, *, h0=True, chunk_size=None):
         np64(wl["q"]), np64(wl["k"]), np64(wl["v"]), scale=wl["scale"], g=np64(wl["g"]), a=np64(wl["a"]),
         dt_bias=np64(wl["dt_bias"]), A_log=np64(wl["A_log"]), beta=np64(wl["beta"]), b=np64(wl["b"]),
         h0=np64(wl["h0"]) if h0 else None, cu_seqlens=None if wl["cu_seqlens"] is None else wl["cu_seqlens"].numpy(),
-        l2norm_qk=wl["l2norm"], delta=wl["delta"], chunk_size=chunk_size)
+        l2norm_qk=wl["l2norm"], delta=wl["delta"], chunk_size=chunk_size, g_head=np64(wl.get("g_head")))
 
 
 def subset_heads(wl, heads):
@@ -53,7 +53,7 @@ def subset_heads(wl, heads):
     out = dict(wl)
     out["H"] = len(heads)
     idx = torch.tensor(heads)
-    for key in ("q", "k", "v", "g", "beta", "b"):
+    for key in ("q", "k", "v", "g", "g_head", "beta", "b"):
         if wl.get(key) is not None:
             out[key] = wl[key].index_select(2, idx).contiguous()
     if wl.get("a") is not None:
@@ -74,7 +74,7 @@ def subset_sequence(wl, n):
     out["cu_seqlens"] = None
     out["N"] = 1
     out["T"] = e - s
-    for key in ("q", "k", "v", "g", "a", "beta", "b"):
+    for key in ("q", "k", "v", "g", "g_head", "a", "beta", "b"):
         if wl.get(key) is not None:
             out[key] = wl[key][:, s:e].contiguous()
     if wl.get("h0") is not None:

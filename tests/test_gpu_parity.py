@@ -94,6 +94,19 @@ def test_bf16_gated_delta_off():
     _check_chunk(wl, "bf16_gla")
 
 
+@pytest.mark.parametrize("dtype,K,B,T,lengths", [
+    (torch.float32, 64, 2, 75, None),              # CUDA-core fp32 path
+    (torch.bfloat16, 64, 2, 75, None),             # two-kernel tensor-core path (d = 64)
+    (torch.bfloat16, 128, 2, 75, None),            # fused cluster kernel
+    (torch.bfloat16, 128, 1, 0, [40, 0, 130, 17]),  # fused, packed sequences
+], ids=["fp32_d64", "bf16_d64", "bf16_d128", "bf16_d128_varlen"])
+def test_gated_deltanet_head_gate(dtype, K, B, T, lengths):
+    """Gated DeltaNet (one log-decay per token and head on every key channel)
+    through every chunk-forward path."""
+    wl = W.chunk_workload(seed=45 + K, B=B, T=T or 1, H=3, K=K, V=K, dtype=dtype, gate="head", lengths=lengths)
+    _check_chunk(wl, "gdn")
+
+
 def test_bf16_prefill_reduced():
     """The prefill recipe at T=1024 on 4 heads: checked in full."""
     _check_chunk(W.prefill(T=1024, H=4), "prefill_1024")

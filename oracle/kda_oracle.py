@@ -416,6 +416,17 @@ def kda_recurrent_pool(q, k, v, a, b, A_log, dt_bias, state_pool, indices, *,
     return o, pool
 
 
+def head_rmsnorm(x, weight, eps):
+    """Output-side per-head RMSNorm ([LA] §1 and §4 (3): GLA / GDN / KDA drop
+    the linear-attention normaliser and put an RMSNorm on each head's output).
+    The pages give no formula; the plain RMSNorm is taken: for every row (one
+    token of one head) y = x / sqrt(mean(x^2) + eps) * weight, eps from the caller.
+    x: [..., V]; weight: [V]. Returns y with the shape of x."""
+    x = np.asarray(x, np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + float(eps)) * np.asarray(weight, np.float64)
+
+
 def default_scale(K: int) -> float:
     """K^-0.5, the scale the decode caller passes ([PR] head_k_dim ** -0.5)."""
     return 1.0 / math.sqrt(K)

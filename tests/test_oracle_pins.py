@@ -429,6 +429,22 @@ def pin_head_gate_semiseparable():
     np.testing.assert_allclose(h1, h2, rtol=1e-14, atol=1e-14)
 
 
+def pin_head_rmsnorm():
+    """Hand-worked rows: [3, 4] has mean square 25/2, so with eps = 0 and weight
+    [1, 2] the result is [3, 8] * sqrt(2) / 5; [1, 1] with eps = 1/2 gives
+    weight / sqrt(3/2); a zero row stays zero. With unit weight and eps = 0 every
+    nonzero row comes out with unit mean square, whatever its scale."""
+    y = ko.head_rmsnorm(np.array([[3.0, 4.0]]), np.array([1.0, 2.0]), 0.0)
+    np.testing.assert_allclose(y, [[3 * math.sqrt(2) / 5, 8 * math.sqrt(2) / 5]], rtol=1e-15)
+    y = ko.head_rmsnorm(np.array([[1.0, 1.0], [0.0, 0.0]]), np.array([0.5, -3.0]), 0.5)
+    np.testing.assert_allclose(y[0], np.array([0.5, -3.0]) / math.sqrt(1.5), rtol=1e-15)
+    assert np.all(y[1] == 0.0)
+    x = _rng(19).standard_normal((5, 7)) * np.array([[1e-3], [1.0], [30.0], [2.0], [1e3]])
+    y = ko.head_rmsnorm(x, np.ones(7), 0.0)
+    np.testing.assert_allclose(np.mean(y * y, axis=-1), 1.0, rtol=1e-13)
+    np.testing.assert_allclose(y, ko.head_rmsnorm(4.5 * x, np.ones(7), 0.0), rtol=1e-13)
+
+
 PINS = [
     pin_hand_worked_chunk, pin_level1_quadratic_form, pin_level1_chunk_identity,
     pin_gla_parallel_form, pin_retnet_scalar_decay, pin_chunked_equals_recurrent,
@@ -436,6 +452,7 @@ PINS = [
     pin_beta_zero_pure_decay, pin_orthonormal_keys, pin_gate_sigmoid_l2norm,
     pin_decode_golden, pin_decode_head_grouping, pin_split_sequence, pin_value_split_invariance,
     pin_recurrent_pool_is_repeated_decode, pin_recurrent_pool_tokens_matter, pin_head_gate_semiseparable,
+    pin_head_rmsnorm,
 ]
 
 
@@ -561,6 +578,21 @@ _orig_chunk_matrices = ko.chunk_matrices
 _orig_recurrent_pool = ko.kda_recurrent_pool
 
 
+def _rms_no_weight(x, weight, eps):
+    x = np.asarray(x, np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+
+
+def _rms_sum_not_mean(x, weight, eps):
+    x = np.asarray(x, np.float64)
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps) * np.asarray(weight)
+
+
+def _rms_eps_outside(x, weight, eps):
+    x = np.asarray(x, np.float64)
+    return x / (np.sqrt(np.mean(x * x, axis=-1, keepdims=True)) + eps) * np.asarray(weight)
+
+
 def _hg_first_channel_only(g_head, K):
     g = np.asarray(g_head, np.float64)
     out = np.zeros(g.shape + (K,))
@@ -615,6 +647,9 @@ MUTANTS = [
     ("kda_recurrent_pool", _rp_state_not_carried),
     ("head_gate_to_channels", _hg_first_channel_only),
     ("head_gate_to_channels", _hg_exp_twice),
+    ("head_rmsnorm", _rms_no_weight),
+    ("head_rmsnorm", _rms_sum_not_mean),
+    ("head_rmsnorm", _rms_eps_outside),
 ]
 
 

@@ -362,6 +362,26 @@ def run_gpu(args):
                "algorithmic_bytes": vbytes, "achieved_gbs": vbytes / v_avg / 1e9,
                "launches_per_call": 2, "note": "kda_plan_kernel + kda_chunk_fused_kernel"}
 
+    # --- output-side per-head RMSNorm of the prefill's o (its own timed region) ---
+    rms = None
+    if args.only == "all":
+        w_rms = torch.linspace(0.5, 1.5, D, device=dev)
+        y_rms = torch.empty_like(o)
+        for _ in range(args.warmup):
+            kda.kda_head_rmsnorm(o, w_rms, eps=1e-6, out=y_rms, stream=stream)
+        n0, n1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        n0.record(stream)
+        for _ in range(K):
+            kda.kda_head_rmsnorm(o, w_rms, eps=1e-6, out=y_rms, stream=stream)
+        n1.record(stream)
+        torch.cuda.synchronize(dev)
+        n_avg = n0.elapsed_time(n1) / 1000.0 / K
+        nbytes = 2 * o.numel() * o.element_size() + D * 4
+        rms = {"us": 1e6 * n_avg, "rows": o.numel() // D, "algorithmic_bytes": nbytes,
+               "achieved_gbs": nbytes / n_avg / 1e9, "kernel": "kda_rmsnorm_kernel",
+               "note": "64 MB in + 64 MB out: partly served by L2 (129 MB), so it can exceed the HBM copy rate"}
+
     # --- short-T recurrent step (its own timed region, not part of the step) ---
     rec = None
     if args.only == "all":
@@ -425,6 +445,7 @@ def run_gpu(args):
             "chunk_fwd": {"ms": 1000.0 * chunk_avg, "tokens_per_s": value,
                           "roofline_time_us": 1e6 * t_roof, "frac_of_roofline": t_roof / chunk_avg if chunk_avg > 0 else 0.0},
             "varlen": var,
+            "head_rmsnorm": rms,
             "recurrent": rec,
             "decode": {"us_per_step": 1e6 * dec_avg, "n_valid_rows": n_valid,
                        "roofline": {"bound": "hbm", "achieved": dach, "peak": hbm, "unit": "GB/s",
@@ -441,6 +462,8 @@ def run_gpu(args):
         }
         if var is not None:
             var["frac_of_roofline"] = var["achieved_gbs"] / hbm
+        if rms is not None:
+            rms["frac_of_hbm"] = rms["achieved_gbs"] / hbm
         if rec is not None:
             rec["roofline"]["peak"] = hbm
             rec["roofline"]["frac"] = rec["roofline"]["achieved"] / hbm

@@ -6,6 +6,7 @@
  *   kda_chunk_workspace_size  scratch bytes kda_chunk_fwd needs for given arguments
  *   kda_decode_step           fused T=1 decode step on a packed q|k|v row with a slot pool
  *   kda_recurrent_step        T tokens per row (T <= 64) on a slot pool: speculative / extend steps
+ *   kda_head_rmsnorm          output-side per-head RMSNorm of attention outputs
  *   kda_chunk_fwd_noalloc     kda_chunk_fwd on a library-owned scratch buffer (no allocation)
  *   kda_version               library version string
  *
@@ -234,6 +235,27 @@ typedef struct kda_recurrent_args {
 
 /* Short-T recurrent step. Returns KDA_OK once the work is enqueued. */
 kda_status kda_recurrent_step(const kda_recurrent_args* args, kda_stream_t stream);
+
+/*
+ * Output-side per-head RMSNorm ("06 · linear 路线（一）" §1 and §4 (3): GLA, GDN
+ * and KDA drop the linear-attention normaliser and normalise each head's
+ * output instead). The pages give no formula; this is the plain RMSNorm:
+ *   y[r, :] = x[r, :] / sqrt(mean(x[r, :]^2) + eps) * weight[:]
+ * over R rows of V values, a row being one token of one head (o of the chunk
+ * forward or the decode viewed as [B*T*H, V]).
+ *   x, y    [R, V]   bf16, 16-byte aligned; y may be x (in place)
+ *   weight  [V]      fp32, 16-byte aligned
+ * Supported: V in {64, 128}. Returns KDA_OK once the work is enqueued.
+ */
+typedef struct kda_rmsnorm_args {
+  int64_t R;
+  int32_t V;
+  float eps;
+  const void* x;
+  const float* weight;
+  void* y;
+} kda_rmsnorm_args;
+kda_status kda_head_rmsnorm(const kda_rmsnorm_args* args, kda_stream_t stream);
 
 /*
  * Chunk forward for callers that cannot allocate device memory.

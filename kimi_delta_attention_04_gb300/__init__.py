@@ -13,6 +13,7 @@ from ._lib import (  # noqa: F401
     kda_chunk_fwd,
     kda_chunk_fwd_noalloc,
     kda_decode_step,
+    kda_head_rmsnorm,
     kda_recurrent_step,
     lib_path,
     load,

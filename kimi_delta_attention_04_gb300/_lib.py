@@ -80,8 +80,16 @@ class RecurrentArgs(ctypes.Structure):
 
 KDA_RECURRENT_MAX_T = 64
 
+
+class RmsNormArgs(ctypes.Structure):
+    _fields_ = [
+        ("R", ctypes.c_int64), ("V", ctypes.c_int32), ("eps", ctypes.c_float),
+        ("x", ctypes.c_void_p), ("weight", ctypes.c_void_p), ("y", ctypes.c_void_p),
+    ]
+
+
 EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_chunk_workspace_size", "kda_decode_step",
-           "kda_recurrent_step", "kda_version")
+           "kda_recurrent_step", "kda_head_rmsnorm", "kda_version")
 
 
 def lib_path() -> Path:
@@ -107,6 +115,8 @@ def load() -> ctypes.CDLL:
         lib.kda_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
         lib.kda_recurrent_step.restype = ctypes.c_int
         lib.kda_recurrent_step.argtypes = [ctypes.POINTER(RecurrentArgs), ctypes.c_void_p]
+        lib.kda_head_rmsnorm.restype = ctypes.c_int
+        lib.kda_head_rmsnorm.argtypes = [ctypes.POINTER(RmsNormArgs), ctypes.c_void_p]
         lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
         lib.kda_chunk_fwd_noalloc.argtypes = [ctypes.POINTER(ChunkArgs), ctypes.c_void_p]
         lib.kda_version.restype = ctypes.c_char_p
@@ -299,3 +309,20 @@ def kda_recurrent_step(q, k, v, a, b, A_log, dt_bias, state_pool, indices, *, sc
     if st != KDA_OK:
         raise KdaError(st, "kda_recurrent_step")
     return o
+
+
+def kda_head_rmsnorm(x, weight, *, eps, out=None, stream=None):
+    """Per-head RMSNorm over the last axis (V) of x (bf16, any leading shape) with
+    an fp32 weight [V]; out may be x itself. Returns out."""
+    lib = load()
+    if out is None:
+        out = torch.empty_like(x)
+    args = RmsNormArgs()
+    args.V = int(x.shape[-1])
+    args.R = int(x.numel() // max(args.V, 1))
+    args.eps = float(eps)
+    args.x, args.weight, args.y = _ptr(x), _ptr(weight), _ptr(out)
+    st = lib.kda_head_rmsnorm(ctypes.byref(args), _stream_ptr(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_head_rmsnorm")
+    return out

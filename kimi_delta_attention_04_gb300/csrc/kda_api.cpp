@@ -218,6 +218,24 @@ kda_status kda_recurrent_step(const kda_recurrent_args* a, kda_stream_t stream) 
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+kda_status kda_head_rmsnorm(const kda_rmsnorm_args* a, kda_stream_t stream) {
+  if (a == nullptr || a->R < 0 || !(a->eps >= 0.f)) return KDA_ERR_INVALID_ARG;
+  if (a->V != 64 && a->V != 128) return KDA_ERR_UNSUPPORTED;
+  if (a->R > 0) {
+    if (!a->x || !a->weight || !a->y) return KDA_ERR_INVALID_ARG;
+    if (!aligned(a->x, 16) || !aligned(a->y, 16) || !aligned(a->weight, 16)) return KDA_ERR_INVALID_ARG;
+  }
+  kda::RmsNormCall c;
+  c.R = a->R;
+  c.V = a->V;
+  c.eps = a->eps;
+  c.x = a->x;
+  c.weight = a->weight;
+  c.y = a->y;
+  const cudaError_t e = kda::launch_rmsnorm(c, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 const char* kda_version(void) { return "kda-gb300 0.1.0 sm_103a"; }
 
 }  // extern "C"

@@ -81,6 +81,15 @@ struct RecurrentCall {
   int32_t* err;
 };
 
+struct RmsNormCall {
+  long long R;
+  int V;
+  float eps;
+  const void* x;
+  const float* weight;
+  void* y;
+};
+
 // Bytes of one (chunk, head) prep record.
 size_t record_bytes_tc(int d);           // bf16 tensor-core path, dk = dv = d
 size_t record_bytes_f32(int dk, int dv);  // fp32 path
@@ -93,5 +102,6 @@ size_t fused_smem_bytes();
 size_t fused_workspace_bytes();  // pool of per-cluster global rings (fixed size)
 cudaError_t launch_decode(const DecodeCall& c, cudaStream_t s);
 cudaError_t launch_recurrent(const RecurrentCall& c, cudaStream_t s);
+cudaError_t launch_rmsnorm(const RmsNormCall& c, cudaStream_t s);
 
 }  // namespace kda

@@ -51,6 +51,7 @@ def test_struct_layout_matches_c(tmp_path):
     fields_c = [f for f, _ in _lib.ChunkArgs._fields_]
     fields_d = [f for f, _ in _lib.DecodeArgs._fields_]
     fields_r = [f for f, _ in _lib.RecurrentArgs._fields_]
+    fields_n = [f for f, _ in _lib.RmsNormArgs._fields_]
     lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void){"]
     lines.append('printf("chunk %zu\\n", sizeof(kda_chunk_args));')
     for f in fields_c:
@@ -62,6 +63,9 @@ def test_struct_layout_matches_c(tmp_path):
     for f in fields_r:
         lines.append(f'printf("r.{f} %zu\\n", offsetof(kda_recurrent_args, {f}));')
     lines.append('printf("maxT %d\\n", KDA_RECURRENT_MAX_T);')
+    lines.append('printf("rmsnorm %zu\\n", sizeof(kda_rmsnorm_args));')
+    for f in fields_n:
+        lines.append(f'printf("n.{f} %zu\\n", offsetof(kda_rmsnorm_args, {f}));')
     lines.append("return 0;}")
     src.write_text("\n".join(lines))
     exe = tmp_path / "layout"
@@ -78,6 +82,9 @@ def test_struct_layout_matches_c(tmp_path):
     for f in fields_r:
         assert int(got[f"r.{f}"]) == getattr(_lib.RecurrentArgs, f).offset, f
     assert int(got["maxT"]) == _lib.KDA_RECURRENT_MAX_T
+    assert int(got["rmsnorm"]) == ctypes.sizeof(_lib.RmsNormArgs)
+    for f in fields_n:
+        assert int(got[f"n.{f}"]) == getattr(_lib.RmsNormArgs, f).offset, f
 
 
 # --- host-side validation, exercised with fake (never dereferenced) pointers ---
@@ -210,6 +217,24 @@ def test_recurrent_validation_rejects(lib, over, status):
     a = _rec(**over)
     assert lib.kda_recurrent_step(ctypes.byref(a), None) == status
     assert lib.kda_recurrent_step(None, None) == _lib.KDA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(V=96), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(R=-1), _lib.KDA_ERR_INVALID_ARG),
+    (dict(x=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(weight=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(y=FAKE + 2), _lib.KDA_ERR_INVALID_ARG),   # misaligned
+    (dict(eps=-1.0), _lib.KDA_ERR_INVALID_ARG),
+    (dict(eps=float("nan")), _lib.KDA_ERR_INVALID_ARG),
+])
+def test_rmsnorm_validation_rejects(lib, over, status):
+    a = _lib.RmsNormArgs()
+    a.R, a.V, a.eps = 10, 128, 1e-6
+    a.x = a.weight = a.y = FAKE
+    for k, v in over.items():
+        setattr(a, k, v)
+    assert lib.kda_head_rmsnorm(ctypes.byref(a), None) == status
 
 
 def test_python_binding_refuses_cpu_tensors():

@@ -427,6 +427,51 @@ def head_rmsnorm(x, weight, eps):
     return x / np.sqrt(ms + float(eps)) * np.asarray(weight, np.float64)
 
 
+def silu(x):
+    """x * sigmoid(x), the activation the decode path applies after the conv."""
+    x = np.asarray(x, np.float64)
+    return x * sigmoid(x)
+
+
+def causal_conv1d_update(x, conv_state, weight, bias):
+    """One step of a depthwise causal convolution per channel ([PR] "关键源码片段",
+    KDAAttnBackend.forward_decode: causal_conv1d_update(mixed_qkv, conv_states,
+    conv_weights, bias, activation="silu") runs before the packed decode).
+
+    x: [C] new input; conv_state: [W-1, C] the previous W-1 inputs, oldest
+    first; weight: [C, W] (tap W-1 multiplies the newest input); bias: [C] or
+    None. Returns (y = silu(sum_i weight[:, i] * window[i] + bias), new_state)
+    with window = [conv_state; x] and new_state = window[1:].
+    """
+    x = np.asarray(x, np.float64)
+    window = np.concatenate([np.asarray(conv_state, np.float64), x[None]], axis=0)  # [W, C]
+    pre = np.einsum("cw,wc->c", np.asarray(weight, np.float64), window)
+    if bias is not None:
+        pre = pre + np.asarray(bias, np.float64)
+    return silu(pre), window[1:]
+
+
+def kda_decode_conv(mixed_qkv, conv_state, conv_weight, conv_bias, a, b, A_log, dt_bias, state_pool,
+                    indices, *, H, HV, K, V, scale, l2norm_qk=True):
+    """The decode step with its conv in front: per valid row, causal_conv1d_update
+    + SiLU of the packed [q | k | v] row on the row's slot of the conv-state pool,
+    then kda_decode on the result. conv_state: [num_slots, W-1, C], C = 2*H*K +
+    HV*V. Returns (o, new_state_pool, new_conv_state); inputs are not modified.
+    Pad rows: o = 0, neither pool touched."""
+    x = np.asarray(mixed_qkv, np.float64)
+    cs = np.array(np.asarray(conv_state, np.float64))
+    idx = np.asarray(indices).astype(np.int64)
+    y = np.zeros_like(x)
+    for row in range(x.shape[0]):
+        s = int(idx[row])
+        if s < 0:
+            continue
+        y[row], cs[s] = causal_conv1d_update(x[row], cs[s], conv_weight, conv_bias)
+    o, pool = kda_decode(y, a, b, A_log, dt_bias, state_pool, indices, H=H, HV=HV, K=K, V=V, scale=scale,
+                         l2norm_qk=l2norm_qk)
+    return o, pool, cs
+
+
 def default_scale(K: int) -> float:
     """K^-0.5, the scale the decode caller passes ([PR] head_k_dim ** -0.5)."""
     return 1.0 / math.sqrt(K)

@@ -445,6 +445,66 @@ def pin_head_rmsnorm():
     np.testing.assert_allclose(y, ko.head_rmsnorm(4.5 * x, np.ones(7), 0.0), rtol=1e-13)
 
 
+def pin_conv1d_update_is_causal_convolution():
+    """Stepping causal_conv1d_update through a sequence equals numpy's full
+    convolution of each channel with its (reversed-tap) kernel, truncated to the
+    causal part, then SiLU; an impulse history returns the taps; SiLU(x) =
+    x / (1 + e^{-x})."""
+    r = _rng(20)
+    C, W, T = 5, 4, 11
+    x = r.standard_normal((T, C))
+    w = r.standard_normal((C, W))
+    bias = r.standard_normal(C)
+    state = np.zeros((W - 1, C))
+    ys = []
+    for t in range(T):
+        y, state = ko.causal_conv1d_update(x[t], state, w, bias)
+        ys.append(y)
+    for c in range(C):
+        full = np.convolve(x[:, c], w[c, ::-1])[:T] + bias[c]
+        np.testing.assert_allclose(np.array(ys)[:, c], full / (1 + np.exp(-full)), rtol=1e-13, atol=1e-14)
+    imp = np.zeros((W - 1, C))
+    imp[0] = 1.0
+    y, _ = ko.causal_conv1d_update(np.zeros(C), imp, w, None)
+    pre = w[:, 0]
+    np.testing.assert_allclose(y, pre / (1 + np.exp(-pre)), rtol=1e-14)
+
+
+def pin_decode_conv_state_and_pads():
+    """After W-1 decode steps with the conv in front, a valid row's conv state
+    holds exactly its last W-1 inputs (whatever it started as); pad rows get
+    o = 0 and leave both pools alone; a valid row's output matches decoding the
+    SiLU of the causal convolution over its full input history."""
+    r = _rng(21)
+    B, H, HV, K, V, W, slots = 3, 1, 2, 4, 3, 3, 4
+    C = 2 * H * K + HV * V
+    w = r.standard_normal((C, W))
+    bias = r.standard_normal(C)
+    cs0 = r.standard_normal((slots, W - 1, C))
+    pool = r.standard_normal((slots, HV, V, K))
+    idx = np.array([2, -1, 0])
+    A_log, dt = r.uniform(0, 1, HV), r.uniform(-1, 1, HV * K)
+    xs = [r.standard_normal((B, C)) for _ in range(W - 1)]
+    cs, p = cs0, pool
+    for x in xs:
+        a, bb = r.standard_normal((B, HV * K)), r.standard_normal((B, HV))
+        o, p, cs = ko.kda_decode_conv(x, cs, w, bias, a, bb, A_log, dt, p, idx, H=H, HV=HV, K=K, V=V, scale=0.5)
+        assert np.all(o[1] == 0.0)
+    for row, s in ((0, 2), (2, 0)):
+        np.testing.assert_array_equal(cs[s], np.stack([x[row] for x in xs]))
+    for s in (1, 3):
+        np.testing.assert_array_equal(cs[s], cs0[s])
+        np.testing.assert_array_equal(p[s], pool[s])
+    # one more step from a zero history: the output is the decode of SiLU(w[:, -1] x + bias)
+    x = r.standard_normal((B, C))
+    a, bb = r.standard_normal((B, HV * K)), r.standard_normal((B, HV))
+    o, _, _ = ko.kda_decode_conv(x, np.zeros_like(cs0), w, bias, a, bb, A_log, dt, pool, idx, H=H, HV=HV, K=K, V=V,
+                                 scale=0.5)
+    pre = w[:, -1] * x + bias
+    o2, _ = ko.kda_decode(pre / (1 + np.exp(-pre)), a, bb, A_log, dt, pool, idx, H=H, HV=HV, K=K, V=V, scale=0.5)
+    np.testing.assert_allclose(o, o2, rtol=1e-13, atol=1e-14)
+
+
 PINS = [
     pin_hand_worked_chunk, pin_level1_quadratic_form, pin_level1_chunk_identity,
     pin_gla_parallel_form, pin_retnet_scalar_decay, pin_chunked_equals_recurrent,
@@ -452,7 +512,7 @@ PINS = [
     pin_beta_zero_pure_decay, pin_orthonormal_keys, pin_gate_sigmoid_l2norm,
     pin_decode_golden, pin_decode_head_grouping, pin_split_sequence, pin_value_split_invariance,
     pin_recurrent_pool_is_repeated_decode, pin_recurrent_pool_tokens_matter, pin_head_gate_semiseparable,
-    pin_head_rmsnorm,
+    pin_head_rmsnorm, pin_conv1d_update_is_causal_convolution, pin_decode_conv_state_and_pads,
 ]
 
 
@@ -578,6 +638,42 @@ _orig_chunk_matrices = ko.chunk_matrices
 _orig_recurrent_pool = ko.kda_recurrent_pool
 
 
+def _conv_taps_reversed(x, conv_state, weight, bias):
+    return ko_conv_orig(x, conv_state, np.asarray(weight)[:, ::-1], bias)
+
+
+def _conv_no_shift(x, conv_state, weight, bias):
+    y, _ = ko_conv_orig(x, conv_state, weight, bias)
+    return y, np.asarray(conv_state, np.float64)
+
+
+def _silu_plain_sigmoid(x):
+    return ko.sigmoid(x)
+
+
+ko_conv_orig = ko.causal_conv1d_update
+_orig_decode_conv = ko.kda_decode_conv
+
+
+def _dc_conv_on_pads(mixed_qkv, conv_state, conv_weight, conv_bias, *args, **kw):
+    o, pool, cs = _orig_decode_conv(mixed_qkv, conv_state, conv_weight, conv_bias, *args, **kw)
+    idx = np.asarray(args[5])
+    cs = np.array(cs)
+    for row in np.nonzero(idx < 0)[0]:
+        _, cs[(row + 1) % cs.shape[0]] = ko.causal_conv1d_update(mixed_qkv[row], cs[(row + 1) % cs.shape[0]],
+                                                                 conv_weight, conv_bias)
+    return o, pool, cs
+
+
+def _dc_no_activation(mixed_qkv, conv_state, conv_weight, conv_bias, *args, **kw):
+    saved = ko.silu
+    ko.silu = lambda x: np.asarray(x, np.float64)
+    try:
+        return _orig_decode_conv(mixed_qkv, conv_state, conv_weight, conv_bias, *args, **kw)
+    finally:
+        ko.silu = saved
+
+
 def _rms_no_weight(x, weight, eps):
     x = np.asarray(x, np.float64)
     return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
@@ -650,6 +746,11 @@ MUTANTS = [
     ("head_rmsnorm", _rms_no_weight),
     ("head_rmsnorm", _rms_sum_not_mean),
     ("head_rmsnorm", _rms_eps_outside),
+    ("causal_conv1d_update", _conv_taps_reversed),
+    ("causal_conv1d_update", _conv_no_shift),
+    ("silu", _silu_plain_sigmoid),
+    ("kda_decode_conv", _dc_conv_on_pads),
+    ("kda_decode_conv", _dc_no_activation),
 ]
 
 

@@ -362,6 +362,33 @@ def run_gpu(args):
                "algorithmic_bytes": vbytes, "achieved_gbs": vbytes / v_avg / 1e9,
                "launches_per_call": 2, "note": "kda_plan_kernel + kda_chunk_fused_kernel"}
 
+    # --- decode with the causal conv1d + SiLU fused in front (its own timed region) ---
+    dconv = None
+    if args.only == "all":
+        cw = W.decode_conv_workload(seed=6 + 100 * rank, W=4)
+        cd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in cw.items()}
+        oc = torch.empty(cw["B"], cw["HV"], cw["V"], dtype=torch.bfloat16, device=dev)
+
+        def conv_step():
+            kda.kda_decode_conv_step(cd["packed_qkv"], cd["conv_state"], cd["conv_weight"], cd["conv_bias"], cd["a"],
+                                     cd["b"], cd["A_log"], cd["dt_bias"], cd["state_pool"], cd["indices"], H=cw["H"],
+                                     HV=cw["HV"], K=cw["K"], V=cw["V"], scale=cw["scale"], o=oc, stream=stream)
+        for _ in range(args.warmup):
+            conv_step()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        c0.record(stream)
+        for _ in range(K):
+            conv_step()
+        c1.record(stream)
+        torch.cuda.synchronize(dev)
+        c_avg = c0.elapsed_time(c1) / 1000.0 / K
+        c_valid = int((cw["indices"] >= 0).sum())
+        C = cw["packed_qkv"].shape[1]
+        cbytes = decode_algorithmic_bytes(c_valid) + c_valid * (cw["W"] - 1) * C * 2 * 2 + C * cw["W"] * 4 + C * 4
+        dconv = {"us_per_step": 1e6 * c_avg, "width": cw["W"], "n_valid_rows": c_valid, "algorithmic_bytes": cbytes,
+                 "achieved_gbs": cbytes / c_avg / 1e9, "kernel": "kda_decode_kernel<conv>"}
+
     # --- output-side per-head RMSNorm of the prefill's o (its own timed region) ---
     rms = None
     if args.only == "all":
@@ -446,6 +473,7 @@ def run_gpu(args):
                           "roofline_time_us": 1e6 * t_roof, "frac_of_roofline": t_roof / chunk_avg if chunk_avg > 0 else 0.0},
             "varlen": var,
             "head_rmsnorm": rms,
+            "decode_conv": dconv,
             "recurrent": rec,
             "decode": {"us_per_step": 1e6 * dec_avg, "n_valid_rows": n_valid,
                        "roofline": {"bound": "hbm", "achieved": dach, "peak": hbm, "unit": "GB/s",
@@ -464,6 +492,8 @@ def run_gpu(args):
             var["frac_of_roofline"] = var["achieved_gbs"] / hbm
         if rms is not None:
             rms["frac_of_hbm"] = rms["achieved_gbs"] / hbm
+        if dconv is not None:
+            dconv["frac_of_hbm"] = dconv["achieved_gbs"] / hbm
         if rec is not None:
             rec["roofline"]["peak"] = hbm
             rec["roofline"]["frac"] = rec["roofline"]["achieved"] / hbm

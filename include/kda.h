@@ -5,6 +5,7 @@
  *   kda_chunk_fwd             chunkwise KDA forward over one batch of sequences
  *   kda_chunk_workspace_size  scratch bytes kda_chunk_fwd needs for given arguments
  *   kda_decode_step           fused T=1 decode step on a packed q|k|v row with a slot pool
+ *   kda_decode_conv_step      the decode step with its causal conv1d + SiLU fused in front
  *   kda_recurrent_step        T tokens per row (T <= 64) on a slot pool: speculative / extend steps
  *   kda_head_rmsnorm          output-side per-head RMSNorm of attention outputs
  *   kda_chunk_fwd_noalloc     kda_chunk_fwd on a library-owned scratch buffer (no allocation)
@@ -187,6 +188,40 @@ typedef struct kda_decode_args {
 
 /* Fused T=1 decode step. Returns KDA_OK once the work is enqueued. */
 kda_status kda_decode_step(const kda_decode_args* args, kda_stream_t stream);
+
+/*
+ * The decode step with its depthwise causal conv1d + SiLU fused in front (the
+ * sglang PR #26586 summary's KDAAttnBackend.forward_decode runs
+ * causal_conv1d_update(mixed_qkv, conv_states, conv_weights, bias,
+ * activation="silu") right before the packed decode). For every valid row b
+ * with slot s and every channel c of the packed row (C = 2*H*K + HV*V):
+ *   window = [conv_state_in[s, 0..W-2, c], dec.packed_qkv[b, c]]   (oldest first)
+ *   x[b, c] = silu(sum_i conv_weight[c, i] * window[i] + conv_bias[c])
+ *   conv_state_out[s, :, c] = window[1..W-1]
+ * then the decode step of kda_decode_step runs on x as its packed q|k|v row.
+ *   dec             all fields as for kda_decode_step; dec.packed_qkv holds
+ *                   the conv input (bf16 [B, C])
+ *   W               conv width, 2..4
+ *   conv_state_in   bf16 [num_slots, W-1, C]
+ *   conv_state_out  bf16 [num_slots, W-1, C]; only the valid rows' slots are
+ *                   written. It may be conv_state_in (update in place) only
+ *                   when HV == H: with HV > H a q/k channel is read by the HV/H
+ *                   value heads of its group and written by the first one, so
+ *                   an in-place update would race.
+ *   conv_weight     fp32 [C, W] (tap W-1 multiplies the newest input)
+ *   conv_bias       fp32 [C] or NULL
+ * Padding rows write o = 0 and touch neither pool. Returns KDA_OK once the
+ * work is enqueued.
+ */
+typedef struct kda_decode_conv_args {
+  kda_decode_args dec;
+  int32_t W;
+  const void* conv_state_in;
+  void* conv_state_out;
+  const float* conv_weight;
+  const float* conv_bias;
+} kda_decode_conv_args;
+kda_status kda_decode_conv_step(const kda_decode_conv_args* args, kda_stream_t stream);
 
 /*
  * Arguments of kda_recurrent_step: T tokens per batch row on a state-slot pool.

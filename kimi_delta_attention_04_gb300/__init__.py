@@ -12,6 +12,7 @@ from ._lib import (  # noqa: F401
     chunk_workspace_size,
     kda_chunk_fwd,
     kda_chunk_fwd_noalloc,
+    kda_decode_conv_step,
     kda_decode_step,
     kda_head_rmsnorm,
     kda_recurrent_step,

@@ -66,6 +66,13 @@ class DecodeArgs(ctypes.Structure):
     ]
 
 
+class DecodeConvArgs(ctypes.Structure):
+    _fields_ = [
+        ("dec", DecodeArgs), ("W", ctypes.c_int32), ("conv_state_in", ctypes.c_void_p),
+        ("conv_state_out", ctypes.c_void_p), ("conv_weight", ctypes.c_void_p), ("conv_bias", ctypes.c_void_p),
+    ]
+
+
 class RecurrentArgs(ctypes.Structure):
     _fields_ = [
         ("B", ctypes.c_int32), ("T", ctypes.c_int32), ("H", ctypes.c_int32), ("HV", ctypes.c_int32),
@@ -89,7 +96,7 @@ class RmsNormArgs(ctypes.Structure):
 
 
 EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_chunk_workspace_size", "kda_decode_step",
-           "kda_recurrent_step", "kda_head_rmsnorm", "kda_version")
+           "kda_decode_conv_step", "kda_recurrent_step", "kda_head_rmsnorm", "kda_version")
 
 
 def lib_path() -> Path:
@@ -115,6 +122,8 @@ def load() -> ctypes.CDLL:
         lib.kda_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
         lib.kda_recurrent_step.restype = ctypes.c_int
         lib.kda_recurrent_step.argtypes = [ctypes.POINTER(RecurrentArgs), ctypes.c_void_p]
+        lib.kda_decode_conv_step.restype = ctypes.c_int
+        lib.kda_decode_conv_step.argtypes = [ctypes.POINTER(DecodeConvArgs), ctypes.c_void_p]
         lib.kda_head_rmsnorm.restype = ctypes.c_int
         lib.kda_head_rmsnorm.argtypes = [ctypes.POINTER(RmsNormArgs), ctypes.c_void_p]
         lib.kda_chunk_fwd_noalloc.restype = ctypes.c_int
@@ -326,3 +335,27 @@ def kda_head_rmsnorm(x, weight, *, eps, out=None, stream=None):
     if st != KDA_OK:
         raise KdaError(st, "kda_head_rmsnorm")
     return out
+
+
+def kda_decode_conv_step(mixed_qkv, conv_state_in, conv_weight, conv_bias, a, b, A_log, dt_bias, state_pool,
+                         indices, *, H, HV, K, V, scale, conv_state_out=None, l2norm_qk=True, o=None, err=None,
+                         stream=None):
+    """Decode with its causal conv1d + SiLU in front (see include/kda.h).
+    mixed_qkv bf16 [B, C] is the conv input; conv_state_in bf16 [slots, W-1, C];
+    conv_weight fp32 [C, W]; conv_bias fp32 [C] or None. conv_state_out defaults
+    to conv_state_in (in place, allowed when HV == H). state_pool is updated in
+    place. Returns o [B, HV, V] bf16."""
+    lib = load()
+    if o is None:
+        o = torch.empty(mixed_qkv.shape[0], HV, V, dtype=torch.bfloat16, device=mixed_qkv.device)
+    args = DecodeConvArgs()
+    args.dec = make_decode_args(mixed_qkv, a, b, A_log, dt_bias, state_pool, indices, H=H, HV=HV, K=K, V=V,
+                                scale=scale, l2norm_qk=l2norm_qk, o=o, err=err)
+    args.W = int(conv_weight.shape[-1])
+    args.conv_state_in = _ptr(conv_state_in)
+    args.conv_state_out = _ptr(conv_state_in if conv_state_out is None else conv_state_out)
+    args.conv_weight, args.conv_bias = _ptr(conv_weight), _ptr(conv_bias)
+    st = lib.kda_decode_conv_step(ctypes.byref(args), _stream_ptr(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_conv_step")
+    return o

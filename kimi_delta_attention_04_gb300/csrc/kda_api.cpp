@@ -135,7 +135,9 @@ kda_status kda_chunk_fwd(const kda_chunk_args* args, void* workspace, size_t ws_
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
-kda_status kda_decode_step(const kda_decode_args* a, kda_stream_t stream) {
+namespace {
+
+kda_status check_decode(const kda_decode_args* a, kda::DecodeCall* c) {
   if (a == nullptr) return KDA_ERR_INVALID_ARG;
   if (a->B < 0 || a->H < 1 || a->HV < 1 || a->K < 1 || a->V < 1 || a->num_slots < 0) return KDA_ERR_INVALID_ARG;
   if (a->HV % a->H != 0) return KDA_ERR_INVALID_ARG;
@@ -151,24 +153,60 @@ kda_status kda_decode_step(const kda_decode_args* a, kda_stream_t stream) {
     if (a->num_slots > 0 && (!a->state_pool || !aligned(a->state_pool, 16))) return KDA_ERR_INVALID_ARG;
   }
   if (a->err && !aligned(a->err, 4)) return KDA_ERR_INVALID_ARG;
+  c->B = a->B;
+  c->H = a->H;
+  c->HV = a->HV;
+  c->K = a->K;
+  c->V = a->V;
+  c->num_slots = a->num_slots;
+  c->l2norm = (a->flags & KDA_FLAG_L2NORM_QK) != 0;
+  c->scale = a->scale;
+  c->packed_qkv = a->packed_qkv;
+  c->a = a->a;
+  c->b = a->b;
+  c->A_log = a->A_log;
+  c->dt_bias = a->dt_bias;
+  c->state_pool = a->state_pool;
+  c->indices = a->indices;
+  c->o = a->o;
+  c->err = a->err;
+  c->conv_W = 0;
+  c->conv_in = nullptr;
+  c->conv_out = nullptr;
+  c->conv_w = nullptr;
+  c->conv_b = nullptr;
+  return KDA_OK;
+}
+
+}  // namespace
+
+kda_status kda_decode_step(const kda_decode_args* a, kda_stream_t stream) {
   kda::DecodeCall c;
-  c.B = a->B;
-  c.H = a->H;
-  c.HV = a->HV;
-  c.K = a->K;
-  c.V = a->V;
-  c.num_slots = a->num_slots;
-  c.l2norm = (a->flags & KDA_FLAG_L2NORM_QK) != 0;
-  c.scale = a->scale;
-  c.packed_qkv = a->packed_qkv;
-  c.a = a->a;
-  c.b = a->b;
-  c.A_log = a->A_log;
-  c.dt_bias = a->dt_bias;
-  c.state_pool = a->state_pool;
-  c.indices = a->indices;
-  c.o = a->o;
-  c.err = a->err;
+  const kda_status st = check_decode(a, &c);
+  if (st != KDA_OK) return st;
+  const cudaError_t e = kda::launch_decode(c, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_decode_conv_step(const kda_decode_conv_args* a, kda_stream_t stream) {
+  if (a == nullptr) return KDA_ERR_INVALID_ARG;
+  kda::DecodeCall c;
+  const kda_status st = check_decode(&a->dec, &c);
+  if (st != KDA_OK) return st;
+  if (a->W < 2 || a->W > 4) return KDA_ERR_UNSUPPORTED;
+  if (a->dec.B > 0 && a->dec.num_slots > 0) {
+    if (!a->conv_state_in || !a->conv_state_out || !a->conv_weight) return KDA_ERR_INVALID_ARG;
+    if (!aligned(a->conv_state_in, 2) || !aligned(a->conv_state_out, 2) || !aligned(a->conv_weight, 4) ||
+        (a->conv_bias && !aligned(a->conv_bias, 4)))
+      return KDA_ERR_INVALID_ARG;
+    if (a->conv_state_in == a->conv_state_out && a->dec.HV != a->dec.H) return KDA_ERR_INVALID_ARG;
+  }
+  c.conv_W = a->W;
+  c.conv_in = a->conv_state_in;
+  c.conv_out = a->conv_state_out;
+  c.conv_w = a->conv_weight;
+  c.conv_b = a->conv_bias;
+  // (without slots every row is padding or out of range: the kernel only zeroes o)
   const cudaError_t e = kda::launch_decode(c, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -50,7 +50,47 @@ __device__ __forceinline__ void load_bf16(const __nv_bfloat16* p, float (&x)[CPL
   }
 }
 
-template <int K, int V>
+// Causal conv1d + SiLU of one channel c of a row ("关键源码片段",
+// KDAAttnBackend.forward_decode: causal_conv1d_update before the packed decode):
+// window = [conv state (W-1 inputs, oldest first); x], y = silu(w . window + b).
+// When `write`, the slot's state becomes window[1:] (exact bf16 copies).
+__device__ __forceinline__ float conv_silu(const DecodeCall& p, int slot, int b, int C, int c, bool write) {
+  const int W = p.conv_W;
+  const __nv_bfloat16* in = reinterpret_cast<const __nv_bfloat16*>(p.conv_in) + static_cast<size_t>(slot) * (W - 1) * C;
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.conv_out) + static_cast<size_t>(slot) * (W - 1) * C;
+  const __nv_bfloat16 x = reinterpret_cast<const __nv_bfloat16*>(p.packed_qkv)[static_cast<size_t>(b) * C + c];
+  float acc = p.conv_b ? p.conv_b[c] : 0.f;
+  __nv_bfloat16 win[3];
+#pragma unroll
+  for (int i = 0; i < 3; ++i)
+    if (i < W - 1) {
+      win[i] = in[static_cast<size_t>(i) * C + c];
+      acc += p.conv_w[static_cast<size_t>(c) * W + i] * __bfloat162float(win[i]);
+    }
+  acc += p.conv_w[static_cast<size_t>(c) * W + W - 1] * __bfloat162float(x);
+  if (write) {
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+      if (i < W - 1) out[static_cast<size_t>(i) * C + c] = (i + 1 < W - 1) ? win[i + 1] : x;
+  }
+  return acc / (1.f + expf(-acc));
+}
+
+// The state shift of conv_silu alone (window[1:] into the slot), for channels
+// whose output was computed by several threads that all had to read first.
+__device__ __forceinline__ void conv_shift(const DecodeCall& p, int slot, int b, int C, int c) {
+  const int W = p.conv_W;
+  const __nv_bfloat16* in = reinterpret_cast<const __nv_bfloat16*>(p.conv_in) + static_cast<size_t>(slot) * (W - 1) * C;
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.conv_out) + static_cast<size_t>(slot) * (W - 1) * C;
+#pragma unroll
+  for (int i = 0; i < 3; ++i)
+    if (i < W - 1)
+      out[static_cast<size_t>(i) * C + c] =
+          (i + 1 < W - 1) ? in[static_cast<size_t>(i + 1) * C + c]
+                          : reinterpret_cast<const __nv_bfloat16*>(p.packed_qkv)[static_cast<size_t>(b) * C + c];
+}
+
+template <int K, int V, bool CONV>
 __global__ void __launch_bounds__(kDecodeThreads) kda_decode_kernel(const DecodeCall p) {
   constexpr int CPL = K / 32;                 // key channels per lane
   constexpr int ROWS_PER_WARP = V / 4;
@@ -82,11 +122,34 @@ __global__ void __launch_bounds__(kDecodeThreads) kda_decode_kernel(const Decode
   for (int r = 0; r < kRowGroup; ++r)
     cur[r] = __ldcs(reinterpret_cast<const Vec*>(S + static_cast<size_t>(row0 + r) * K + col0));
 
-  const __nv_bfloat16* row = reinterpret_cast<const __nv_bfloat16*>(p.packed_qkv) +
-                             static_cast<size_t>(b) * (2 * p.H * K + p.HV * V);
+  const int C = 2 * p.H * K + p.HV * V;
+  const __nv_bfloat16* row = reinterpret_cast<const __nv_bfloat16*>(p.packed_qkv) + static_cast<size_t>(b) * C;
   float qv[CPL], kv[CPL], av[CPL];
-  load_bf16<CPL>(row + h * K + col0, qv);
-  load_bf16<CPL>(row + p.H * K + h * K + col0, kv);
+  __shared__ float vconv[CONV ? V : 1];
+  if (CONV) {
+    // Every warp needs the whole q and k (they differ only in state rows), and a
+    // q/k channel is also read by the other value heads of its group: all
+    // convolve from the old state first; after the barrier, warp 0 of the
+    // group's first value head writes the new q/k state. Each v channel has one
+    // owning thread, which reads and writes it.
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      qv[i] = conv_silu(p, slot, b, C, h * K + col0 + i, false);
+      kv[i] = conv_silu(p, slot, b, C, p.H * K + h * K + col0 + i, false);
+    }
+    for (int r = threadIdx.x; r < V; r += kDecodeThreads) vconv[r] = conv_silu(p, slot, b, C, 2 * p.H * K + hv * V + r, true);
+    __syncthreads();
+    if (warp == 0 && hv % (p.HV / p.H) == 0) {
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
+        conv_shift(p, slot, b, C, h * K + col0 + i);
+        conv_shift(p, slot, b, C, p.H * K + h * K + col0 + i);
+      }
+    }
+  } else {
+    load_bf16<CPL>(row + h * K + col0, qv);
+    load_bf16<CPL>(row + p.H * K + h * K + col0, kv);
+  }
   load_bf16<CPL>(reinterpret_cast<const __nv_bfloat16*>(p.a) + static_cast<size_t>(b) * p.HV * K + hv * K + col0, av);
   const __nv_bfloat16* vrow = row + 2 * p.H * K + hv * V;
 
@@ -126,7 +189,7 @@ __global__ void __launch_bounds__(kDecodeThreads) kda_decode_kernel(const Decode
       for (int r = 0; r < kRowGroup; ++r)
         nxt[r] = __ldcs(reinterpret_cast<const Vec*>(S + static_cast<size_t>(rbase + kRowGroup + r) * K + col0));
     }
-    const float vr = __bfloat162float(vrow[rbase + rj]);
+    const float vr = CONV ? vconv[rbase + rj] : __bfloat162float(vrow[rbase + rj]);
 
     float sd[kRowGroup][CPL];
     float red[16];
@@ -169,7 +232,8 @@ __global__ void __launch_bounds__(kDecodeThreads) kda_decode_kernel(const Decode
 template <int K, int V>
 cudaError_t launch_decode_t(const DecodeCall& c, cudaStream_t s) {
   const unsigned grid = static_cast<unsigned>(c.B) * static_cast<unsigned>(c.HV);
-  kda_decode_kernel<K, V><<<grid, kDecodeThreads, 0, s>>>(c);
+  if (c.conv_in != nullptr) kda_decode_kernel<K, V, true><<<grid, kDecodeThreads, 0, s>>>(c);
+  else kda_decode_kernel<K, V, false><<<grid, kDecodeThreads, 0, s>>>(c);
   return cudaGetLastError();
 }
 

@@ -56,6 +56,12 @@ struct DecodeCall {
   const int32_t* indices;
   void* o;
   int32_t* err;
+  // causal conv1d + SiLU in front (conv_in == nullptr: packed_qkv is q|k|v already)
+  int conv_W;
+  const void* conv_in;
+  void* conv_out;
+  const float* conv_w;
+  const float* conv_b;
 };
 
 // Workspace layout: [plan header | records]. The header holds N + 2 int32.

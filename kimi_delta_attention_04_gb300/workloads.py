@@ -133,6 +133,21 @@ def decode_workload(*, seed=4, B=256, H=32, HV=32, K=128, V=128, num_slots=512,
                 scale=(1.0 / math.sqrt(K)) if scale is None else float(scale))
 
 
+def decode_conv_workload(*, seed=6, W=4, bias=True, **kw):
+    """A decode workload (decode_workload with the same arguments, drawn first)
+    plus the conv in front of it: conv state bf16 [num_slots, W-1, C] ~ N(0,1),
+    conv weight fp32 [C, W] ~ N(0, 1/W), conv bias fp32 [C] ~ N(0, 0.1^2) (or
+    None), C = 2*H*K + HV*V; the packed row is then the conv input."""
+    out = decode_workload(seed=seed, **kw)
+    gen = _gen(seed + 1000)
+    C = out["packed_qkv"].shape[1]
+    out["conv_state"] = _randn(gen, (out["num_slots"], W - 1, C), torch.bfloat16)
+    out["conv_weight"] = _randn(gen, (C, W), torch.float32, 1.0 / math.sqrt(W))
+    out["conv_bias"] = _randn(gen, (C,), torch.float32, 0.1) if bias else None
+    out["W"] = W
+    return out
+
+
 def recurrent_workload(*, seed=5, B=64, T=8, H=32, HV=32, K=128, V=128, num_slots=128,
                        pad_frac=0.1, state_std=0.1, scale=None):
     """Inputs of one short-T recurrent step (T tokens per row on a slot pool).

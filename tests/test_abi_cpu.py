@@ -52,6 +52,7 @@ def test_struct_layout_matches_c(tmp_path):
     fields_d = [f for f, _ in _lib.DecodeArgs._fields_]
     fields_r = [f for f, _ in _lib.RecurrentArgs._fields_]
     fields_n = [f for f, _ in _lib.RmsNormArgs._fields_]
+    fields_c2 = [f for f, _ in _lib.DecodeConvArgs._fields_]
     lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void){"]
     lines.append('printf("chunk %zu\\n", sizeof(kda_chunk_args));')
     for f in fields_c:
@@ -64,6 +65,9 @@ def test_struct_layout_matches_c(tmp_path):
         lines.append(f'printf("r.{f} %zu\\n", offsetof(kda_recurrent_args, {f}));')
     lines.append('printf("maxT %d\\n", KDA_RECURRENT_MAX_T);')
     lines.append('printf("rmsnorm %zu\\n", sizeof(kda_rmsnorm_args));')
+    lines.append('printf("dconv %zu\\n", sizeof(kda_decode_conv_args));')
+    for f in fields_c2:
+        lines.append(f'printf("dc.{f} %zu\\n", offsetof(kda_decode_conv_args, {f}));')
     for f in fields_n:
         lines.append(f'printf("n.{f} %zu\\n", offsetof(kda_rmsnorm_args, {f}));')
     lines.append("return 0;}")
@@ -83,6 +87,9 @@ def test_struct_layout_matches_c(tmp_path):
         assert int(got[f"r.{f}"]) == getattr(_lib.RecurrentArgs, f).offset, f
     assert int(got["maxT"]) == _lib.KDA_RECURRENT_MAX_T
     assert int(got["rmsnorm"]) == ctypes.sizeof(_lib.RmsNormArgs)
+    assert int(got["dconv"]) == ctypes.sizeof(_lib.DecodeConvArgs)
+    for f in fields_c2:
+        assert int(got[f"dc.{f}"]) == getattr(_lib.DecodeConvArgs, f).offset, f
     for f in fields_n:
         assert int(got[f"n.{f}"]) == getattr(_lib.RmsNormArgs, f).offset, f
 
@@ -217,6 +224,23 @@ def test_recurrent_validation_rejects(lib, over, status):
     a = _rec(**over)
     assert lib.kda_recurrent_step(ctypes.byref(a), None) == status
     assert lib.kda_recurrent_step(None, None) == _lib.KDA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(W=1), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(W=5), _lib.KDA_ERR_UNSUPPORTED),
+    (dict(conv_state_in=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(conv_weight=None), _lib.KDA_ERR_INVALID_ARG),
+    (dict(conv_state_out=FAKE), _lib.KDA_ERR_INVALID_ARG),       # in place with HV = 2H races
+    (dict(conv_bias=FAKE + 2), _lib.KDA_ERR_INVALID_ARG),        # misaligned
+])
+def test_decode_conv_validation_rejects(lib, over, status):
+    a = _lib.DecodeConvArgs()
+    a.dec = _dec()                  # H = 2, HV = 4
+    a.W, a.conv_state_in, a.conv_state_out, a.conv_weight, a.conv_bias = 4, FAKE, FAKE + 0x1000, FAKE, None
+    for k, v in over.items():
+        setattr(a, k, v)
+    assert lib.kda_decode_conv_step(ctypes.byref(a), None) == status
 
 
 @pytest.mark.parametrize("over,status", [

@@ -196,6 +196,26 @@ def kda_forward(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None,
     return o, hT
 
 
+def chunk_start_states(q, k, v, g, beta, scale, C, h0=None, delta=True):
+    """The state entering every C-token chunk of ONE sequence (stored layout
+    [n_chunks, H, V, K]): snapshot 0 is h0, snapshot c the state after tokens
+    0 .. cC-1. These are the per-chunk states a chunk-parallel output pass
+    needs (the materialised h of [TL] §6 / [LA] §3.3's chunkwise form: inter-chunk
+    recurrence first, then every chunk's output from its entering state)."""
+    T = np.asarray(q).shape[0]
+    H, K = np.asarray(q).shape[1:]
+    V = np.asarray(v).shape[-1]
+    n = (T + C - 1) // C
+    out = np.zeros((n, H, V, K))
+    state = np.zeros((H, V, K)) if h0 is None else np.asarray(h0, np.float64)
+    for c in range(n):
+        out[c] = state
+        s, e = c * C, min(T, (c + 1) * C)
+        _, state = kda_recurrent(q[s:e], k[s:e], v[s:e], g[s:e], beta[s:e] if beta is not None else None,
+                                 scale, h0=state, delta=delta)
+    return out
+
+
 # ----------------------------------------------------------------------------
 # Chunked form: L, Mqk, exact inverse ([FKDA]; [TL] §2; [LA] §3.3)
 # ----------------------------------------------------------------------------

@@ -505,6 +505,23 @@ def pin_decode_conv_state_and_pads():
     np.testing.assert_allclose(o, o2, rtol=1e-13, atol=1e-14)
 
 
+def pin_chunk_start_states():
+    """Snapshot 0 is h0; running each chunk alone from its snapshot reproduces
+    that chunk's outputs of the whole-sequence run and lands on the next
+    snapshot (the last one leads to hT): outputs are chunk-parallel given the
+    snapshots."""
+    q, k, v, g, b, h0 = _rand_case(22, T=37, H=2, K=4, V=3)
+    o, hT = ko.kda_recurrent(q, k, v, g, b, 0.6, h0=h0)
+    snaps = ko.chunk_start_states(q, k, v, g, b, 0.6, 16, h0=h0)
+    assert snaps.shape == (3, 2, 3, 4)
+    np.testing.assert_array_equal(snaps[0], h0)
+    for c in range(3):
+        s, e = 16 * c, min(37, 16 * (c + 1))
+        oc, hc = ko.kda_recurrent(q[s:e], k[s:e], v[s:e], g[s:e], b[s:e], 0.6, h0=snaps[c])
+        assert _rel(oc, o[s:e]) < 1e-12
+        assert _rel(hc, snaps[c + 1] if c < 2 else hT) < 1e-12
+
+
 PINS = [
     pin_hand_worked_chunk, pin_level1_quadratic_form, pin_level1_chunk_identity,
     pin_gla_parallel_form, pin_retnet_scalar_decay, pin_chunked_equals_recurrent,
@@ -513,6 +530,7 @@ PINS = [
     pin_decode_golden, pin_decode_head_grouping, pin_split_sequence, pin_value_split_invariance,
     pin_recurrent_pool_is_repeated_decode, pin_recurrent_pool_tokens_matter, pin_head_gate_semiseparable,
     pin_head_rmsnorm, pin_conv1d_update_is_causal_convolution, pin_decode_conv_state_and_pads,
+    pin_chunk_start_states,
 ]
 
 
@@ -653,6 +671,13 @@ def _silu_plain_sigmoid(x):
 
 ko_conv_orig = ko.causal_conv1d_update
 _orig_decode_conv = ko.kda_decode_conv
+_orig_chunk_start_states = ko.chunk_start_states
+
+
+def _cs_after_not_before(q, k, v, g, beta, scale, C, h0=None, delta=True):
+    snaps = _orig_chunk_start_states(q, k, v, g, beta, scale, C, h0=h0, delta=delta)
+    _, hT = ko.kda_recurrent(q, k, v, g, beta, scale, h0=h0, delta=delta)
+    return np.concatenate([snaps[1:], hT[None]], axis=0)
 
 
 def _dc_conv_on_pads(mixed_qkv, conv_state, conv_weight, conv_bias, *args, **kw):
@@ -751,6 +776,7 @@ MUTANTS = [
     ("silu", _silu_plain_sigmoid),
     ("kda_decode_conv", _dc_conv_on_pads),
     ("kda_decode_conv", _dc_no_activation),
+    ("chunk_start_states", _cs_after_not_before),
 ]
 
 

@@ -436,6 +436,49 @@ def run_gpu(args):
                "roofline": {"bound": "hbm", "achieved": rbytes / r_avg / 1e9, "unit": "GB/s",
                             "algorithmic_bytes": rbytes, "kernel": "kda_recurrent_kernel"}}
 
+    # --- per-chunk entering states, then the chunk-parallel output pass (own timed regions) ---
+    cst = None
+    if args.only == "all":
+        nc = kda.chunk_count(1, T)
+        hc = torch.empty(nc, PREFILL_H, D, D, dtype=torch.float32, device=dev)
+        o_par = torch.empty_like(o)
+        sargs = kda.make_chunk_args(d["q"], d["k"], d["v"], scale=d["scale"], a=d["a"], dt_bias=d["dt_bias"],
+                                    A_log=d["A_log"], b=d["b"], h0=d["h0"], l2norm_qk=True, o=o, hT=hT, h_chunks=hc)
+        sws = torch.empty(kda.chunk_workspace_size(sargs), dtype=torch.uint8, device=dev)
+
+        def snap_step():
+            kda.kda_chunk_fwd(d["q"], d["k"], d["v"], scale=d["scale"], a=d["a"], dt_bias=d["dt_bias"],
+                              A_log=d["A_log"], b=d["b"], h0=d["h0"], l2norm_qk=True, o=o, hT=hT, workspace=sws,
+                              h_chunks=hc, stream=stream)
+
+        def par_step():
+            kda.kda_chunk_output(d["q"], d["k"], d["v"], hc, scale=d["scale"], a=d["a"], dt_bias=d["dt_bias"],
+                                 A_log=d["A_log"], b=d["b"], l2norm_qk=True, o=o_par, workspace=sws, stream=stream)
+
+        def timed(fn):
+            for _ in range(args.warmup):
+                fn()
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            s0.record(stream)
+            for _ in range(K):
+                fn()
+            s1.record(stream)
+            torch.cuda.synchronize(dev)
+            return s0.elapsed_time(s1) / 1000.0 / K
+        t_snap = timed(snap_step)
+        t_par = timed(par_step)
+        hc_bytes = hc.numel() * 4
+        snap_bytes = prefill_algorithmic_bytes(T) + hc_bytes
+        par_bytes = T * BYTES_PER_TOKEN + PARAM_BYTES + hc_bytes
+        cst = {"chunks": nc, "h_chunks_bytes": hc_bytes,
+               "fwd_with_states": {"ms": 1000.0 * t_snap, "algorithmic_bytes": snap_bytes,
+                                   "achieved_gbs": snap_bytes / t_snap / 1e9,
+                                   "kernels": "kda_prep_tc_kernel + kda_recur_tc_kernel (serial, writes h_chunks)"},
+               "output_pass": {"ms": 1000.0 * t_par, "algorithmic_bytes": par_bytes,
+                               "achieved_gbs": par_bytes / t_par / 1e9,
+                               "kernels": "kda_prep_tc_kernel + kda_recur_tc_kernel (one CTA per chunk, reads h_chunks)"}}
+
     # --- reduce over ranks: max time ---
     t_chunk = sum(chunk_ms) / 1000.0
     t_dec = sum(dec_ms) / 1000.0
@@ -475,6 +518,7 @@ def run_gpu(args):
             "head_rmsnorm": rms,
             "decode_conv": dconv,
             "recurrent": rec,
+            "chunk_states": cst,
             "decode": {"us_per_step": 1e6 * dec_avg, "n_valid_rows": n_valid,
                        "roofline": {"bound": "hbm", "achieved": dach, "peak": hbm, "unit": "GB/s",
                                     "frac": dach / hbm, "algorithmic_bytes": dbytes,
@@ -494,6 +538,9 @@ def run_gpu(args):
             rms["frac_of_hbm"] = rms["achieved_gbs"] / hbm
         if dconv is not None:
             dconv["frac_of_hbm"] = dconv["achieved_gbs"] / hbm
+        if cst is not None:
+            for part in ("fwd_with_states", "output_pass"):
+                cst[part]["frac_of_hbm"] = cst[part]["achieved_gbs"] / hbm
         if rec is not None:
             rec["roofline"]["peak"] = hbm
             rec["roofline"]["frac"] = rec["roofline"]["achieved"] / hbm

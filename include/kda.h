@@ -4,6 +4,7 @@
  * Operations
  *   kda_chunk_fwd             chunkwise KDA forward over one batch of sequences
  *   kda_chunk_workspace_size  scratch bytes kda_chunk_fwd needs for given arguments
+ *   kda_chunk_output          chunk-parallel output pass from per-chunk entering states
  *   kda_decode_step           fused T=1 decode step on a packed q|k|v row with a slot pool
  *   kda_decode_conv_step      the decode step with its causal conv1d + SiLU fused in front
  *   kda_recurrent_step        T tokens per row (T <= 64) on a slot pool: speculative / extend steps
@@ -130,7 +131,20 @@ typedef struct kda_chunk_args {
   void* o;
   float* hT;
   int32_t* err;        /* optional device status word */
+  float* h_chunks;     /* optional per-chunk entering states (see below), or NULL */
 } kda_chunk_args;
+
+/*
+ * Per-chunk entering states (h_chunks). When non-NULL, kda_chunk_fwd also
+ * writes the state entering every 16-token chunk: fp32 [C_total, H, dv, dk],
+ * chunk by chunk in sequence order (uniform batches: B * ceil(T/16) entries,
+ * chunk c of sequence n at n * ceil(T/16) + c; with cu_seqlens: the sum over
+ * sequences of ceil(len/16), each sequence's chunks after the previous
+ * sequence's). Entry 0 of a sequence is its h0 (or zeros). These are the
+ * materialised states of the chunkwise form that a chunk-parallel output pass
+ * (kda_chunk_output) and a backward pass start from. bf16 only; the call then
+ * runs the two-kernel path (workspace as kda_chunk_workspace_size reports).
+ */
 
 /*
  * Bytes of device scratch memory kda_chunk_fwd needs for these arguments
@@ -149,6 +163,17 @@ size_t kda_chunk_workspace_size(const kda_chunk_args* args);
  */
 kda_status kda_chunk_fwd(const kda_chunk_args* args, void* workspace, size_t workspace_bytes,
                          kda_stream_t stream);
+
+/*
+ * Chunk-parallel output pass: o from the inputs and the per-chunk entering
+ * states args->h_chunks (read, as kda_chunk_fwd writes them). Every chunk's
+ * output o_c = q_dec,c S_c + Mqk_c U_c, U_c = U~_c - W_c S_c, is formed
+ * independently of the others (the serial dependence lives in the states).
+ * Same arguments, workspace and layouts as kda_chunk_fwd; h0 and hT are
+ * ignored; bf16 only, h_chunks required (KDA_ERR_INVALID_ARG otherwise).
+ */
+kda_status kda_chunk_output(const kda_chunk_args* args, void* workspace, size_t workspace_bytes,
+                            kda_stream_t stream);
 
 /*
  * Arguments of kda_decode_step (sglang PR #26586, fused_recurrent_kda_packed_decode:

@@ -9,8 +9,10 @@ library has not been built (python -m kimi_delta_attention_04_gb300.build).
 
 from ._lib import (  # noqa: F401
     KdaError,
+    chunk_count,
     chunk_workspace_size,
     kda_chunk_fwd,
+    kda_chunk_output,
     kda_chunk_fwd_noalloc,
     kda_decode_conv_step,
     kda_decode_step,

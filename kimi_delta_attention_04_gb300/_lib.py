@@ -52,6 +52,7 @@ class ChunkArgs(ctypes.Structure):
         ("a", ctypes.c_void_p), ("A_log", ctypes.c_void_p), ("dt_bias", ctypes.c_void_p),
         ("beta", ctypes.c_void_p), ("h0", ctypes.c_void_p), ("cu_seqlens", ctypes.c_void_p),
         ("o", ctypes.c_void_p), ("hT", ctypes.c_void_p), ("err", ctypes.c_void_p),
+        ("h_chunks", ctypes.c_void_p),
     ]
 
 
@@ -95,7 +96,7 @@ class RmsNormArgs(ctypes.Structure):
     ]
 
 
-EXPORTS = ("kda_chunk_fwd", "kda_chunk_fwd_noalloc", "kda_chunk_workspace_size", "kda_decode_step",
+EXPORTS = ("kda_chunk_fwd", "kda_chunk_output", "kda_chunk_fwd_noalloc", "kda_chunk_workspace_size", "kda_decode_step",
            "kda_decode_conv_step", "kda_recurrent_step", "kda_head_rmsnorm", "kda_version")
 
 
@@ -116,6 +117,8 @@ def load() -> ctypes.CDLL:
         lib = ctypes.CDLL(str(_LIB_PATH))
         lib.kda_chunk_fwd.restype = ctypes.c_int
         lib.kda_chunk_fwd.argtypes = [ctypes.POINTER(ChunkArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        lib.kda_chunk_output.restype = ctypes.c_int
+        lib.kda_chunk_output.argtypes = [ctypes.POINTER(ChunkArgs), ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
         lib.kda_chunk_workspace_size.restype = ctypes.c_size_t
         lib.kda_chunk_workspace_size.argtypes = [ctypes.POINTER(ChunkArgs)]
         lib.kda_decode_step.restype = ctypes.c_int
@@ -165,7 +168,8 @@ def _dtype_code(dt: torch.dtype) -> int:
 
 
 def make_chunk_args(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None, beta=None, b=None,
-                    h0=None, cu_seqlens=None, l2norm_qk=False, delta=True, o=None, hT=None, err=None, g_head=None):
+                    h0=None, cu_seqlens=None, l2norm_qk=False, delta=True, o=None, hT=None, err=None, g_head=None,
+                    h_chunks=None):
     """Fill the C argument struct from tensors (no allocation, no launch)."""
     B, T, H, dk = q.shape
     dv = v.shape[-1]
@@ -196,6 +200,7 @@ def make_chunk_args(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None,
     args.beta = _ptr(beta_t)
     args.h0, args.cu_seqlens = _ptr(h0), _ptr(cu_seqlens)
     args.o, args.hT, args.err = _ptr(o), _ptr(hT), _ptr(err)
+    args.h_chunks = _ptr(h_chunks)
     return args
 
 
@@ -205,7 +210,7 @@ def chunk_workspace_size(args: ChunkArgs) -> int:
 
 def kda_chunk_fwd(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None, beta=None, b=None,
                   h0=None, cu_seqlens=None, l2norm_qk=False, delta=True, o=None, hT=None,
-                  output_final_state=True, workspace=None, err=None, stream=None, g_head=None):
+                  output_final_state=True, workspace=None, err=None, stream=None, g_head=None, h_chunks=None):
     """Chunkwise KDA forward through libkda (see include/kda.h for the contract).
 
     q, k [B, T, H, dk]; v [B, T, H, dv] (bf16 or fp32, same dtype). The gate is
@@ -213,6 +218,8 @@ def kda_chunk_fwd(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None, b
     (fp32 [H*dk]) + A_log (fp32 [H]), or the Gated DeltaNet per-head gate g_head
     (fp32 [B, T, H]), or none (g = 0). beta [B, T, H] is given
     as values (beta=) or logits (b=). h0 / returned hT are fp32 [N, H, dv, dk].
+    h_chunks (fp32 [chunk_count(...), H, dv, dk], bf16 only) receives the state
+    entering every 16-token chunk when given.
     Returns (o, hT) with hT None when output_final_state is False.
     """
     lib = load()
@@ -224,7 +231,7 @@ def kda_chunk_fwd(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None, b
         hT = torch.empty(N, H, v.shape[-1], q.shape[-1], dtype=torch.float32, device=q.device)
     args = make_chunk_args(q, k, v, scale=scale, g=g, a=a, dt_bias=dt_bias, A_log=A_log, beta=beta, b=b,
                            h0=h0, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk, delta=delta, o=o, hT=hT,
-                           err=err, g_head=g_head)
+                           err=err, g_head=g_head, h_chunks=h_chunks)
     need = int(lib.kda_chunk_workspace_size(ctypes.byref(args)))
     if need == 0:
         st = lib.kda_chunk_fwd(ctypes.byref(args), None, 0, _stream_ptr(stream))
@@ -239,7 +246,7 @@ def kda_chunk_fwd(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None, b
 
 def kda_chunk_fwd_noalloc(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None, beta=None, b=None,
                           h0=None, cu_seqlens=None, l2norm_qk=False, delta=True, o=None, hT=None,
-                          output_final_state=True, err=None, stream=None, g_head=None):
+                          output_final_state=True, err=None, stream=None, g_head=None, h_chunks=None):
     """kda_chunk_fwd on the library's own scratch buffer: the C call allocates
     nothing (for callers that may not allocate device memory; see
     include/kda.h). Outputs o / hT are allocated here with torch unless given.
@@ -254,7 +261,7 @@ def kda_chunk_fwd_noalloc(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log
         hT = torch.empty(N, H, v.shape[-1], q.shape[-1], dtype=torch.float32, device=q.device)
     args = make_chunk_args(q, k, v, scale=scale, g=g, a=a, dt_bias=dt_bias, A_log=A_log, beta=beta, b=b,
                            h0=h0, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk, delta=delta, o=o, hT=hT,
-                           err=err, g_head=g_head)
+                           err=err, g_head=g_head, h_chunks=h_chunks)
     st = lib.kda_chunk_fwd_noalloc(ctypes.byref(args), _stream_ptr(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_chunk_fwd_noalloc")
@@ -358,4 +365,36 @@ def kda_decode_conv_step(mixed_qkv, conv_state_in, conv_weight, conv_bias, a, b,
     st = lib.kda_decode_conv_step(ctypes.byref(args), _stream_ptr(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_decode_conv_step")
+    return o
+
+
+def chunk_count(B, T, cu_seqlens=None):
+    """Number of 16-token chunks of a call: the first dimension of h_chunks."""
+    if cu_seqlens is None:
+        return B * ((T + 15) // 16)
+    cu = cu_seqlens.detach().to("cpu").tolist()
+    return sum((cu[i + 1] - cu[i] + 15) // 16 for i in range(len(cu) - 1))
+
+
+def kda_chunk_output(q, k, v, h_chunks, *, scale, g=None, a=None, dt_bias=None, A_log=None, beta=None, b=None,
+                     cu_seqlens=None, l2norm_qk=False, delta=True, o=None, workspace=None, err=None, stream=None,
+                     g_head=None):
+    """Chunk-parallel output pass: o from the inputs and the per-chunk entering
+    states h_chunks that kda_chunk_fwd(h_chunks=...) wrote. Returns o."""
+    lib = load()
+    B, T, H, _ = q.shape
+    if o is None:
+        o = torch.empty(B, T, H, v.shape[-1], dtype=q.dtype, device=q.device)
+    args = make_chunk_args(q, k, v, scale=scale, g=g, a=a, dt_bias=dt_bias, A_log=A_log, beta=beta, b=b,
+                           cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk, delta=delta, o=o, err=err, g_head=g_head,
+                           h_chunks=h_chunks)
+    need = int(lib.kda_chunk_workspace_size(ctypes.byref(args)))
+    if need == 0:
+        st = lib.kda_chunk_output(ctypes.byref(args), None, 0, _stream_ptr(stream))
+        raise KdaError(st if st != KDA_OK else KDA_ERR_INVALID_ARG, "kda_chunk_output")
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = lib.kda_chunk_output(ctypes.byref(args), ctypes.c_void_p(_ptr(workspace)), need, _stream_ptr(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_chunk_output")
     return o

@@ -17,8 +17,11 @@ bool chunk_dims_supported(const kda_chunk_args& a) {
 }
 
 // bf16 with dk = dv = 128 runs the fused cluster kernel (prep and recurrence in
-// one launch); other shapes run the two-kernel path through workspace records.
-bool uses_fused(const kda_chunk_args& a) { return a.dtype == KDA_DTYPE_BF16 && a.dk == 128 && a.dv == 128; }
+// one launch); other shapes, and calls that want per-chunk states, run the
+// two-kernel path through workspace records.
+bool uses_fused(const kda_chunk_args& a) {
+  return a.dtype == KDA_DTYPE_BF16 && a.dk == 128 && a.dv == 128 && a.h_chunks == nullptr;
+}
 
 // Returns KDA_OK and fills geometry when the arguments are well formed.
 kda_status check_chunk(const kda_chunk_args* a, kda::ChunkGeom* geo, size_t* rec_bytes) {
@@ -39,6 +42,10 @@ kda_status check_chunk(const kda_chunk_args* a, kda::ChunkGeom* geo, size_t* rec
   if (tokens * a->H * (a->dk > a->dv ? a->dk : a->dv) > INT64_C(1) << 40) return KDA_ERR_INVALID_ARG;
   if (tokens > INT32_MAX / 2) return KDA_ERR_INVALID_ARG;
   if (!chunk_dims_supported(*a)) return KDA_ERR_UNSUPPORTED;
+  if (a->h_chunks != nullptr) {  // per-chunk states: the bf16 two-kernel path only
+    if (a->dtype != KDA_DTYPE_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!aligned(a->h_chunks, 16)) return KDA_ERR_INVALID_ARG;
+  }
   if (tokens > 0) {
     if (!a->q || !a->k || !a->v || !a->o) return KDA_ERR_INVALID_ARG;
     if (!aligned(a->q, 16) || !aligned(a->k, 16) || !aligned(a->v, 16) || !aligned(a->o, 16)) return KDA_ERR_INVALID_ARG;
@@ -93,11 +100,15 @@ size_t kda_chunk_workspace_size(const kda_chunk_args* args) {
   return workspace_bytes(*args, geo, rec);
 }
 
-kda_status kda_chunk_fwd(const kda_chunk_args* args, void* workspace, size_t ws_bytes, kda_stream_t stream) {
+namespace {
+
+kda_status run_chunk(const kda_chunk_args* args, void* workspace, size_t ws_bytes, kda_stream_t stream,
+                     bool output_pass) {
   kda::ChunkGeom geo;
   size_t rec = 0;
   kda_status st = check_chunk(args, &geo, &rec);
   if (st != KDA_OK) return st;
+  if (output_pass && args->h_chunks == nullptr) return KDA_ERR_INVALID_ARG;
   const size_t need = workspace_bytes(*args, geo, rec);
   if (workspace == nullptr || ws_bytes < need || !aligned(workspace, 256)) return KDA_ERR_INVALID_ARG;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -125,14 +136,26 @@ kda_status kda_chunk_fwd(const kda_chunk_args* args, void* workspace, size_t ws_
   c.hT = args->hT;
   c.err = args->err;
   c.records = static_cast<unsigned char*>(workspace) + kda::plan_header_bytes(geo.N);
+  c.h_chunks = args->h_chunks;
 
   cudaError_t e = cudaSuccess;
   if (geo.cu_seqlens != nullptr) e = kda::launch_plan(c, s);
   if (e == cudaSuccess) {
-    if (uses_fused(*args)) e = kda::launch_chunk_fused(c, s);
+    if (output_pass) e = kda::launch_chunk_output_tc(c, s);
+    else if (uses_fused(*args)) e = kda::launch_chunk_fused(c, s);
     else e = args->dtype == KDA_DTYPE_BF16 ? kda::launch_chunk_tc(c, s) : kda::launch_chunk_f32(c, s);
   }
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+}  // namespace
+
+kda_status kda_chunk_fwd(const kda_chunk_args* args, void* workspace, size_t ws_bytes, kda_stream_t stream) {
+  return run_chunk(args, workspace, ws_bytes, stream, false);
+}
+
+kda_status kda_chunk_output(const kda_chunk_args* args, void* workspace, size_t ws_bytes, kda_stream_t stream) {
+  return run_chunk(args, workspace, ws_bytes, stream, true);
 }
 
 namespace {

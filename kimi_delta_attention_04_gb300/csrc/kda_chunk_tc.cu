@@ -391,7 +391,12 @@ struct RecSmem {
   __align__(16) __nv_bfloat16 ostage[16][16 * WARPS + 8];
 };
 
-template <int D, int WARPS, bool DELTA>
+// PAR = false: the serial chunk recurrence of one (sequence, head, value block),
+// writing the state entering every chunk to p.h_chunks when it is given.
+// PAR = true: the chunk-parallel output pass: one CTA per (global chunk, head,
+// value block) starts from that chunk's entering state in p.h_chunks and forms
+// only the chunk's output (the state update is the serial pass's business).
+template <int D, int WARPS, bool DELTA, bool PAR>
 __global__ void __launch_bounds__(WARPS * 32) kda_recur_tc_kernel(const ChunkCall p) {
   using ST2 = std::conditional_t<DELTA, F16, Bf16>;
   using S2 = typename ST2::T;
@@ -403,19 +408,28 @@ __global__ void __launch_bounds__(WARPS * 32) kda_recur_tc_kernel(const ChunkCal
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
 
   const int H = p.geo.H;
-  const int n = blockIdx.x / H;
-  const int h = blockIdx.x - n * H;
+  const int unit = blockIdx.x / H;  // sequence, or global chunk (PAR)
+  const int h = blockIdx.x - unit * H;
   const int dv0 = blockIdx.y * 16 * WARPS;
+  int n = unit, c_begin = 0;
+  if (PAR) {
+    ChunkPos pos;
+    if (!locate_chunk(p.geo, unit, pos)) return;
+    n = pos.n;
+    c_begin = pos.c;
+  }
   int ts, te, cb;
   if (!locate_seq(p.geo, n, ts, te, cb)) return;
-  const int nch = (te - ts + kChunk - 1) / kChunk;
+  const int nch = PAR ? c_begin + 1 : (te - ts + kChunk - 1) / kChunk;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t = lane & 3;
   const int r0 = dv0 + warp * 16;  // first value row of this warp
 
   float S[NT][4];
-  if (p.h0 != nullptr) {
-    const float* src = p.h0 + (static_cast<size_t>(n) * H + h) * D * D;
+  const float* s_src = PAR ? p.h_chunks + (static_cast<size_t>(unit) * H + h) * D * D
+                           : (p.h0 != nullptr ? p.h0 + (static_cast<size_t>(n) * H + h) * D * D : nullptr);
+  if (s_src != nullptr) {
+    const float* src = s_src;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const float2 x = *reinterpret_cast<const float2*>(src + (r0 + g) * D + 8 * nt + 2 * t);
@@ -448,20 +462,29 @@ __global__ void __launch_bounds__(WARPS * 32) kda_recur_tc_kernel(const ChunkCal
     }
   };
 
-  if (nch > 0) {
-    load_stage(0, 0);
+  if (nch > c_begin) {
+    load_stage(c_begin, 0);
     cp_async_commit();
   }
-  for (int c = 0; c < nch; ++c) {
+  for (int c = c_begin; c < nch; ++c) {
+    const int it = c - c_begin;
     if (c + 1 < nch) {
-      load_stage(c + 1, (c + 1) & 1);
+      load_stage(c + 1, (it + 1) & 1);
       cp_async_commit();
       cp_async_wait<1>();
     } else {
       cp_async_wait<0>();
     }
     __syncthreads();
-    const RecStage<D, WARPS, S2>& st = sm.st[c & 1];
+    const RecStage<D, WARPS, S2>& st = sm.st[it & 1];
+    if (!PAR && p.h_chunks != nullptr) {  // the state entering chunk c
+      float* dst = p.h_chunks + (static_cast<size_t>(cb + c) * H + h) * D * D;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        *reinterpret_cast<float2*>(dst + (r0 + g) * D + 8 * nt + 2 * t) = make_float2(S[nt][0], S[nt][1]);
+        *reinterpret_cast<float2*>(dst + (r0 + g + 8) * D + 8 * nt + 2 * t) = make_float2(S[nt][2], S[nt][3]);
+      }
+    }
 
     // S^T as bf16 A fragments (accumulator layout == A layout for tile pairs)
     uint32_t sa[D / 16][4];
@@ -509,7 +532,7 @@ __global__ void __launch_bounds__(WARPS * 32) kda_recur_tc_kernel(const ChunkCal
 
     // stage 2a: S^T = S^T diag(gamma) + U^T k_res   (the serial dependency)
 #pragma unroll
-    for (int np = 0; np < D / 16; ++np) {
+    for (int np = 0; np < (PAR ? 0 : D / 16); ++np) {
       uint32_t b[4];
       ldsm_x4_trans(b, &st.kr[lane & 15][16 * np + (lane >> 4) * 8]);
 #pragma unroll
@@ -552,7 +575,7 @@ __global__ void __launch_bounds__(WARPS * 32) kda_recur_tc_kernel(const ChunkCal
     }
   }
 
-  if (p.hT != nullptr) {
+  if (!PAR && p.hT != nullptr) {
     float* dst = p.hT + (static_cast<size_t>(n) * H + h) * D * D;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -570,7 +593,7 @@ cudaError_t launch_prep_t(const ChunkCall& c, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int D, bool DELTA>
+template <int D, bool DELTA, bool PAR>
 cudaError_t launch_recur_t(const ChunkCall& c, cudaStream_t s) {
   constexpr int WARPS = 2;
   using ST2 = std::conditional_t<DELTA, F16, Bf16>;
@@ -578,27 +601,29 @@ cudaError_t launch_recur_t(const ChunkCall& c, cudaStream_t s) {
   const size_t smem = sizeof(Smem);
   static bool attr_set = false;  // per instantiation; the attribute is per device-function
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kda_recur_tc_kernel<D, WARPS, DELTA>,
+    cudaError_t e = cudaFuncSetAttribute(kda_recur_tc_kernel<D, WARPS, DELTA, PAR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(c.geo.N * c.geo.H, D / (16 * WARPS));
-  kda_recur_tc_kernel<D, WARPS, DELTA><<<grid, WARPS * 32, smem, s>>>(c);
+  const unsigned units = PAR ? static_cast<unsigned>(c.geo.max_chunks) : static_cast<unsigned>(c.geo.N);
+  if (units == 0) return cudaSuccess;
+  dim3 grid(units * c.geo.H, D / (16 * WARPS));
+  kda_recur_tc_kernel<D, WARPS, DELTA, PAR><<<grid, WARPS * 32, smem, s>>>(c);
   return cudaGetLastError();
 }
 
-template <int D>
+template <int D, bool PAR>
 cudaError_t launch_chunk_tc_d(const ChunkCall& c, cudaStream_t s) {
   cudaError_t e;
   if (c.delta) {
     e = c.l2norm ? launch_prep_t<D, true, true>(c, s) : launch_prep_t<D, true, false>(c, s);
     if (e != cudaSuccess) return e;
-    return launch_recur_t<D, true>(c, s);
+    return launch_recur_t<D, true, PAR>(c, s);
   }
   e = c.l2norm ? launch_prep_t<D, false, true>(c, s) : launch_prep_t<D, false, false>(c, s);
   if (e != cudaSuccess) return e;
-  return launch_recur_t<D, false>(c, s);
+  return launch_recur_t<D, false, PAR>(c, s);
 }
 
 }  // namespace
@@ -610,8 +635,15 @@ size_t record_bytes_tc(int d) {
 }
 
 cudaError_t launch_chunk_tc(const ChunkCall& c, cudaStream_t s) {
-  if (c.dk == 128) return launch_chunk_tc_d<128>(c, s);
-  if (c.dk == 64) return launch_chunk_tc_d<64>(c, s);
+  if (c.dk == 128) return launch_chunk_tc_d<128, false>(c, s);
+  if (c.dk == 64) return launch_chunk_tc_d<64, false>(c, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_chunk_output_tc(const ChunkCall& c, cudaStream_t s) {
+  if (c.h_chunks == nullptr) return cudaErrorInvalidValue;
+  if (c.dk == 128) return launch_chunk_tc_d<128, true>(c, s);
+  if (c.dk == 64) return launch_chunk_tc_d<64, true>(c, s);
   return cudaErrorInvalidValue;
 }
 

@@ -41,6 +41,8 @@ struct ChunkCall {
   int32_t* err;
   unsigned char* records;  // workspace after the plan header: per (chunk, head) prep records,
                            // or the fused kernel's pool of global rings
+  float* h_chunks;         // per-chunk entering states [chunks, H, dv, dk] (written, or read by the
+                           // chunk-parallel output pass), or nullptr
 };
 
 struct DecodeCall {
@@ -102,6 +104,7 @@ size_t record_bytes_f32(int dk, int dv);  // fp32 path
 
 cudaError_t launch_plan(const ChunkCall& c, cudaStream_t s);
 cudaError_t launch_chunk_tc(const ChunkCall& c, cudaStream_t s);
+cudaError_t launch_chunk_output_tc(const ChunkCall& c, cudaStream_t s);  // chunk-parallel o from h_chunks
 cudaError_t launch_chunk_f32(const ChunkCall& c, cudaStream_t s);
 cudaError_t launch_chunk_fused(const ChunkCall& c, cudaStream_t s);  // bf16, dk = dv = 128
 size_t fused_smem_bytes();

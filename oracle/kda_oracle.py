@@ -151,7 +151,7 @@ def _sequences(B, T, cu_seqlens):
 
 def kda_forward(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None,
                 beta=None, b=None, h0=None, cu_seqlens=None, l2norm_qk=False,
-                delta=True, chunk_size=None, g_head=None):
+                delta=True, chunk_size=None, g_head=None, chunk_states=False):
     """The chunk-forward operation as the C ABI exposes it, computed in fp64.
 
     q, k: [B, T, H, K]; v: [B, T, H, V]. The gate is given either as g
@@ -161,7 +161,9 @@ def kda_forward(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None,
     beta [B, T, H] is given directly or as logits b (beta = sigmoid(b)).
     h0: [N, H, V, K] or None. cu_seqlens: [N+1] over a single row (B == 1) or None.
     chunk_size None runs the token recurrence; an integer runs kda_chunked.
-    Returns (o [B, T, H, V], hT [N, H, V, K]).
+    Returns (o [B, T, H, V], hT [N, H, V, K]), and with chunk_states also the
+    states entering every 16-token chunk, sequence after sequence
+    ([sum_n ceil(len_n/16), H, V, K], chunk_start_states).
     """
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
@@ -186,6 +188,7 @@ def kda_forward(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None,
     seqs = _sequences(B, T, cu_seqlens)
     o = np.zeros((B, T, H, V))
     hT = np.zeros((len(seqs), H, V, K))
+    snaps = []
     for n, (row, s, e) in enumerate(seqs):
         h0n = None if h0 is None else np.asarray(h0, np.float64)[n]
         args = (q[row, s:e], k[row, s:e], v[row, s:e], g[row, s:e], beta[row, s:e], scale)
@@ -193,6 +196,10 @@ def kda_forward(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None,
             o[row, s:e], hT[n] = kda_recurrent(*args, h0=h0n, delta=delta)
         else:
             o[row, s:e], hT[n] = kda_chunked(*args, C=chunk_size, h0=h0n, delta=delta)
+        if chunk_states and e > s:
+            snaps.append(chunk_start_states(*args, C=16, h0=h0n, delta=delta))
+    if chunk_states:
+        return o, hT, (np.concatenate(snaps) if snaps else np.zeros((0, H, V, K)))
     return o, hT
 
 

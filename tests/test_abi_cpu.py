@@ -137,6 +137,9 @@ def test_workspace_size_formula(lib):
     f = _chunk(dtype=_lib.KDA_DTYPE_FP32, dk=64, dv=128)
     recf = 3 * 16 * 64 * 4 + 128 * 16 * 4 + 16 * 16 * 4 + 64 * 4
     assert _ws(lib, f) == 256 + 7 * 2 * recf
+    # per-chunk states take the two-kernel path at d=128 as well
+    rec128 = 3 * 16 * 128 * 2 + 128 * 16 * 4 + 16 * 16 * 2 + 128 * 4
+    assert _ws(lib, _chunk(h_chunks=FAKE)) == 256 + 7 * 2 * rec128
 
 
 @pytest.mark.parametrize("over,status", [
@@ -157,11 +160,22 @@ def test_workspace_size_formula(lib):
     (dict(dk=64, dv=128), _lib.KDA_ERR_UNSUPPORTED),           # bf16 path needs dk == dv
     (dict(gate_mode=_lib.KDA_GATE_INPUTS, a=FAKE, A_log=None, dt_bias=FAKE), _lib.KDA_ERR_INVALID_ARG),
     (dict(h0=FAKE + 8), _lib.KDA_ERR_INVALID_ARG),
+    (dict(h_chunks=FAKE + 8), _lib.KDA_ERR_INVALID_ARG),       # per-chunk states need 16-byte alignment
+    (dict(h_chunks=FAKE, dtype=_lib.KDA_DTYPE_FP32, dk=64, dv=64), _lib.KDA_ERR_UNSUPPORTED),  # bf16 only
 ])
 def test_chunk_validation_rejects(lib, over, status):
     a = _chunk(**over)
     assert _ws(lib, a) == 0
     assert _fwd(lib, a) == status
+    assert lib.kda_chunk_output(ctypes.byref(a), ctypes.c_void_p(FAKE), ctypes.c_size_t(1 << 40), None) == status
+
+
+def test_chunk_output_needs_states(lib):
+    """The chunk-parallel output pass reads h_chunks: without it the call is refused."""
+    a = _chunk()
+    assert lib.kda_chunk_output(ctypes.byref(a), ctypes.c_void_p(FAKE), ctypes.c_size_t(1 << 40), None) == \
+        _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_chunk_output(None, None, 0, None) == _lib.KDA_ERR_INVALID_ARG
 
 
 def test_chunk_workspace_checks(lib):

@@ -1,0 +1,55 @@
+"""Per-chunk entering states (h_chunks) written by kda_chunk_fwd and the
+chunk-parallel output pass kda_chunk_output, against the fp64 oracle through
+the C ABI: snapshots, o and hT within the bf16 tolerances (rel-Frobenius
+<= 5e-3, max-abs <= 2e-2)."""
+
+import pytest
+import torch
+
+import kimi_delta_attention_04_gb300 as kda
+from kimi_delta_attention_04_gb300 import workloads as W
+from oracle import kda_oracle as ko
+
+from kda_cases import assert_close, np64, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from kimi_delta_attention_04_gb300 import build
+    build.build()
+    kda.load()
+
+
+def _kw(d):
+    return dict(scale=d["scale"], g=d["g"], a=d["a"], dt_bias=d["dt_bias"], A_log=d["A_log"], beta=d["beta"],
+                b=d["b"], cu_seqlens=d["cu_seqlens"], l2norm_qk=d["l2norm"], delta=d["delta"], g_head=d.get("g_head"))
+
+
+@pytest.mark.parametrize("K,B,T,lengths,gate", [
+    (64, 2, 70, None, "inputs"),
+    (128, 1, 200, None, "inputs"),
+    (128, 1, 0, [40, 0, 130, 17], "inputs"),
+    (128, 2, 45, None, "head"),
+], ids=["d64", "d128", "d128_varlen", "d128_gdn"])
+def test_chunk_states_and_parallel_output(K, B, T, lengths, gate):
+    wl = W.chunk_workload(seed=140 + K + (T or 7), B=B, T=T or 1, H=3, K=K, V=K, lengths=lengths, gate=gate)
+    d = to_dev(wl)
+    nc = kda.chunk_count(wl["B"], wl["T"], wl["cu_seqlens"])
+    hc = torch.full((nc, wl["H"], K, K), float("nan"), dtype=torch.float32, device="cuda")
+    o, hT = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], h0=d["h0"], h_chunks=hc, **_kw(d))
+    torch.cuda.synchronize()
+    o_ref, h_ref, s_ref = ko.kda_forward(
+        np64(wl["q"]), np64(wl["k"]), np64(wl["v"]), scale=wl["scale"], g=np64(wl["g"]), a=np64(wl["a"]),
+        dt_bias=np64(wl["dt_bias"]), A_log=np64(wl["A_log"]), beta=np64(wl["beta"]), b=np64(wl["b"]),
+        h0=np64(wl["h0"]), cu_seqlens=None if wl["cu_seqlens"] is None else wl["cu_seqlens"].numpy(),
+        l2norm_qk=wl["l2norm"], delta=wl["delta"], g_head=np64(wl.get("g_head")), chunk_states=True)
+    assert s_ref.shape[0] == nc
+    assert_close("snapshots", np64(hc), s_ref, torch.bfloat16)
+    assert_close("o (snapshot path)", np64(o), o_ref, torch.bfloat16)
+    assert_close("hT (snapshot path)", np64(hT), h_ref, torch.bfloat16)
+    # every chunk's output again, in parallel, from its snapshot
+    o2 = kda.kda_chunk_output(d["q"], d["k"], d["v"], hc, **_kw(d))
+    torch.cuda.synchronize()
+    assert_close("o (chunk-parallel pass)", np64(o2), o_ref, torch.bfloat16)

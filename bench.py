@@ -474,10 +474,10 @@ def run_gpu(args):
         cst = {"chunks": nc, "h_chunks_bytes": hc_bytes,
                "fwd_with_states": {"ms": 1000.0 * t_snap, "algorithmic_bytes": snap_bytes,
                                    "achieved_gbs": snap_bytes / t_snap / 1e9,
-                                   "kernels": "kda_prep_tc_kernel + kda_recur_tc_kernel (serial, writes h_chunks)"},
+                                   "kernel": "kda_chunk_fused_kernel (its recurrence writes h_chunks)"},
                "output_pass": {"ms": 1000.0 * t_par, "algorithmic_bytes": par_bytes,
                                "achieved_gbs": par_bytes / t_par / 1e9,
-                               "kernels": "kda_prep_tc_kernel + kda_recur_tc_kernel (one CTA per chunk, reads h_chunks)"}}
+                               "kernel": "kda_chunk_fused_kernel, output-pass mode (state of each chunk read from h_chunks)"}}
 
     # --- reduce over ranks: max time ---
     t_chunk = sum(chunk_ms) / 1000.0

@@ -142,8 +142,9 @@ typedef struct kda_chunk_args {
  * sequences of ceil(len/16), each sequence's chunks after the previous
  * sequence's). Entry 0 of a sequence is its h0 (or zeros). These are the
  * materialised states of the chunkwise form that a chunk-parallel output pass
- * (kda_chunk_output) and a backward pass start from. bf16 only; the call then
- * runs the two-kernel path (workspace as kda_chunk_workspace_size reports).
+ * (kda_chunk_output) and a backward pass start from. bf16 only. With
+ * dk = dv = 128 the fused kernel writes them as it goes (streaming stores of
+ * the state its recurrence holds); d = 64 runs the two-kernel path.
  */
 
 /*
@@ -153,6 +154,8 @@ typedef struct kda_chunk_args {
  * dk = dv = 128 it is a fixed ~14 MB (a pool of L2-resident rings through
  * which the kernel hands prepared chunks between the CTAs of a cluster) plus a
  * small per-sequence header; other shapes need per-(chunk, head) records.
+ * kda_chunk_output needs the same scratch as kda_chunk_fwd for the same
+ * arguments.
  */
 size_t kda_chunk_workspace_size(const kda_chunk_args* args);
 

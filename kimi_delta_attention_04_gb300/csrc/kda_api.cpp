@@ -17,10 +17,11 @@ bool chunk_dims_supported(const kda_chunk_args& a) {
 }
 
 // bf16 with dk = dv = 128 runs the fused cluster kernel (prep and recurrence in
-// one launch); other shapes, and calls that want per-chunk states, run the
-// two-kernel path through workspace records.
+// one launch; it also writes per-chunk states when asked, and forms the
+// chunk-parallel output pass from them); other shapes run the two-kernel path
+// through workspace records.
 bool uses_fused(const kda_chunk_args& a) {
-  return a.dtype == KDA_DTYPE_BF16 && a.dk == 128 && a.dv == 128 && a.h_chunks == nullptr;
+  return a.dtype == KDA_DTYPE_BF16 && a.dk == 128 && a.dv == 128;
 }
 
 // Returns KDA_OK and fills geometry when the arguments are well formed.
@@ -75,15 +76,14 @@ kda_status check_chunk(const kda_chunk_args* a, kda::ChunkGeom* geo, size_t* rec
   } else {
     geo->max_chunks = geo->chunks_per_seq + a->N;  // each sequence adds at most one partial chunk
   }
-  if (uses_fused(*a)) {
-    *rec_bytes = 0;  // no per-chunk records: a fixed pool of rings instead
-    return KDA_OK;
-  }
   *rec_bytes = a->dtype == KDA_DTYPE_BF16 ? kda::record_bytes_tc(a->dk) : kda::record_bytes_f32(a->dk, a->dv);
   if (*rec_bytes == 0) return KDA_ERR_UNSUPPORTED;
   return KDA_OK;
 }
 
+// Scratch of a call (kda_chunk_fwd and kda_chunk_output alike): the fused
+// kernel's fixed pool of rings, or one record per (chunk, head) for the
+// two-kernel path.
 size_t workspace_bytes(const kda_chunk_args& a, const kda::ChunkGeom& geo, size_t rec_bytes) {
   if (uses_fused(a)) return kda::plan_header_bytes(geo.N) + kda::fused_workspace_bytes();
   return kda::plan_header_bytes(geo.N) + static_cast<size_t>(geo.max_chunks) * geo.H * rec_bytes;
@@ -137,12 +137,13 @@ kda_status run_chunk(const kda_chunk_args* args, void* workspace, size_t ws_byte
   c.err = args->err;
   c.records = static_cast<unsigned char*>(workspace) + kda::plan_header_bytes(geo.N);
   c.h_chunks = args->h_chunks;
+  c.output_pass = output_pass;
 
   cudaError_t e = cudaSuccess;
   if (geo.cu_seqlens != nullptr) e = kda::launch_plan(c, s);
   if (e == cudaSuccess) {
-    if (output_pass) e = kda::launch_chunk_output_tc(c, s);
-    else if (uses_fused(*args)) e = kda::launch_chunk_fused(c, s);
+    if (uses_fused(*args)) e = kda::launch_chunk_fused(c, s);
+    else if (output_pass) e = kda::launch_chunk_output_tc(c, s);
     else e = args->dtype == KDA_DTYPE_BF16 ? kda::launch_chunk_tc(c, s) : kda::launch_chunk_f32(c, s);
   }
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;

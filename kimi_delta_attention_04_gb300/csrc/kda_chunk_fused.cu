@@ -228,15 +228,21 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     const int g = lane >> 2, t = lane & 3;
     const int row0 = static_cast<int>(rank) * kRows + dvb * 16;  // first value row of this warp
     const int kc0 = dkh * 64;                                    // first key channel of this warp
+    // Output pass: no recurrence; S holds the next chunk's entering state,
+    // loaded from h_chunks one chunk ahead of its use.
+    const bool outp = p.output_pass;
     float S[8][4];
-    if (ok && p.h0 != nullptr) {
-      const float* src = p.h0 + (static_cast<size_t>(n) * H + h) * FD * FD;
+    auto load_state = [&](const float* src) {
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
-        const float2 x = *reinterpret_cast<const float2*>(src + (row0 + g) * FD + kc0 + 8 * nt + 2 * t);
-        const float2 y = *reinterpret_cast<const float2*>(src + (row0 + g + 8) * FD + kc0 + 8 * nt + 2 * t);
+        const float2 x = __ldcs(reinterpret_cast<const float2*>(src + (row0 + g) * FD + kc0 + 8 * nt + 2 * t));
+        const float2 y = __ldcs(reinterpret_cast<const float2*>(src + (row0 + g + 8) * FD + kc0 + 8 * nt + 2 * t));
         S[nt][0] = x.x; S[nt][1] = x.y; S[nt][2] = y.x; S[nt][3] = y.y;
       }
+    };
+    auto snapshot = [&](int cc) { return p.h_chunks + (static_cast<size_t>(cb + cc) * H + h) * FD * FD; };
+    if (outp ? nch > 0 : (ok && p.h0 != nullptr)) {
+      load_state(outp ? snapshot(0) : p.h0 + (static_cast<size_t>(n) * H + h) * FD * FD);
     } else {
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.f;
@@ -277,10 +283,31 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         sa[kk][3] = Bf16::pack(S[2 * kk + 1][2], S[2 * kk + 1][3]);
       }
     };
+    // this CTA's 32 value rows of chunk cc's state: one contiguous 16 KB slab, pulled
+    // into L2 kSnapAhead chunks before its loads
+    constexpr int kSnapAhead = 4;
+    auto prefetch_state = [&](int cc) {
+      if (warp == 0 && lane == 0 && cc < nch) bulk_prefetch_l2(snapshot(cc) + rank * kRows * FD, kRows * FD * 4);
+    };
     pack_state();
+    if (outp) {
+      for (int cc = 2; cc < 2 + kSnapAhead; ++cc) prefetch_state(cc);
+      if (nch > 1) load_state(snapshot(1));
+    }
+    float* const snap = (p.h_chunks == nullptr || outp)
+                            ? nullptr
+                            : p.h_chunks + (static_cast<size_t>(cb) * H + h) * FD * FD + (row0 + g) * FD + kc0 + 2 * t;
     for (int c = 0; c < nch; ++c) {
       const int s = c & (kRing - 1);
       const uint32_t par = static_cast<uint32_t>(c / kRing) & 1u;
+      if (snap != nullptr) {  // the state entering chunk c, before its decay (streaming stores)
+        float* dst = snap + static_cast<size_t>(c) * H * FD * FD;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          __stcs(reinterpret_cast<float2*>(dst + 8 * nt), make_float2(S[nt][0], S[nt][1]));
+          __stcs(reinterpret_cast<float2*>(dst + 8 * FD + 8 * nt), make_float2(S[nt][2], S[nt][3]));
+        }
+      }
       if (!failed && !mbar_wait_bounded(smem_u32(&sm.full[s]), par, kWaitLimitNs)) {
         failed = true;
         if (lane == 0) set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
@@ -316,8 +343,10 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       if (c > 0) post_output(c - 1);
       // operands of the state update, independent of U: loaded while U settles
       uint32_t krb[4][4];
+      if (!outp) {
 #pragma unroll
-      for (int np = 0; np < 4; ++np) ldsm_x4(krb[np], &st.kr[0][0] + cm_off(kc0 + 16 * np + nm_row, nm_half));
+        for (int np = 0; np < 4; ++np) ldsm_x4(krb[np], &st.kr[0][0] + cm_off(kc0 + 16 * np + nm_row, nm_half));
+      }
       // Exchange the two key halves' U^T partial sums (split-K).
       {
         float* mine = sm.rs.xch[c & 1][dvb][dkh][lane];
@@ -337,7 +366,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       ua[3] = ST2::pack(u[1][2], u[1][3]);
       // state update on this warp's key half: S^T = S^T diag(gamma) + U^T k_res
 #pragma unroll
-      for (int np = 0; np < 4; ++np) {
+      for (int np = 0; np < (outp ? 0 : 4); ++np) {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const int nt = 2 * np + half;
@@ -364,11 +393,15 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         mma16816<ST2>(o[1], ua, b[2], b[3]);
       }
       pack_state();
+      if (outp) {
+        if (c + 2 < nch) load_state(snapshot(c + 2));
+        prefetch_state(c + 2 + kSnapAhead);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive_local(&sm.empty[s]);
     }
     if (nch > 0) post_output(nch - 1);
-    if (ok && p.hT != nullptr) {
+    if (ok && p.hT != nullptr && !outp) {
       float* dst = p.hT + (static_cast<size_t>(n) * H + h) * FD * FD;
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {

@@ -177,6 +177,12 @@ __device__ __forceinline__ void bulk_load_g2s(void* smem, const void* gmem, uint
       : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (no completion to wait for); the
+// address and the size are multiples of 16 bytes.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* gmem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
+}
+
 // 32-bit load from the shared memory of another CTA of the cluster.
 __device__ __forceinline__ int ld_shared_cluster_s32(uint32_t cluster_addr) {
   int v;

@@ -43,6 +43,7 @@ struct ChunkCall {
                            // or the fused kernel's pool of global rings
   float* h_chunks;         // per-chunk entering states [chunks, H, dv, dk] (written, or read by the
                            // chunk-parallel output pass), or nullptr
+  bool output_pass;        // o from the states in h_chunks instead of the recurrence
 };
 
 struct DecodeCall {

@@ -137,9 +137,9 @@ def test_workspace_size_formula(lib):
     f = _chunk(dtype=_lib.KDA_DTYPE_FP32, dk=64, dv=128)
     recf = 3 * 16 * 64 * 4 + 128 * 16 * 4 + 16 * 16 * 4 + 64 * 4
     assert _ws(lib, f) == 256 + 7 * 2 * recf
-    # per-chunk states take the two-kernel path at d=128 as well
-    rec128 = 3 * 16 * 128 * 2 + 128 * 16 * 4 + 16 * 16 * 2 + 128 * 4
-    assert _ws(lib, _chunk(h_chunks=FAKE)) == 256 + 7 * 2 * rec128
+    # per-chunk states and the output pass run on the same fused kernel: same pool
+    assert _ws(lib, _chunk(h_chunks=FAKE)) == 256 + pool
+    assert _ws(lib, _chunk(h_chunks=FAKE, T=100000)) == 256 + pool
 
 
 @pytest.mark.parametrize("over,status", [

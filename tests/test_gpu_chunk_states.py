@@ -53,3 +53,18 @@ def test_chunk_states_and_parallel_output(K, B, T, lengths, gate):
     o2 = kda.kda_chunk_output(d["q"], d["k"], d["v"], hc, **_kw(d))
     torch.cuda.synchronize()
     assert_close("o (chunk-parallel pass)", np64(o2), o_ref, torch.bfloat16)
+
+
+def test_chunk_states_noalloc_matches_workspace_call():
+    """The no-alloc entry point with per-chunk states writes the same states and o."""
+    wl = W.chunk_workload(seed=151, B=1, T=90, H=2, K=128, V=128)
+    d = to_dev(wl)
+    nc = kda.chunk_count(1, 90)
+    hc1 = torch.zeros(nc, 2, 128, 128, dtype=torch.float32, device="cuda")
+    hc2 = torch.ones_like(hc1)
+    o1, h1 = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], h0=d["h0"], h_chunks=hc1, **_kw(d))
+    o2, h2 = kda.kda_chunk_fwd_noalloc(d["q"], d["k"], d["v"], h0=d["h0"], h_chunks=hc2, **_kw(d))
+    torch.cuda.synchronize()
+    assert torch.equal(hc1, hc2)
+    assert torch.equal(o1, o2)
+    assert torch.equal(h1, h2)

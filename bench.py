@@ -409,10 +409,9 @@ def run_gpu(args):
                "achieved_gbs": nbytes / n_avg / 1e9, "kernel": "kda_rmsnorm_kernel",
                "note": "64 MB in + 64 MB out: partly served by L2 (129 MB), so it can exceed the HBM copy rate"}
 
-    # --- short-T recurrent step (its own timed region, not part of the step) ---
-    rec = None
-    if args.only == "all":
-        rw = W.recurrent_workload(seed=5 + 100 * rank, B=RECURRENT_B, T=RECURRENT_T, num_slots=RECURRENT_SLOTS)
+    # --- short-T recurrent step (its own timed regions, not part of the step) ---
+    def recurrent_field(B_r, T_r, slots):
+        rw = W.recurrent_workload(seed=5 + 100 * rank, B=B_r, T=T_r, num_slots=slots)
         rd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in rw.items()}
         orr = torch.empty(rw["B"], rw["T"], rw["HV"], rw["V"], dtype=torch.bfloat16, device=dev)
 
@@ -431,10 +430,16 @@ def run_gpu(args):
         r_avg = r0.elapsed_time(r1) / 1000.0 / K
         r_valid = int((rw["indices"] >= 0).sum())
         rbytes = recurrent_algorithmic_bytes(r_valid, rw["B"], rw["T"])
-        rec = {"us_per_step": 1e6 * r_avg, "rows": rw["B"], "tokens_per_row": rw["T"], "n_valid_rows": r_valid,
-               "tokens_per_s": rw["B"] * rw["T"] / r_avg,
-               "roofline": {"bound": "hbm", "achieved": rbytes / r_avg / 1e9, "unit": "GB/s",
-                            "algorithmic_bytes": rbytes, "kernel": "kda_recurrent_kernel"}}
+        kernel = "kda_recurrent_tc_kernel (chunk form, tensor cores)" if T_r >= 8 else "kda_recurrent_kernel (per token)"
+        return {"us_per_step": 1e6 * r_avg, "rows": rw["B"], "tokens_per_row": rw["T"], "n_valid_rows": r_valid,
+                "tokens_per_s": rw["B"] * rw["T"] / r_avg,
+                "roofline": {"bound": "hbm", "achieved": rbytes / r_avg / 1e9, "unit": "GB/s",
+                             "algorithmic_bytes": rbytes, "kernel": kernel}}
+
+    rec = rec_long = None
+    if args.only == "all":
+        rec = recurrent_field(RECURRENT_B, RECURRENT_T, RECURRENT_SLOTS)
+        rec_long = recurrent_field(RECURRENT_LONG_B, RECURRENT_LONG_T, 2 * RECURRENT_LONG_B)
 
     # --- per-chunk entering states, then the chunk-parallel output pass (own timed regions) ---
     cst = None
@@ -518,6 +523,7 @@ def run_gpu(args):
             "head_rmsnorm": rms,
             "decode_conv": dconv,
             "recurrent": rec,
+            "recurrent_long": rec_long,
             "chunk_states": cst,
             "decode": {"us_per_step": 1e6 * dec_avg, "n_valid_rows": n_valid,
                        "roofline": {"bound": "hbm", "achieved": dach, "peak": hbm, "unit": "GB/s",
@@ -541,10 +547,11 @@ def run_gpu(args):
         if cst is not None:
             for part in ("fwd_with_states", "output_pass"):
                 cst[part]["frac_of_hbm"] = cst[part]["achieved_gbs"] / hbm
-        if rec is not None:
-            rec["roofline"]["peak"] = hbm
-            rec["roofline"]["frac"] = rec["roofline"]["achieved"] / hbm
-            rec["roofline"]["peak_kind"] = peak_kind
+        for r in (rec, rec_long):
+            if r is not None:
+                r["roofline"]["peak"] = hbm
+                r["roofline"]["frac"] = r["roofline"]["achieved"] / hbm
+                r["roofline"]["peak_kind"] = peak_kind
         if args.only != "all" or T != PREFILL_T:
             line["config"]["partial"] = f"only={args.only}, seq_len={T}: a profiling run, not the benchmark line"
         if world == 1 and not args.no_cpu_baseline:

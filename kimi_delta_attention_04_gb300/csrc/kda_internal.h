@@ -112,6 +112,8 @@ size_t fused_smem_bytes();
 size_t fused_workspace_bytes();  // pool of per-cluster global rings (fixed size)
 cudaError_t launch_decode(const DecodeCall& c, cudaStream_t s);
 cudaError_t launch_recurrent(const RecurrentCall& c, cudaStream_t s);
+cudaError_t launch_recurrent_tc(const RecurrentCall& c, cudaStream_t s);  // T tokens as chunks, tensor cores
+cudaError_t launch_recurrent_fma(const RecurrentCall& c, cudaStream_t s);  // T tokens one by one, CUDA cores
 cudaError_t launch_rmsnorm(const RmsNormCall& c, cudaStream_t s);
 
 }  // namespace kda

@@ -216,7 +216,13 @@ cudaError_t launch_recurrent_t(const RecurrentCall& c, cudaStream_t s) {
 
 }  // namespace
 
+// A few tokens per row: the per-token kernel streams the state once for
+// all of them and wins; from 8 tokens the chunk form on the tensor cores does.
 cudaError_t launch_recurrent(const RecurrentCall& c, cudaStream_t s) {
+  return c.T >= 8 ? launch_recurrent_tc(c, s) : launch_recurrent_fma(c, s);
+}
+
+cudaError_t launch_recurrent_fma(const RecurrentCall& c, cudaStream_t s) {
   if (c.B == 0) return cudaSuccess;
   if (c.T < 1 || c.T > kMaxT) return cudaErrorInvalidValue;
   if (c.K == 128 && c.V == 128) return launch_recurrent_t<128, 128>(c, s);

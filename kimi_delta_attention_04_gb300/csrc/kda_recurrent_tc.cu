@@ -1,0 +1,462 @@
+// Short-T KDA recurrent step on a state-slot pool, on the tensor cores.
+//
+// The operation is that of kda_recurrent.cu (the general fused recurrent path
+// that the packed decode specialises; sglang PR #26586 summary, 功能与动机 and
+// 实现拆解): T <= 64 tokens per batch row applied in order to the row's slot,
+// separate q/k/v tensors, value-head grouping hv -> hv / (HV / H), q and k
+// L2-normalised (eps 1e-6 in the root), g = -exp(A_log) softplus(a + dt_bias)
+// per key channel, beta = sigmoid(b).
+//
+// GB300 design. The T tokens of a row are ceil(T/16) chunks of the chunkwise
+// form ("FlashKDA里的L矩阵和Mqk矩阵": L, Mqk, the Neumann inverse, the chunk step
+// "U = INV beta (v - k_dec S); out = q_dec S + Mqk U; S = e^{g_total} S +
+// k_res^T U"), so the state work runs as mma.sync m16n8k16 with fp32
+// accumulation instead of per-token FMA loops. One CTA of V / 16 warps per
+// (row, value head):
+//  * the CTA first asks L2 for the row's 64 KiB slot (bulk prefetch), then
+//    prepares a chunk in shared memory with one thread per key channel (L2
+//    norms, decay products, the anchored level split of L and Mqk, each warp
+//    forming the inverse in registers for its columns of W and U~);
+//  * each warp owns 16 value rows of the state, S^T [16 x K] fp32 in
+//    registers as MMA accumulators, loaded after the chunk's preparation and
+//    stored back after its step (between chunks of a long T the rows make an
+//    L2 round trip rather than stay live across the next preparation):
+//    U^T = U~^T - S^T W^T, O^T = S^T q_dec^T + U^T Mqk^T, S^T = S^T diag(gamma)
+//    + U^T k_res;
+//  * o is staged in shared memory and written as 16-byte rows.
+// Operand precision as in the chunk forward: S, W, q_dec bf16; U, k_res, Mqk
+// fp16; L/Mqk/INV operands fp16 (q, k normalised) or bf16; U~ fp32.
+#include <type_traits>
+
+#include "kda_cluster.cuh"
+#include "kda_common.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kMaxT = 64;
+
+template <int K, int V, typename Q>
+struct RtcSmem {
+  // the chunk's inputs, staged by cp.async ([token][channel], rows past T zeroed)
+  __align__(16) __nv_bfloat16 in_q[16][K];
+  __align__(16) __nv_bfloat16 in_k[16][K];
+  __align__(16) __nv_bfloat16 in_a[16][K];
+  __align__(16) __nv_bfloat16 in_v[16][V];
+  // chunk preparation
+  __align__(16) Q A_lv[4][16][K + 8];  // per level: rows 0-7 k*F, rows 8-15 q*F of the row tokens
+  __align__(16) Q B_lv[4][8][K + 8];   // per level: k*F of the column tokens
+  __align__(16) Q kdec[16][K + 8];
+  __align__(16) __nv_bfloat16 vs[16][V + 8];
+  float Lm[16][17];
+  float Mq[16][17];
+  float red[K / 32][48];
+  float rnq[16], rnk[16], beta[16];
+  // operands of the chunk step
+  __align__(16) __nv_bfloat16 W[16][K + 8];   // -W = -(INV diag(beta) k_dec), [token][channel]
+  __align__(16) __nv_bfloat16 qd[16][K + 8];  // scale q e^{G}
+  __align__(16) __half kr[16][K + 8];         // k e^{G_last - G}
+  __align__(16) __half mqk[16][24];
+  __align__(16) float gamma[K];
+  __align__(16) float ut[V][24];              // U~^T [value row][token]
+  __align__(16) __nv_bfloat16 ostage[16][V + 8];
+};
+
+__device__ __forceinline__ int rt_row_tok(int s, int r) { return (r / s) * 2 * s + s + (r % s); }
+__device__ __forceinline__ int rt_col_tok(int s, int r) { return (r / s) * 2 * s + (r % s); }
+
+template <int K, int V, bool L2N>
+__global__ void __launch_bounds__(V * 2, 2) kda_recurrent_tc_kernel(const RecurrentCall p) {
+  using QK = std::conditional_t<L2N, F16, Bf16>;
+  using Q = typename QK::T;
+  constexpr int WARPS = V / 16;
+  constexpr int NTHR = V * 2;
+  constexpr int NT = K / 8;   // n-tiles of a state row
+  constexpr int KK = K / 16;  // k-steps over the key channels
+  static_assert(NTHR >= K, "one thread per key channel");
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  RtcSmem<K, V, Q>& sm = *reinterpret_cast<RtcSmem<K, V, Q>*>(smem_raw);
+
+  const int T = p.T;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const int unit = blockIdx.x;  // b * HV + hv
+  const int b = unit / p.HV;
+  const int hv = unit - b * p.HV;
+  const int h = hv / (p.HV / p.H);
+  const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(p.q);
+  const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(p.k);
+  const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(p.v);
+  const __nv_bfloat16* ab = reinterpret_cast<const __nv_bfloat16*>(p.a);
+  const __nv_bfloat16* bb = reinterpret_cast<const __nv_bfloat16*>(p.b);
+
+  const int slot = p.indices[b];
+  if (slot < 0 || slot >= p.num_slots) {
+    if (slot >= p.num_slots && tid == 0) set_err(p.err, 1 /* KDA_ERR_INVALID_ARG */);
+    for (int i = tid; i < T * (V / 8); i += NTHR) {
+      const int tok = i / (V / 8), v8 = i - tok * (V / 8);
+      *reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o) +
+                                ((static_cast<size_t>(b) * T + tok) * p.HV + hv) * V + v8 * 8) = make_uint4(0, 0, 0, 0);
+    }
+    return;
+  }
+  float* const S_slot = p.state_pool + (static_cast<size_t>(slot) * p.HV + hv) * static_cast<size_t>(V) * K;
+  if (tid == 0) {
+    constexpr uint32_t kPart = 16384;
+    for (uint32_t off = 0; off < static_cast<uint32_t>(V * K * 4); off += kPart)
+      bulk_prefetch_l2(reinterpret_cast<const unsigned char*>(S_slot) + off, kPart);
+  }
+
+  const bool kown = tid < K;
+  const bool vown = tid < V;
+  const int ch = kown ? tid : 0;
+  const float Aexp = expf(p.A_log[hv]);
+  const float dtb = kown ? p.dt_bias[hv * K + ch] : 0.f;
+
+  const int r0 = warp * 16;  // first value row of this warp
+  const int nch = (T + 15) / 16;
+  for (int c = 0; c < nch; ++c) {
+    const int tok0 = 16 * c;
+    const int ntok = min(16, T - tok0);
+    // ---------------- chunk preparation ----------------
+    {  // 16-byte rows of q, k (head h), a and v (value head hv)
+      const size_t bt0 = static_cast<size_t>(b) * T + tok0;
+      for (int i = tid; i < 16 * (K / 8); i += NTHR) {
+        const int row = i / (K / 8), c8 = i - row * (K / 8);
+        if (row < ntok) {
+          const size_t qk = ((bt0 + row) * p.H + h) * K + c8 * 8;
+          cp_async16(&sm.in_q[row][c8 * 8], qb + qk);
+          cp_async16(&sm.in_k[row][c8 * 8], kb + qk);
+          cp_async16(&sm.in_a[row][c8 * 8], ab + ((bt0 + row) * p.HV + hv) * K + c8 * 8);
+        } else {
+          *reinterpret_cast<uint4*>(&sm.in_q[row][c8 * 8]) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(&sm.in_k[row][c8 * 8]) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(&sm.in_a[row][c8 * 8]) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      for (int i = tid; i < 16 * (V / 8); i += NTHR) {
+        const int row = i / (V / 8), c8 = i - row * (V / 8);
+        if (row < ntok) cp_async16(&sm.in_v[row][c8 * 8], vb + ((bt0 + row) * p.HV + hv) * V + c8 * 8);
+        else *reinterpret_cast<uint4*>(&sm.in_v[row][c8 * 8]) = make_uint4(0, 0, 0, 0);
+      }
+      cp_async_commit();
+    }
+    for (int i = tid; i < 16 * 17; i += NTHR) {
+      (&sm.Lm[0][0])[i] = 0.f;
+      (&sm.Mq[0][0])[i] = 0.f;
+    }
+    if (tid < 16) {
+      float bt = 0.f;
+      if (tid < ntok) bt = sigmoid_f(__bfloat162float(bb[(static_cast<size_t>(b) * T + tok0 + tid) * p.HV + hv]));
+      sm.beta[tid] = bt;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+    float qv[16], kv[16], al[16];
+    if (kown) {
+      constexpr float kLog2e = 1.4426950408889634f;
+      const float nA = -Aexp;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const bool valid = i < ntok;
+        qv[i] = __bfloat162float(sm.in_q[i][ch]);
+        kv[i] = __bfloat162float(sm.in_k[i][ch]);
+        const float x = __bfloat162float(sm.in_a[i][ch]) + dtb;
+        // alpha = e^{-A softplus(x)} = 2^{-A log2(1 + 2^{x log2 e})}, x itself above 20
+        const float l2 = lg2_approx(1.f + ex2_approx(fminf(x, 20.f) * kLog2e));
+        const float sp2 = x > 20.f ? x * kLog2e : l2;
+        al[i] = valid ? ex2_approx(nA * sp2) : 1.f;
+      }
+      float red[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) red[i] = qv[i] * qv[i];
+      const float t1 = warp_transpose_reduce16(red, lane);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) red[i] = kv[i] * kv[i];
+      const float t2 = warp_transpose_reduce16(red, lane);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) red[i] = qv[i] * kv[i];
+      const float t3 = warp_transpose_reduce16(red, lane);
+      if ((lane & 1) == 0) {
+        const int j = lane >> 1;
+        sm.red[warp][j] = t1;
+        sm.red[warp][16 + j] = t2;
+        sm.red[warp][32 + j] = t3;
+      }
+    }
+    if (vown) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sm.vs[i][tid] = sm.in_v[i][tid];
+    }
+    __syncthreads();
+    if (tid < 16) {
+      float sq = 0.f, sk = 0.f, sqk = 0.f;
+#pragma unroll
+      for (int w = 0; w < K / 32; ++w) {
+        sq += sm.red[w][tid];
+        sk += sm.red[w][16 + tid];
+        sqk += sm.red[w][32 + tid];
+      }
+      const float rq = p.l2norm ? rsqrtf(sq + 1e-6f) : 1.f;
+      const float rk = p.l2norm ? rsqrtf(sk + 1e-6f) : 1.f;
+      sm.rnq[tid] = rq;
+      sm.rnk[tid] = rk;
+      sm.Mq[tid][tid] = p.scale * sqk * rq * rk;
+    }
+    __syncthreads();
+    if (kown) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        qv[i] *= sm.rnq[i];
+        kv[i] *= sm.rnk[i];
+      }
+      float P[16], Rs[16];
+      P[0] = al[0];
+#pragma unroll
+      for (int i = 1; i < 16; ++i) P[i] = P[i - 1] * al[i];
+      Rs[15] = 1.f;
+#pragma unroll
+      for (int i = 14; i >= 0; --i) Rs[i] = Rs[i + 1] * al[i + 1];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        sm.qd[i][ch] = __float2bfloat16_rn(p.scale * qv[i] * P[i]);
+        sm.kr[i][ch] = __float2half_rn(kv[i] * Rs[i]);
+        sm.kdec[i][ch] = QK::cvt(kv[i] * P[i]);
+      }
+      sm.gamma[ch] = P[15];
+#pragma unroll
+      for (int lv = 0; lv < 4; ++lv) {
+        const int s = 8 >> lv;
+#pragma unroll
+        for (int blk = 0; blk < 8 / s; ++blk) {
+          const int m = blk * 2 * s + s;  // anchor: first row of the upper half
+          float f = 1.f;
+#pragma unroll
+          for (int i = m; i < m + s; ++i) {  // row tokens: prod_{m<t<=i} alpha_t
+            if (i > m) f *= al[i];
+            const int r = blk * s + (i - m);
+            sm.A_lv[lv][r][ch] = QK::cvt(kv[i] * f);
+            sm.A_lv[lv][8 + r][ch] = QK::cvt(qv[i] * f);
+          }
+          f = 1.f;
+#pragma unroll
+          for (int i = m - 1; i >= m - s; --i) {  // column tokens: prod_{i<t<=m} alpha_t
+            f *= al[i + 1];
+            sm.B_lv[lv][blk * s + (i - (m - s))][ch] = QK::cvt(kv[i] * f);
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (warp < 4) {  // level `warp` of the anchored split: L (rows 0-7) and Mqk (rows 8-15)
+      const int lv = warp;
+      const int s = 8 >> lv;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kk = 0; kk < KK; ++kk) {
+        uint32_t a[4], bq[2];
+        ldsm_x4(a, &sm.A_lv[lv][lane & 15][16 * kk + (lane >> 4) * 8]);
+        ldsm_x2(bq, &sm.B_lv[lv][lane & 7][16 * kk + ((lane >> 3) & 1) * 8]);
+        mma16816<QK>(acc, a, bq[0], bq[1]);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int r = g + ((e & 2) ? 8 : 0);
+        const int cidx = 2 * t + (e & 1);
+        const int rr = r & 7;
+        if (rr / s != cidx / s) continue;  // not a pair of this level
+        const int i = rt_row_tok(s, rr), j = rt_col_tok(s, cidx);
+        if (r < 8) sm.Lm[i][j] = sm.beta[i] * acc[e];
+        else sm.Mq[i][j] = p.scale * acc[e];
+      }
+    }
+    __syncthreads();
+    for (int e = tid; e < 256; e += NTHR) sm.mqk[e >> 4][e & 15] = __float2half_rn(sm.Mq[e >> 4][e & 15]);
+    {
+      // INV' = (I + L)^{-1} diag(beta), formed by every warp in registers
+      Frag16 inv = neumann_inverse16<QK>(&sm.Lm[0][0], 17, lane);
+      Frag16 ihi, ilo;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float x = inv.c[nt][e] * sm.beta[8 * nt + 2 * t + (e & 1)];
+          inv.c[nt][e] = x;
+          ihi.c[nt][e] = __bfloat162float(__float2bfloat16_rn(x));
+          ilo.c[nt][e] = x - ihi.c[nt][e];
+        }
+      uint32_t a[4], ahi[4], alo[4];
+      frag_as_a<QK>(inv, a);
+      frag_as_a<Bf16>(ihi, ahi);
+      frag_as_a<Bf16>(ilo, alo);
+      for (int blk = warp; blk < K / 16; blk += WARPS) {  // -W, 16 key channels per block
+        const int n0 = 16 * blk;
+        uint32_t bw[4];
+        ldsm_x4_trans(bw, &sm.kdec[lane & 15][n0 + (lane >> 4) * 8]);
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816<QK>(c0, a, bw[0], bw[1]);
+        mma16816<QK>(c1, a, bw[2], bw[3]);
+        *reinterpret_cast<uint32_t*>(&sm.W[g][n0 + 2 * t]) = Bf16::pack(-c0[0], -c0[1]);
+        *reinterpret_cast<uint32_t*>(&sm.W[g + 8][n0 + 2 * t]) = Bf16::pack(-c0[2], -c0[3]);
+        *reinterpret_cast<uint32_t*>(&sm.W[g][n0 + 8 + 2 * t]) = Bf16::pack(-c1[0], -c1[1]);
+        *reinterpret_cast<uint32_t*>(&sm.W[g + 8][n0 + 8 + 2 * t]) = Bf16::pack(-c1[2], -c1[3]);
+      }
+      for (int blk = warp; blk < V / 16; blk += WARPS) {  // U~ (fp32 through a hi/lo split), 16 value channels
+        const int n0 = 16 * blk;
+        uint32_t bv[4];
+        ldsm_x4_trans(bv, &sm.vs[lane & 15][n0 + (lane >> 4) * 8]);
+        float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma16816<Bf16>(u0, ahi, bv[0], bv[1]);
+        mma16816<Bf16>(u0, alo, bv[0], bv[1]);
+        mma16816<Bf16>(u1, ahi, bv[2], bv[3]);
+        mma16816<Bf16>(u1, alo, bv[2], bv[3]);
+        sm.ut[n0 + 2 * t][g] = u0[0];
+        sm.ut[n0 + 2 * t + 1][g] = u0[1];
+        sm.ut[n0 + 2 * t][g + 8] = u0[2];
+        sm.ut[n0 + 2 * t + 1][g + 8] = u0[3];
+        sm.ut[n0 + 8 + 2 * t][g] = u1[0];
+        sm.ut[n0 + 8 + 2 * t + 1][g] = u1[1];
+        sm.ut[n0 + 8 + 2 * t][g + 8] = u1[2];
+        sm.ut[n0 + 8 + 2 * t + 1][g + 8] = u1[3];
+      }
+    }
+    float S[NT][4];
+    {  // the state, in the accumulator layout (its lines are in L2 by now)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float2 x = __ldcs(reinterpret_cast<const float2*>(S_slot + (r0 + g) * K + 8 * nt + 2 * t));
+        const float2 y = __ldcs(reinterpret_cast<const float2*>(S_slot + (r0 + g + 8) * K + 8 * nt + 2 * t));
+        S[nt][0] = x.x; S[nt][1] = x.y; S[nt][2] = y.x; S[nt][3] = y.y;
+      }
+    }
+    __syncthreads();
+
+    // ---------------- chunk step on this warp's 16 value rows ----------------
+    float u[2][4], u2[2][4], o[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const float2 x = *reinterpret_cast<const float2*>(&sm.ut[r0 + g][8 * nt + 2 * t]);
+      const float2 y = *reinterpret_cast<const float2*>(&sm.ut[r0 + g + 8][8 * nt + 2 * t]);
+      u[nt][0] = x.x; u[nt][1] = x.y; u[nt][2] = y.x; u[nt][3] = y.y;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) { u2[nt][e] = 0.f; o[nt][e] = 0.f; }
+    }
+    // U^T = U~^T + S^T (-W)^T ; O^T = S^T q_dec^T (S^T as bf16 A fragments, one
+    // k-step at a time: the accumulator layout of two n-tiles is the A layout)
+#pragma unroll
+    for (int kk = 0; kk < KK; ++kk) {
+      uint32_t sa[4];
+      sa[0] = Bf16::pack(S[2 * kk][0], S[2 * kk][1]);
+      sa[1] = Bf16::pack(S[2 * kk][2], S[2 * kk][3]);
+      sa[2] = Bf16::pack(S[2 * kk + 1][0], S[2 * kk + 1][1]);
+      sa[3] = Bf16::pack(S[2 * kk + 1][2], S[2 * kk + 1][3]);
+      const int row = ((lane >> 4) << 3) + (lane & 7);
+      const int col = 16 * kk + ((lane >> 3) & 1) * 8;
+      uint32_t bm[4];
+      ldsm_x4(bm, &sm.W[row][col]);
+      float (&acc)[2][4] = (kk & 1) ? u2 : u;
+      mma16816<Bf16>(acc[0], sa, bm[0], bm[1]);
+      mma16816<Bf16>(acc[1], sa, bm[2], bm[3]);
+      ldsm_x4(bm, &sm.qd[row][col]);
+      mma16816<Bf16>(o[0], sa, bm[0], bm[1]);
+      mma16816<Bf16>(o[1], sa, bm[2], bm[3]);
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) u[nt][e] += u2[nt][e];
+    uint32_t ua[4];
+    ua[0] = F16::pack(u[0][0], u[0][1]);
+    ua[1] = F16::pack(u[0][2], u[0][3]);
+    ua[2] = F16::pack(u[1][0], u[1][1]);
+    ua[3] = F16::pack(u[1][2], u[1][3]);
+    // S^T = S^T diag(gamma) + U^T k_res
+#pragma unroll
+    for (int np = 0; np < KK; ++np) {
+      uint32_t bm[4];
+      ldsm_x4_trans(bm, &sm.kr[lane & 15][16 * np + (lane >> 4) * 8]);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int nt = 2 * np + half;
+        const float2 gm = *reinterpret_cast<const float2*>(&sm.gamma[8 * nt + 2 * t]);
+        S[nt][0] *= gm.x; S[nt][1] *= gm.y; S[nt][2] *= gm.x; S[nt][3] *= gm.y;
+        mma16816<F16>(S[nt], ua, bm[2 * half], bm[2 * half + 1]);
+      }
+    }
+    // O^T += U^T Mqk^T
+    {
+      uint32_t bm[4];
+      const int row = ((lane >> 4) << 3) + (lane & 7);
+      ldsm_x4(bm, &sm.mqk[row][((lane >> 3) & 1) * 8]);
+      mma16816<F16>(o[0], ua, bm[0], bm[1]);
+      mma16816<F16>(o[1], ua, bm[2], bm[3]);
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const int tok = 8 * nt + 2 * t;
+      sm.ostage[tok][r0 + g] = __float2bfloat16_rn(o[nt][0]);
+      sm.ostage[tok + 1][r0 + g] = __float2bfloat16_rn(o[nt][1]);
+      sm.ostage[tok][r0 + g + 8] = __float2bfloat16_rn(o[nt][2]);
+      sm.ostage[tok + 1][r0 + g + 8] = __float2bfloat16_rn(o[nt][3]);
+    }
+    __syncthreads();
+    for (int i = tid; i < ntok * (V / 8); i += NTHR) {
+      const int row = i / (V / 8), v8 = i - row * (V / 8);
+      __nv_bfloat16* dst =
+          reinterpret_cast<__nv_bfloat16*>(p.o) + ((static_cast<size_t>(b) * T + tok0 + row) * p.HV + hv) * V + v8 * 8;
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&sm.ostage[row][v8 * 8]);
+    }
+    // The state goes back to its slot after every chunk (each warp rereads only
+    // its own rows, after the next chunk's preparation): between chunks it is
+    // an L2 round trip instead of registers held across the preparation.
+    if (c + 1 < nch) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        __stcg(reinterpret_cast<float2*>(S_slot + (r0 + g) * K + 8 * nt + 2 * t), make_float2(S[nt][0], S[nt][1]));
+        __stcg(reinterpret_cast<float2*>(S_slot + (r0 + g + 8) * K + 8 * nt + 2 * t), make_float2(S[nt][2], S[nt][3]));
+      }
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        __stcs(reinterpret_cast<float2*>(S_slot + (r0 + g) * K + 8 * nt + 2 * t), make_float2(S[nt][0], S[nt][1]));
+        __stcs(reinterpret_cast<float2*>(S_slot + (r0 + g + 8) * K + 8 * nt + 2 * t), make_float2(S[nt][2], S[nt][3]));
+      }
+    }
+    __syncthreads();  // the next chunk's preparation reuses every buffer above
+  }
+}
+
+template <int K, int V, bool L2N>
+cudaError_t launch_rtc_t(const RecurrentCall& c, cudaStream_t s) {
+  using Q = typename std::conditional_t<L2N, F16, Bf16>::T;
+  constexpr size_t smem = sizeof(RtcSmem<K, V, Q>);
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e = cudaFuncSetAttribute(kda_recurrent_tc_kernel<K, V, L2N>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const unsigned grid = static_cast<unsigned>(c.B) * static_cast<unsigned>(c.HV);
+  kda_recurrent_tc_kernel<K, V, L2N><<<grid, V * 2, smem, s>>>(c);
+  return cudaGetLastError();
+}
+
+template <int K, int V>
+cudaError_t launch_rtc_kv(const RecurrentCall& c, cudaStream_t s) {
+  return c.l2norm ? launch_rtc_t<K, V, true>(c, s) : launch_rtc_t<K, V, false>(c, s);
+}
+
+}  // namespace
+
+cudaError_t launch_recurrent_tc(const RecurrentCall& c, cudaStream_t s) {
+  if (c.B == 0) return cudaSuccess;
+  if (c.T < 1 || c.T > kMaxT) return cudaErrorInvalidValue;
+  if (c.K == 128 && c.V == 128) return launch_rtc_kv<128, 128>(c, s);
+  if (c.K == 128 && c.V == 64) return launch_rtc_kv<128, 64>(c, s);
+  if (c.K == 64 && c.V == 128) return launch_rtc_kv<64, 128>(c, s);
+  if (c.K == 64 && c.V == 64) return launch_rtc_kv<64, 64>(c, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kda

@@ -1,6 +1,7 @@
 """GPU parity of kda_recurrent_step (T tokens per row on a state-slot pool)
 against the fp64 oracle, through the C ABI (ctypes binding) on the same
-bf16-rounded inputs. Tolerances as for decode: rel-Frobenius <= 5e-3 and
+bf16-rounded inputs. Below 8 tokens the call runs the per-token kernel, from
+8 the chunk-form kernel; the cases cover both sides of the switch. Tolerances as for decode: rel-Frobenius <= 5e-3 and
 max-abs <= 2e-2 for o and the updated slots; padding rows and slots no row
 indexes are bit-exact."""
 
@@ -60,6 +61,9 @@ def _check(wl):
     (3, 33, 1, 2, 128, 64),    # more tokens than one warp's share, HV = 2H
     (6, 1, 2, 4, 64, 128),     # T = 1
     (2, 64, 1, 1, 128, 128),   # the longest T the entry point takes
+    (5, 7, 2, 4, 128, 128),    # the per-token kernel's longest T
+    (5, 16, 2, 2, 128, 128),   # the chunk kernel on one full chunk
+    (3, 17, 2, 4, 64, 128),    # two chunks, the second of one token
 ])
 def test_recurrent_small(B, T, H, HV, K, V):
     wl = W.recurrent_workload(seed=90 + B + T, B=B, T=T, H=H, HV=HV, K=K, V=V, num_slots=2 * B + 3, pad_frac=0.25)

@@ -81,6 +81,7 @@ def decode_algorithmic_bytes(n_valid, H=32, HV=32, K=128, V=128, B=256):
 CHUNK_KERNEL_SOURCES = ["kda_chunk_fused.cu", "kda_common.cuh", "kda_cluster.cuh", "kda_tma.h", "kda_tma.cpp"]
 DECODE_KERNEL_SOURCES = ["kda_decode.cu", "kda_common.cuh"]
 RECURRENT_B, RECURRENT_T, RECURRENT_SLOTS = 128, 8, 256  # speculative-style step: 128 rows x 8 tokens
+RECURRENT_LONG_B, RECURRENT_LONG_T = 64, 64              # the longest T the entry point takes
 CHUNK_LAUNCHES_PER_STEP = 1   # kda_chunk_fused_kernel (bf16, d = 128, no cu_seqlens)
 DECODE_LAUNCHES_PER_STEP = 1  # kda_decode_kernel
 

@@ -176,7 +176,9 @@ __device__ int claim_ring(unsigned char* pool, int32_t* err) {
   }
 }
 
-template <bool DELTA, bool L2N>
+// MODE 0: the forward; 1: the forward writing the state entering every chunk
+// to h_chunks; 2: the chunk-parallel output pass from those states.
+template <bool DELTA, bool L2N, int MODE>
 __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1)
     kda_chunk_fused_kernel(const ChunkCall p, const __grid_constant__ TmaInputMaps maps) {
   using QK = std::conditional_t<L2N, F16, Bf16>;
@@ -230,7 +232,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     const int kc0 = dkh * 64;                                    // first key channel of this warp
     // Output pass: no recurrence; S holds the next chunk's entering state,
     // loaded from h_chunks one chunk ahead of its use.
-    const bool outp = p.output_pass;
+    constexpr bool outp = MODE == 2;
     float S[8][4];
     auto load_state = [&](const float* src) {
 #pragma unroll
@@ -294,13 +296,12 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       for (int cc = 2; cc < 2 + kSnapAhead; ++cc) prefetch_state(cc);
       if (nch > 1) load_state(snapshot(1));
     }
-    float* const snap = (p.h_chunks == nullptr || outp)
-                            ? nullptr
-                            : p.h_chunks + (static_cast<size_t>(cb) * H + h) * FD * FD + (row0 + g) * FD + kc0 + 2 * t;
+    float* const snap = MODE != 1 ? nullptr
+                                  : p.h_chunks + (static_cast<size_t>(cb) * H + h) * FD * FD + (row0 + g) * FD + kc0 + 2 * t;
     for (int c = 0; c < nch; ++c) {
       const int s = c & (kRing - 1);
       const uint32_t par = static_cast<uint32_t>(c / kRing) & 1u;
-      if (snap != nullptr) {  // the state entering chunk c, before its decay (streaming stores)
+      if (MODE == 1) {  // the state entering chunk c, before its decay (streaming stores)
         float* dst = snap + static_cast<size_t>(c) * H * FD * FD;
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
@@ -827,13 +828,13 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
   }
 }
 
-template <bool DELTA, bool L2N>
+template <bool DELTA, bool L2N, int MODE>
 cudaError_t launch_fused_t(const ChunkCall& c, cudaStream_t s) {
   using QK = std::conditional_t<L2N, F16, Bf16>;
   const size_t smem = sizeof(FusedSmem<typename QK::T>);
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kda_chunk_fused_kernel<DELTA, L2N>,
+    cudaError_t e = cudaFuncSetAttribute(kda_chunk_fused_kernel<DELTA, L2N, MODE>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     attr = true;
@@ -845,7 +846,7 @@ cudaError_t launch_fused_t(const ChunkCall& c, cudaStream_t s) {
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(c.records, 0, kPoolHeader, s);  // every pool ring free
   if (e != cudaSuccess) return e;
-  kda_chunk_fused_kernel<DELTA, L2N><<<grid, kFusedThreads, smem, s>>>(c, maps);
+  kda_chunk_fused_kernel<DELTA, L2N, MODE><<<grid, kFusedThreads, smem, s>>>(c, maps);
   return cudaGetLastError();
 }
 
@@ -858,10 +859,16 @@ size_t fused_smem_bytes() { return sizeof(FusedSmem<__half>); }
 
 size_t fused_workspace_bytes() { return kPoolHeader + static_cast<size_t>(kPool) * kRingBytes; }
 
+template <int MODE>
+cudaError_t launch_fused_mode(const ChunkCall& c, cudaStream_t s) {
+  if (c.delta) return c.l2norm ? launch_fused_t<true, true, MODE>(c, s) : launch_fused_t<true, false, MODE>(c, s);
+  return c.l2norm ? launch_fused_t<false, true, MODE>(c, s) : launch_fused_t<false, false, MODE>(c, s);
+}
+
 cudaError_t launch_chunk_fused(const ChunkCall& c, cudaStream_t s) {
   if (c.dk != FD || c.dv != FD) return cudaErrorInvalidValue;
-  if (c.delta) return c.l2norm ? launch_fused_t<true, true>(c, s) : launch_fused_t<true, false>(c, s);
-  return c.l2norm ? launch_fused_t<false, true>(c, s) : launch_fused_t<false, false>(c, s);
+  if (c.output_pass) return c.h_chunks != nullptr ? launch_fused_mode<2>(c, s) : cudaErrorInvalidValue;
+  return c.h_chunks != nullptr ? launch_fused_mode<1>(c, s) : launch_fused_mode<0>(c, s);
 }
 
 }  // namespace kda

@@ -17,6 +17,7 @@
 //   * the two dot products of each row (S~ k and S~ q) are reduced for 8 rows
 //     at once with a transpose reduction (16 shuffles for 16 sums); the output
 //     uses o_r = S~_r q + u_r (k q), so no second pass over the updated row.
+#include "kda_cluster.cuh"
 #include "kda_common.cuh"
 
 namespace kda {
@@ -116,6 +117,13 @@ __global__ void __launch_bounds__(kDecodeThreads) kda_decode_kernel(const Decode
   const int row0 = warp * ROWS_PER_WARP;
   const int col0 = lane * CPL;
 
+  // With the conv in front, the stream below waits for the conv's loads and a
+  // barrier: the whole slot is asked of L2 first, so the stream then hits L2.
+  if (CONV && threadIdx.x == 0) {
+    constexpr uint32_t kPart = 16384;
+    for (uint32_t off = 0; off < static_cast<uint32_t>(V * K * 4); off += kPart)
+      bulk_prefetch_l2(reinterpret_cast<const unsigned char*>(S) + off, kPart);
+  }
   // Start the first state rows before anything else: they are the long pole.
   Vec cur[kRowGroup];
 #pragma unroll
@@ -126,19 +134,23 @@ __global__ void __launch_bounds__(kDecodeThreads) kda_decode_kernel(const Decode
   const __nv_bfloat16* row = reinterpret_cast<const __nv_bfloat16*>(p.packed_qkv) + static_cast<size_t>(b) * C;
   float qv[CPL], kv[CPL], av[CPL];
   __shared__ float vconv[CONV ? V : 1];
+  __shared__ __align__(16) float qkconv[CONV ? 2 * K : 4];
   if (CONV) {
-    // Every warp needs the whole q and k (they differ only in state rows), and a
-    // q/k channel is also read by the other value heads of its group: all
-    // convolve from the old state first; after the barrier, warp 0 of the
-    // group's first value head writes the new q/k state. Each v channel has one
-    // owning thread, which reads and writes it.
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-      qv[i] = conv_silu(p, slot, b, C, h * K + col0 + i, false);
-      kv[i] = conv_silu(p, slot, b, C, p.H * K + h * K + col0 + i, false);
-    }
+    // Every warp needs the whole q and k (they differ only in state rows): the
+    // CTA's threads convolve the 2K q/k channels once between them and share
+    // them through shared memory. A q/k channel is also read by the other value
+    // heads of its group, so all convolve from the old state first; after the
+    // barrier, warp 0 of the group's first value head writes the new q/k state.
+    // Each v channel has one owning thread, which reads and writes it.
+    for (int c = threadIdx.x; c < 2 * K; c += kDecodeThreads)
+      qkconv[c] = conv_silu(p, slot, b, C, (c < K ? h * K + c : p.H * K + h * K + c - K), false);
     for (int r = threadIdx.x; r < V; r += kDecodeThreads) vconv[r] = conv_silu(p, slot, b, C, 2 * p.H * K + hv * V + r, true);
     __syncthreads();
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      qv[i] = qkconv[col0 + i];
+      kv[i] = qkconv[K + col0 + i];
+    }
     if (warp == 0 && hv % (p.HV / p.H) == 0) {
 #pragma unroll
       for (int i = 0; i < CPL; ++i) {

@@ -185,9 +185,10 @@ def dist_env():
     return world, rank, local
 
 
-def oracle_sample(T_sample=None, budget_s=20.0):
-    """Time the fp64 oracle (token recurrence, as it stands) on the first tokens
-    of the prefill workload, all 32 heads. Returns (tokens/s, sample text, cores)."""
+def oracle_sample(T_sample=None, budget_s=20.0, chunk_size=None):
+    """Time the fp64 oracle (as it stands: the token recurrence, or with
+    chunk_size its chunked form) on the first tokens of the prefill workload,
+    all 32 heads. Returns (tokens/s, sample text, cores)."""
     import numpy as np  # noqa: F401
 
     from kimi_delta_attention_04_gb300 import workloads as W
@@ -200,16 +201,19 @@ def oracle_sample(T_sample=None, budget_s=20.0):
     t0 = time.perf_counter()
     ko.kda_forward(np64(wl["q"][:, :T_cal]), np64(wl["k"][:, :T_cal]), np64(wl["v"][:, :T_cal]),
                    scale=wl["scale"], a=np64(wl["a"][:, :T_cal]), dt_bias=np64(wl["dt_bias"]),
-                   A_log=np64(wl["A_log"]), b=np64(wl["b"][:, :T_cal]), h0=np64(wl["h0"]), l2norm_qk=True)
+                   A_log=np64(wl["A_log"]), b=np64(wl["b"][:, :T_cal]), h0=np64(wl["h0"]), l2norm_qk=True,
+                   chunk_size=chunk_size)
     per_tok = (time.perf_counter() - t0) / T_cal
     if T_sample is None:
         T_sample = int(max(64, min(PREFILL_T, budget_s / max(per_tok, 1e-6))))
     t0 = time.perf_counter()
     ko.kda_forward(np64(wl["q"][:, :T_sample]), np64(wl["k"][:, :T_sample]), np64(wl["v"][:, :T_sample]),
                    scale=wl["scale"], a=np64(wl["a"][:, :T_sample]), dt_bias=np64(wl["dt_bias"]),
-                   A_log=np64(wl["A_log"]), b=np64(wl["b"][:, :T_sample]), h0=np64(wl["h0"]), l2norm_qk=True)
+                   A_log=np64(wl["A_log"]), b=np64(wl["b"][:, :T_sample]), h0=np64(wl["h0"]), l2norm_qk=True,
+                   chunk_size=chunk_size)
     dt = time.perf_counter() - t0
-    sample = (f"fp64 token-recurrence oracle, first {T_sample} of 8192 tokens of the prefill workload, "
+    form = "token-recurrence" if chunk_size is None else f"chunked (C={chunk_size})"
+    sample = (f"fp64 {form} oracle, first {T_sample} of 8192 tokens of the prefill workload, "
               f"all 32 heads, one process ({dt:.1f} s)")
     return T_sample / dt, sample, 1
 
@@ -309,6 +313,35 @@ def run_gpu(args):
     chunk_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
     dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     total_ms = e0.elapsed_time(e1)
+
+    # --- decode launch overheads: host wall-clock per step including the launch,
+    # and the same steps replayed from a CUDA graph ---
+    dec_wall = dec_graph = None
+    if args.only != "chunk":
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(K):
+            decode_step()
+        torch.cuda.synchronize(dev)
+        dec_wall = (time.perf_counter() - t0) / K
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                kda.kda_decode_step(dd["packed_qkv"], dd["a"], dd["b"], dd["A_log"], dd["dt_bias"], pool,
+                                    dd["indices"], H=dw["H"], HV=dw["HV"], K=dw["K"], V=dw["V"], scale=dw["scale"],
+                                    o=od, stream=cap)
+        stream.wait_stream(cap)
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(K):
+            graph.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        dec_graph = g0.elapsed_time(g1) / 1000.0 / K
 
     # --- e2e through the public API with pinned host buffers ---
     host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in wl.items()}
@@ -527,6 +560,8 @@ def run_gpu(args):
             "recurrent_long": rec_long,
             "chunk_states": cst,
             "decode": {"us_per_step": 1e6 * dec_avg, "n_valid_rows": n_valid,
+                       "wall_us_per_step_with_launch": None if dec_wall is None else 1e6 * dec_wall,
+                       "graph_replay_us_per_step": None if dec_graph is None else 1e6 * dec_graph,
                        "roofline": {"bound": "hbm", "achieved": dach, "peak": hbm, "unit": "GB/s",
                                     "frac": dach / hbm, "algorithmic_bytes": dbytes,
                                     "traffic": stored_traffic("kda_decode_kernel", dec_sha, n_valid), "peak_kind": peak_kind}},
@@ -558,6 +593,9 @@ def run_gpu(args):
         if world == 1 and not args.no_cpu_baseline:
             v, sample, cores = oracle_sample(budget_s=args.cpu_budget)
             line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+            v, sample, cores = oracle_sample(budget_s=args.cpu_budget / 3, chunk_size=16)
+            line["cpu_baseline_chunked"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                            "sample": sample}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -83,6 +83,11 @@ typedef enum {
 /* flags */
 #define KDA_FLAG_L2NORM_QK 0x1u  /* q <- q / sqrt(sum q^2 + 1e-6), same for k, in the kernel */
 #define KDA_FLAG_DELTA_OFF 0x2u  /* u_t = v_t: plain (gated) linear attention, beta ignored */
+/* Debug (decode, decode-conv and recurrent steps): before the step, check that
+ * the valid slot indices are distinct; a repeat writes KDA_ERR_INVALID_ARG to
+ * err (which the flag requires). The step itself still runs: the check
+ * reports a caller error, it does not repair it. O(B^2) work. */
+#define KDA_FLAG_CHECK_INDICES 0x4u
 
 /*
  * Arguments of kda_chunk_fwd.
@@ -194,14 +199,15 @@ kda_status kda_chunk_output(const kda_chunk_args* args, void* workspace, size_t 
  * g = -exp(A_log[hv]) * softplus(a + dt_bias); with KDA_FLAG_L2NORM_QK q and k
  * are L2-normalised (eps 1e-6 inside the root); q is multiplied by scale.
  * A padding row writes o = 0 and touches no state. Valid indices must be
- * distinct (rows sharing a slot race). An index >= num_slots writes
- * KDA_ERR_INVALID_ARG to err, zeroes that row's o and touches no state.
+ * distinct (rows sharing a slot race; KDA_FLAG_CHECK_INDICES checks it). An
+ * index >= num_slots writes KDA_ERR_INVALID_ARG to err, zeroes that row's o
+ * and touches no state.
  * Supported: K, V in {64, 128}.
  */
 typedef struct kda_decode_args {
   int32_t B, H, HV, K, V;
   int32_t num_slots;
-  uint32_t flags;      /* KDA_FLAG_L2NORM_QK */
+  uint32_t flags;      /* KDA_FLAG_L2NORM_QK, KDA_FLAG_CHECK_INDICES */
   float scale;
   const void* packed_qkv;
   const void* a;
@@ -281,7 +287,7 @@ kda_status kda_decode_conv_step(const kda_decode_conv_args* args, kda_stream_t s
 typedef struct kda_recurrent_args {
   int32_t B, T, H, HV, K, V;
   int32_t num_slots;
-  uint32_t flags;      /* KDA_FLAG_L2NORM_QK */
+  uint32_t flags;      /* KDA_FLAG_L2NORM_QK, KDA_FLAG_CHECK_INDICES */
   float scale;
   const void* q;
   const void* k;

@@ -34,6 +34,7 @@ KDA_GATE_NONE, KDA_GATE_G, KDA_GATE_INPUTS, KDA_GATE_HEAD_G = 0, 1, 2, 3
 KDA_BETA_VALUES, KDA_BETA_LOGITS = 0, 1
 KDA_FLAG_L2NORM_QK = 0x1
 KDA_FLAG_DELTA_OFF = 0x2
+KDA_FLAG_CHECK_INDICES = 0x4
 
 
 class KdaError(RuntimeError):
@@ -269,12 +270,12 @@ def kda_chunk_fwd_noalloc(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log
 
 
 def make_decode_args(packed_qkv, a, b, A_log, dt_bias, state_pool, indices, *, H, HV, K, V, scale,
-                     l2norm_qk=True, o=None, err=None):
+                     l2norm_qk=True, o=None, err=None, check_indices=False):
     args = DecodeArgs()
     args.B = packed_qkv.shape[0]
     args.H, args.HV, args.K, args.V = H, HV, K, V
     args.num_slots = state_pool.shape[0]
-    args.flags = KDA_FLAG_L2NORM_QK if l2norm_qk else 0
+    args.flags = (KDA_FLAG_L2NORM_QK if l2norm_qk else 0) | (KDA_FLAG_CHECK_INDICES if check_indices else 0)
     args.scale = float(scale)
     args.packed_qkv, args.a, args.b = _ptr(packed_qkv), _ptr(a), _ptr(b)
     args.A_log, args.dt_bias = _ptr(A_log), _ptr(dt_bias)
@@ -284,13 +285,14 @@ def make_decode_args(packed_qkv, a, b, A_log, dt_bias, state_pool, indices, *, H
 
 
 def kda_decode_step(packed_qkv, a, b, A_log, dt_bias, state_pool, indices, *, H, HV, K, V, scale,
-                    l2norm_qk=True, o=None, err=None, stream=None):
-    """Fused T=1 decode through libkda; state_pool is updated in place. Returns o [B, HV, V] bf16."""
+                    l2norm_qk=True, o=None, err=None, stream=None, check_indices=False):
+    """Fused T=1 decode through libkda; state_pool is updated in place. Returns o [B, HV, V] bf16.
+    check_indices (needs err): a debug check that the valid slot indices are distinct."""
     lib = load()
     if o is None:
         o = torch.empty(packed_qkv.shape[0], HV, V, dtype=torch.bfloat16, device=packed_qkv.device)
     args = make_decode_args(packed_qkv, a, b, A_log, dt_bias, state_pool, indices, H=H, HV=HV, K=K, V=V,
-                            scale=scale, l2norm_qk=l2norm_qk, o=o, err=err)
+                            scale=scale, l2norm_qk=l2norm_qk, o=o, err=err, check_indices=check_indices)
     st = lib.kda_decode_step(ctypes.byref(args), _stream_ptr(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_decode_step")
@@ -298,12 +300,12 @@ def kda_decode_step(packed_qkv, a, b, A_log, dt_bias, state_pool, indices, *, H,
 
 
 def make_recurrent_args(q, k, v, a, b, A_log, dt_bias, state_pool, indices, *, scale, l2norm_qk=True,
-                        o=None, err=None):
+                        o=None, err=None, check_indices=False):
     args = RecurrentArgs()
     args.B, args.T, args.H, args.K = (int(x) for x in q.shape)
     args.HV, args.V = int(v.shape[2]), int(v.shape[3])
     args.num_slots = state_pool.shape[0]
-    args.flags = KDA_FLAG_L2NORM_QK if l2norm_qk else 0
+    args.flags = (KDA_FLAG_L2NORM_QK if l2norm_qk else 0) | (KDA_FLAG_CHECK_INDICES if check_indices else 0)
     args.scale = float(scale)
     args.q, args.k, args.v, args.a, args.b = _ptr(q), _ptr(k), _ptr(v), _ptr(a), _ptr(b)
     args.A_log, args.dt_bias = _ptr(A_log), _ptr(dt_bias)
@@ -313,14 +315,14 @@ def make_recurrent_args(q, k, v, a, b, A_log, dt_bias, state_pool, indices, *, s
 
 
 def kda_recurrent_step(q, k, v, a, b, A_log, dt_bias, state_pool, indices, *, scale, l2norm_qk=True,
-                       o=None, err=None, stream=None):
+                       o=None, err=None, stream=None, check_indices=False):
     """T tokens per row (q, k [B, T, H, K]; v [B, T, HV, V]; a [B, T, HV*K]; b [B, T, HV])
     through libkda on the slot pool, updated in place. Returns o [B, T, HV, V] bf16."""
     lib = load()
     if o is None:
         o = torch.empty(q.shape[0], q.shape[1], v.shape[2], v.shape[3], dtype=torch.bfloat16, device=q.device)
     args = make_recurrent_args(q, k, v, a, b, A_log, dt_bias, state_pool, indices, scale=scale,
-                               l2norm_qk=l2norm_qk, o=o, err=err)
+                               l2norm_qk=l2norm_qk, o=o, err=err, check_indices=check_indices)
     st = lib.kda_recurrent_step(ctypes.byref(args), _stream_ptr(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_recurrent_step")
@@ -346,7 +348,7 @@ def kda_head_rmsnorm(x, weight, *, eps, out=None, stream=None):
 
 def kda_decode_conv_step(mixed_qkv, conv_state_in, conv_weight, conv_bias, a, b, A_log, dt_bias, state_pool,
                          indices, *, H, HV, K, V, scale, conv_state_out=None, l2norm_qk=True, o=None, err=None,
-                         stream=None):
+                         stream=None, check_indices=False):
     """Decode with its causal conv1d + SiLU in front (see include/kda.h).
     mixed_qkv bf16 [B, C] is the conv input; conv_state_in bf16 [slots, W-1, C];
     conv_weight fp32 [C, W]; conv_bias fp32 [C] or None. conv_state_out defaults
@@ -357,7 +359,7 @@ def kda_decode_conv_step(mixed_qkv, conv_state_in, conv_weight, conv_bias, a, b,
         o = torch.empty(mixed_qkv.shape[0], HV, V, dtype=torch.bfloat16, device=mixed_qkv.device)
     args = DecodeConvArgs()
     args.dec = make_decode_args(mixed_qkv, a, b, A_log, dt_bias, state_pool, indices, H=H, HV=HV, K=K, V=V,
-                                scale=scale, l2norm_qk=l2norm_qk, o=o, err=err)
+                                scale=scale, l2norm_qk=l2norm_qk, o=o, err=err, check_indices=check_indices)
     args.W = int(conv_weight.shape[-1])
     args.conv_state_in = _ptr(conv_state_in)
     args.conv_state_out = _ptr(conv_state_in if conv_state_out is None else conv_state_out)

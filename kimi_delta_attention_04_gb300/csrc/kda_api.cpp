@@ -165,7 +165,8 @@ kda_status check_decode(const kda_decode_args* a, kda::DecodeCall* c) {
   if (a == nullptr) return KDA_ERR_INVALID_ARG;
   if (a->B < 0 || a->H < 1 || a->HV < 1 || a->K < 1 || a->V < 1 || a->num_slots < 0) return KDA_ERR_INVALID_ARG;
   if (a->HV % a->H != 0) return KDA_ERR_INVALID_ARG;
-  if (a->flags & ~KDA_FLAG_L2NORM_QK) return KDA_ERR_INVALID_ARG;
+  if (a->flags & ~(KDA_FLAG_L2NORM_QK | KDA_FLAG_CHECK_INDICES)) return KDA_ERR_INVALID_ARG;
+  if ((a->flags & KDA_FLAG_CHECK_INDICES) && a->err == nullptr) return KDA_ERR_INVALID_ARG;
   if (!((a->K == 64 || a->K == 128) && (a->V == 64 || a->V == 128))) return KDA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(a->B) * a->HV > INT32_MAX) return KDA_ERR_INVALID_ARG;
   if (a->B > 0) {
@@ -202,13 +203,22 @@ kda_status check_decode(const kda_decode_args* a, kda::DecodeCall* c) {
   return KDA_OK;
 }
 
+// KDA_FLAG_CHECK_INDICES: the debug check of the slot indices, ahead of the step.
+cudaError_t check_indices_if(uint32_t flags, const int32_t* idx, int B, int num_slots, int32_t* err,
+                             cudaStream_t s) {
+  if (!(flags & KDA_FLAG_CHECK_INDICES)) return cudaSuccess;
+  return kda::launch_check_indices(idx, B, num_slots, err, s);
+}
+
 }  // namespace
 
 kda_status kda_decode_step(const kda_decode_args* a, kda_stream_t stream) {
   kda::DecodeCall c;
   const kda_status st = check_decode(a, &c);
   if (st != KDA_OK) return st;
-  const cudaError_t e = kda::launch_decode(c, reinterpret_cast<cudaStream_t>(stream));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = check_indices_if(a->flags, a->indices, a->B, a->num_slots, a->err, s);
+  if (e == cudaSuccess) e = kda::launch_decode(c, s);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -231,7 +241,9 @@ kda_status kda_decode_conv_step(const kda_decode_conv_args* a, kda_stream_t stre
   c.conv_w = a->conv_weight;
   c.conv_b = a->conv_bias;
   // (without slots every row is padding or out of range: the kernel only zeroes o)
-  const cudaError_t e = kda::launch_decode(c, reinterpret_cast<cudaStream_t>(stream));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = check_indices_if(a->dec.flags, a->dec.indices, a->dec.B, a->dec.num_slots, a->dec.err, s);
+  if (e == cudaSuccess) e = kda::launch_decode(c, s);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -240,7 +252,8 @@ kda_status kda_recurrent_step(const kda_recurrent_args* a, kda_stream_t stream) 
   if (a->B < 0 || a->T < 1 || a->H < 1 || a->HV < 1 || a->K < 1 || a->V < 1 || a->num_slots < 0)
     return KDA_ERR_INVALID_ARG;
   if (a->HV % a->H != 0) return KDA_ERR_INVALID_ARG;
-  if (a->flags & ~KDA_FLAG_L2NORM_QK) return KDA_ERR_INVALID_ARG;
+  if (a->flags & ~(KDA_FLAG_L2NORM_QK | KDA_FLAG_CHECK_INDICES)) return KDA_ERR_INVALID_ARG;
+  if ((a->flags & KDA_FLAG_CHECK_INDICES) && a->err == nullptr) return KDA_ERR_INVALID_ARG;
   if (!((a->K == 64 || a->K == 128) && (a->V == 64 || a->V == 128))) return KDA_ERR_UNSUPPORTED;
   if (a->T > KDA_RECURRENT_MAX_T) return KDA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(a->B) * a->HV > INT32_MAX ||
@@ -276,7 +289,9 @@ kda_status kda_recurrent_step(const kda_recurrent_args* a, kda_stream_t stream) 
   c.indices = a->indices;
   c.o = a->o;
   c.err = a->err;
-  const cudaError_t e = kda::launch_recurrent(c, reinterpret_cast<cudaStream_t>(stream));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = check_indices_if(a->flags, a->indices, a->B, a->num_slots, a->err, s);
+  if (e == cudaSuccess) e = kda::launch_recurrent(c, s);
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -204,6 +204,8 @@ def _dec(**over):
     (dict(state_pool=None), _lib.KDA_ERR_INVALID_ARG),
     (dict(packed_qkv=FAKE + 4), _lib.KDA_ERR_INVALID_ARG),
     (dict(flags=0x2), _lib.KDA_ERR_INVALID_ARG),
+    (dict(flags=0x8), _lib.KDA_ERR_INVALID_ARG),
+    (dict(flags=_lib.KDA_FLAG_CHECK_INDICES), _lib.KDA_ERR_INVALID_ARG),  # the debug check needs err
     (dict(B=-1), _lib.KDA_ERR_INVALID_ARG),
 ])
 def test_decode_validation_rejects(lib, over, status):
@@ -232,6 +234,7 @@ def _rec(**over):
     (dict(state_pool=None), _lib.KDA_ERR_INVALID_ARG),
     (dict(v=FAKE + 4), _lib.KDA_ERR_INVALID_ARG),              # misaligned
     (dict(flags=0x2), _lib.KDA_ERR_INVALID_ARG),
+    (dict(flags=_lib.KDA_FLAG_CHECK_INDICES), _lib.KDA_ERR_INVALID_ARG),  # the debug check needs err
     (dict(B=-1), _lib.KDA_ERR_INVALID_ARG),
 ])
 def test_recurrent_validation_rejects(lib, over, status):

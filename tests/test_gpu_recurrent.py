@@ -114,3 +114,41 @@ def test_recurrent_split_tokens_equals_one_call():
     o2, pool2 = _run(second)
     assert_close("o split", np64(torch.cat([o1, o2], dim=1)), np64(o), torch.bfloat16)
     assert_close("state split", np64(pool2), np64(pool), torch.bfloat16)
+
+
+@pytest.mark.parametrize("entry", ["decode", "recurrent"])
+def test_check_indices_flag(entry):
+    """KDA_FLAG_CHECK_INDICES: a repeated valid slot index is reported through err;
+    distinct indices (pads and repeated -1s included) leave err at 0 and the
+    results as without the check."""
+    wl = W.recurrent_workload(seed=123, B=300, T=8, H=2, HV=2, K=64, V=64, num_slots=400, pad_frac=0.2)
+    B, H, HV, K, V = wl["B"], wl["H"], wl["HV"], wl["K"], wl["V"]
+
+    def call(indices, check):
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        pool = wl["state_pool"].cuda().clone()
+        if entry == "recurrent":
+            d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in wl.items()}
+            o = kda.kda_recurrent_step(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], pool,
+                                       indices.cuda(), scale=wl["scale"], err=err, check_indices=check)
+        else:
+            packed = torch.cat([wl["q"][:, 0].reshape(B, H * K), wl["k"][:, 0].reshape(B, H * K),
+                                wl["v"][:, 0].reshape(B, HV * V)], dim=1).cuda().contiguous()
+            o = kda.kda_decode_step(packed, wl["a"][:, 0].reshape(B, HV * K).cuda().contiguous(),
+                                    wl["b"][:, 0].reshape(B, HV).cuda().contiguous(), wl["A_log"].cuda(),
+                                    wl["dt_bias"].cuda(), pool, indices.cuda(), H=H, HV=HV, K=K, V=V,
+                                    scale=wl["scale"], err=err, check_indices=check)
+        torch.cuda.synchronize()
+        return int(err.item()), o, pool
+
+    idx = wl["indices"]
+    assert int((idx < 0).sum()) > 1  # several pads share -1, which is not a repeat
+    e0, o0, p0 = call(idx, False)
+    e1, o1, p1 = call(idx, True)
+    assert e0 == 0 and e1 == 0
+    assert torch.equal(o0, o1) and torch.equal(p0, p1)
+    dup = idx.clone()
+    valid = (dup >= 0).nonzero().flatten()
+    dup[valid[-1]] = dup[valid[3]]  # rows far apart (different check tiles) share a slot
+    e2, _, _ = call(dup, True)
+    assert e2 == 1

@@ -343,25 +343,50 @@ def run_gpu(args):
         torch.cuda.synchronize(dev)
         dec_graph = g0.elapsed_time(g1) / 1000.0 / K
 
-    # --- e2e through the public API with pinned host buffers ---
+    # --- e2e through the public API with pinned host buffers: every step copies
+    # its inputs in from pinned host memory and reads o and hT back. The copies run
+    # on their own streams with two device buffers each way, so step i+1's inputs
+    # travel while step i computes and step i-1's outputs travel back. ---
     host = {k: (v.pin_memory() if isinstance(v, torch.Tensor) else v) for k, v in wl.items()}
-    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    hT_h = torch.empty(hT.shape, dtype=hT.dtype).pin_memory()
     names = ("q", "k", "v", "a", "dt_bias", "A_log", "b", "h0")
+    o_hs = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for _ in range(2)]
+    hT_hs = [torch.empty(hT.shape, dtype=hT.dtype).pin_memory() for _ in range(2)]
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
-    d2h = o_h.numel() * o_h.element_size() + hT_h.numel() * hT_h.element_size()
-    e2e_steps = max(2, min(K, 5)) if args.only != "decode" else 0
-    torch.cuda.synchronize(dev)
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        dev_in = {n: host[n].to(dev, non_blocking=True) for n in names}
-        kda.kda_chunk_fwd(dev_in["q"], dev_in["k"], dev_in["v"], scale=wl["scale"], a=dev_in["a"],
-                          dt_bias=dev_in["dt_bias"], A_log=dev_in["A_log"], b=dev_in["b"], h0=dev_in["h0"],
-                          l2norm_qk=True, o=o, hT=hT, workspace=ws, stream=stream)
-        o_h.copy_(o, non_blocking=True)
-        hT_h.copy_(hT, non_blocking=True)
+    d2h = o_hs[0].numel() * o_hs[0].element_size() + hT_hs[0].numel() * hT_hs[0].element_size()
+    e2e_steps = max(4, min(K, 10)) if args.only != "decode" else 0
+    e2e_s = 0.0
+    if e2e_steps:
+        h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        dbuf = [{n: torch.empty_like(host[n], device=dev) for n in names} for _ in range(2)]
+        obuf = [torch.empty_like(o) for _ in range(2)]
+        hbuf = [torch.empty_like(hT) for _ in range(2)]
+        in_ready, in_free, out_ready, out_free = ([torch.cuda.Event() for _ in range(2)] for _ in range(4))
         torch.cuda.synchronize(dev)
-    e2e_s = (time.perf_counter() - t0) / max(e2e_steps, 1)
+        t0 = time.perf_counter()
+        for i in range(e2e_steps):
+            sl = i % 2
+            with torch.cuda.stream(h2d_stream):
+                if i >= 2:
+                    h2d_stream.wait_event(in_free[sl])
+                for n in names:
+                    dbuf[sl][n].copy_(host[n], non_blocking=True)
+                in_ready[sl].record(h2d_stream)
+            stream.wait_event(in_ready[sl])
+            if i >= 2:
+                stream.wait_event(out_free[sl])
+            di = dbuf[sl]
+            kda.kda_chunk_fwd(di["q"], di["k"], di["v"], scale=wl["scale"], a=di["a"], dt_bias=di["dt_bias"],
+                              A_log=di["A_log"], b=di["b"], h0=di["h0"], l2norm_qk=True, o=obuf[sl], hT=hbuf[sl],
+                              workspace=ws, stream=stream)
+            in_free[sl].record(stream)
+            out_ready[sl].record(stream)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(out_ready[sl])
+                o_hs[sl].copy_(obuf[sl], non_blocking=True)
+                hT_hs[sl].copy_(hbuf[sl], non_blocking=True)
+                out_free[sl].record(d2h_stream)
+        torch.cuda.synchronize(dev)
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
 
     # --- varlen prefill: 16 packed sequences (its own timed region) ---
     var = None
@@ -569,7 +594,9 @@ def run_gpu(args):
                          "traffic": stored_traffic("kda_chunk_fused_kernel", chunk_sha, T), "kernel": "kda_chunk_fused_kernel (prep + recurrence in one launch)",
                          "algorithmic_bytes": abytes, "peak_kind": peak_kind},
             "e2e": {"value": T * world / e2e_s if e2e_steps else None, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                    "note": "copies on their own streams, two buffers each way: step i+1's inputs in and step "
+                            "i-1's o and hT out while step i computes"},
             "gpu_launches": (CHUNK_LAUNCHES_PER_STEP if args.only != "decode" else 0) * K
                             + (DECODE_LAUNCHES_PER_STEP if args.only != "chunk" else 0) * K,
             "clocks": clk,

@@ -10,7 +10,7 @@ import kimi_delta_attention_04_gb300 as kda
 from kimi_delta_attention_04_gb300 import workloads as W
 from oracle import kda_oracle as ko
 
-from kda_cases import assert_close, np64, to_dev
+from kda_cases import assert_close, np64, subset_heads, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -68,3 +68,30 @@ def test_chunk_states_noalloc_matches_workspace_call():
     assert torch.equal(hc1, hc2)
     assert torch.equal(o1, o2)
     assert torch.equal(h1, h2)
+
+
+def test_chunk_states_full_size_sampled_heads():
+    """The prefill recipe at full size (B=1, H=32, T=8192) in the benchmark's
+    launch: the fused kernel's snapshot forward and output pass; the oracle
+    recomputes the per-chunk states and o of two heads (heads are independent),
+    and the output pass must give the forward's o."""
+    wl = W.prefill()
+    d = to_dev(wl)
+    nc = kda.chunk_count(1, wl["T"])
+    hc = torch.empty(nc, wl["H"], 128, 128, dtype=torch.float32, device="cuda")
+    o, hT = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], h0=d["h0"], h_chunks=hc, **_kw(d))
+    o2 = kda.kda_chunk_output(d["q"], d["k"], d["v"], hc, **_kw(d))
+    o_plain, _ = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], h0=d["h0"], **_kw(d))
+    torch.cuda.synchronize()
+    assert_close("snapshot forward vs plain forward", np64(o), np64(o_plain), torch.bfloat16)
+    heads = [2, 29]
+    sub = subset_heads(wl, heads)
+    o_ref, h_ref, s_ref = ko.kda_forward(
+        np64(sub["q"]), np64(sub["k"]), np64(sub["v"]), scale=sub["scale"], a=np64(sub["a"]),
+        dt_bias=np64(sub["dt_bias"]), A_log=np64(sub["A_log"]), b=np64(sub["b"]), h0=np64(sub["h0"]),
+        l2norm_qk=sub["l2norm"], delta=sub["delta"], chunk_states=True)
+    assert_close("full snapshots", np64(hc[:, heads]), s_ref, torch.bfloat16)
+    assert_close("full o (snapshot forward)", np64(o)[:, :, heads], o_ref, torch.bfloat16)
+    assert_close("full hT (snapshot forward)", np64(hT)[:, heads], h_ref, torch.bfloat16)
+    assert_close("full o (output pass)", np64(o2)[:, :, heads], o_ref, torch.bfloat16)
+    assert_close("output pass vs forward", np64(o2), np64(o), torch.bfloat16)

@@ -11,13 +11,14 @@
 // form ("FlashKDA里的L矩阵和Mqk矩阵": L, Mqk, the Neumann inverse, the chunk step
 // "U = INV beta (v - k_dec S); out = q_dec S + Mqk U; S = e^{g_total} S +
 // k_res^T U"), so the state work runs as mma.sync m16n8k16 with fp32
-// accumulation instead of per-token FMA loops. One CTA of V / 16 warps per
-// (row, value head):
+// accumulation instead of per-token FMA loops. One CTA of 4 warps per
+// (row, value head), four CTAs per SM:
 //  * the CTA first asks L2 for the row's 64 KiB slot (bulk prefetch), then
 //    prepares a chunk in shared memory with one thread per key channel (L2
 //    norms, decay products, the anchored level split of L and Mqk, each warp
 //    forming the inverse in registers for its columns of W and U~);
-//  * each warp owns 16 value rows of the state, S^T [16 x K] fp32 in
+//  * each warp owns V / 4 value rows of the state and steps them 16 at a
+//    time, S^T [16 x K] fp32 in
 //    registers as MMA accumulators, loaded after the chunk's preparation and
 //    stored back after its step (between chunks of a long T the rows make an
 //    L2 round trip rather than stay live across the next preparation):
@@ -36,46 +37,65 @@ namespace {
 
 constexpr int kMaxT = 64;
 
+constexpr size_t rt_max(size_t x, size_t y) { return x > y ? x : y; }
+
+// Shared memory of one CTA. Three buffers live one after another in `region`:
+// the chunk's staged inputs (until each thread has read its channel), the level
+// operands (until the L / Mqk MMAs), then -W, U~^T and the output staging
+// (through the step). Barriers separate the phases, so the CTA needs ~48 KB
+// (K = V = 128) and four fit on an SM.
 template <int K, int V, typename Q>
 struct RtcSmem {
-  // the chunk's inputs, staged by cp.async ([token][channel], rows past T zeroed)
-  __align__(16) __nv_bfloat16 in_q[16][K];
-  __align__(16) __nv_bfloat16 in_k[16][K];
-  __align__(16) __nv_bfloat16 in_a[16][K];
-  __align__(16) __nv_bfloat16 in_v[16][V];
-  // chunk preparation
-  __align__(16) Q A_lv[4][16][K + 8];  // per level: rows 0-7 k*F, rows 8-15 q*F of the row tokens
-  __align__(16) Q B_lv[4][8][K + 8];   // per level: k*F of the column tokens
+  struct In {  // [token][channel], rows past T zeroed
+    __nv_bfloat16 q[16][K];
+    __nv_bfloat16 k[16][K];
+    __nv_bfloat16 a[16][K];
+    __nv_bfloat16 v[16][V];
+  };
+  struct Lv {
+    Q A[4][16][K + 8];  // per level: rows 0-7 k*F, rows 8-15 q*F of the row tokens
+    Q B[4][8][K + 8];   // per level: k*F of the column tokens
+  };
+  struct St {
+    __nv_bfloat16 W[16][K + 8];  // -W = -(INV diag(beta) k_dec), [token][channel]
+    float ut[V][24];             // U~^T [value row][token]
+    __nv_bfloat16 ostage[16][V + 8];
+  };
+  __align__(16) unsigned char region[rt_max(sizeof(In), rt_max(sizeof(Lv), sizeof(St)))];
   __align__(16) Q kdec[16][K + 8];
   __align__(16) __nv_bfloat16 vs[16][V + 8];
-  float Lm[16][17];
-  float Mq[16][17];
-  float red[K / 32][48];
-  float rnq[16], rnk[16], beta[16];
-  // operands of the chunk step
-  __align__(16) __nv_bfloat16 W[16][K + 8];   // -W = -(INV diag(beta) k_dec), [token][channel]
   __align__(16) __nv_bfloat16 qd[16][K + 8];  // scale q e^{G}
   __align__(16) __half kr[16][K + 8];         // k e^{G_last - G}
   __align__(16) __half mqk[16][24];
   __align__(16) float gamma[K];
-  __align__(16) float ut[V][24];              // U~^T [value row][token]
-  __align__(16) __nv_bfloat16 ostage[16][V + 8];
+  float Lm[16][17];
+  float Mq[16][17];
+  float red[K / 32][48];
+  float rnq[16], rnk[16], beta[16];
+  __device__ __forceinline__ In& in() { return *reinterpret_cast<In*>(region); }
+  __device__ __forceinline__ Lv& lv() { return *reinterpret_cast<Lv*>(region); }
+  __device__ __forceinline__ St& st() { return *reinterpret_cast<St*>(region); }
 };
 
 __device__ __forceinline__ int rt_row_tok(int s, int r) { return (r / s) * 2 * s + s + (r % s); }
 __device__ __forceinline__ int rt_col_tok(int s, int r) { return (r / s) * 2 * s + (r % s); }
 
 template <int K, int V, bool L2N>
-__global__ void __launch_bounds__(V * 2, 2) kda_recurrent_tc_kernel(const RecurrentCall p) {
+__global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const RecurrentCall p) {
   using QK = std::conditional_t<L2N, F16, Bf16>;
   using Q = typename QK::T;
-  constexpr int WARPS = V / 16;
-  constexpr int NTHR = V * 2;
-  constexpr int NT = K / 8;   // n-tiles of a state row
-  constexpr int KK = K / 16;  // k-steps over the key channels
-  static_assert(NTHR >= K, "one thread per key channel");
+  constexpr int WARPS = 4;
+  constexpr int NTHR = 32 * WARPS;
+  constexpr int MT = V / (16 * WARPS);  // 16-row tiles of the state per warp
+  constexpr int NT = K / 8;             // n-tiles of a state row
+  constexpr int KK = K / 16;            // k-steps over the key channels
+  static_assert(NTHR >= K && NTHR >= V, "one thread per key and per value channel");
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  RtcSmem<K, V, Q>& sm = *reinterpret_cast<RtcSmem<K, V, Q>*>(smem_raw);
+  using Smem = RtcSmem<K, V, Q>;
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  typename Smem::In& in = sm.in();
+  typename Smem::Lv& lvo = sm.lv();
+  typename Smem::St& st = sm.st();
 
   const int T = p.T;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -113,7 +133,6 @@ __global__ void __launch_bounds__(V * 2, 2) kda_recurrent_tc_kernel(const Recurr
   const float Aexp = expf(p.A_log[hv]);
   const float dtb = kown ? p.dt_bias[hv * K + ch] : 0.f;
 
-  const int r0 = warp * 16;  // first value row of this warp
   const int nch = (T + 15) / 16;
   for (int c = 0; c < nch; ++c) {
     const int tok0 = 16 * c;
@@ -125,19 +144,19 @@ __global__ void __launch_bounds__(V * 2, 2) kda_recurrent_tc_kernel(const Recurr
         const int row = i / (K / 8), c8 = i - row * (K / 8);
         if (row < ntok) {
           const size_t qk = ((bt0 + row) * p.H + h) * K + c8 * 8;
-          cp_async16(&sm.in_q[row][c8 * 8], qb + qk);
-          cp_async16(&sm.in_k[row][c8 * 8], kb + qk);
-          cp_async16(&sm.in_a[row][c8 * 8], ab + ((bt0 + row) * p.HV + hv) * K + c8 * 8);
+          cp_async16(&in.q[row][c8 * 8], qb + qk);
+          cp_async16(&in.k[row][c8 * 8], kb + qk);
+          cp_async16(&in.a[row][c8 * 8], ab + ((bt0 + row) * p.HV + hv) * K + c8 * 8);
         } else {
-          *reinterpret_cast<uint4*>(&sm.in_q[row][c8 * 8]) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(&sm.in_k[row][c8 * 8]) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(&sm.in_a[row][c8 * 8]) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(&in.q[row][c8 * 8]) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(&in.k[row][c8 * 8]) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(&in.a[row][c8 * 8]) = make_uint4(0, 0, 0, 0);
         }
       }
       for (int i = tid; i < 16 * (V / 8); i += NTHR) {
         const int row = i / (V / 8), c8 = i - row * (V / 8);
-        if (row < ntok) cp_async16(&sm.in_v[row][c8 * 8], vb + ((bt0 + row) * p.HV + hv) * V + c8 * 8);
-        else *reinterpret_cast<uint4*>(&sm.in_v[row][c8 * 8]) = make_uint4(0, 0, 0, 0);
+        if (row < ntok) cp_async16(&in.v[row][c8 * 8], vb + ((bt0 + row) * p.HV + hv) * V + c8 * 8);
+        else *reinterpret_cast<uint4*>(&in.v[row][c8 * 8]) = make_uint4(0, 0, 0, 0);
       }
       cp_async_commit();
     }
@@ -159,9 +178,9 @@ __global__ void __launch_bounds__(V * 2, 2) kda_recurrent_tc_kernel(const Recurr
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const bool valid = i < ntok;
-        qv[i] = __bfloat162float(sm.in_q[i][ch]);
-        kv[i] = __bfloat162float(sm.in_k[i][ch]);
-        const float x = __bfloat162float(sm.in_a[i][ch]) + dtb;
+        qv[i] = __bfloat162float(in.q[i][ch]);
+        kv[i] = __bfloat162float(in.k[i][ch]);
+        const float x = __bfloat162float(in.a[i][ch]) + dtb;
         // alpha = e^{-A softplus(x)} = 2^{-A log2(1 + 2^{x log2 e})}, x itself above 20
         const float l2 = lg2_approx(1.f + ex2_approx(fminf(x, 20.f) * kLog2e));
         const float sp2 = x > 20.f ? x * kLog2e : l2;
@@ -186,7 +205,7 @@ __global__ void __launch_bounds__(V * 2, 2) kda_recurrent_tc_kernel(const Recurr
     }
     if (vown) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) sm.vs[i][tid] = sm.in_v[i][tid];
+      for (int i = 0; i < 16; ++i) sm.vs[i][tid] = in.v[i][tid];
     }
     __syncthreads();
     if (tid < 16) {
@@ -235,14 +254,14 @@ __global__ void __launch_bounds__(V * 2, 2) kda_recurrent_tc_kernel(const Recurr
           for (int i = m; i < m + s; ++i) {  // row tokens: prod_{m<t<=i} alpha_t
             if (i > m) f *= al[i];
             const int r = blk * s + (i - m);
-            sm.A_lv[lv][r][ch] = QK::cvt(kv[i] * f);
-            sm.A_lv[lv][8 + r][ch] = QK::cvt(qv[i] * f);
+            lvo.A[lv][r][ch] = QK::cvt(kv[i] * f);
+            lvo.A[lv][8 + r][ch] = QK::cvt(qv[i] * f);
           }
           f = 1.f;
 #pragma unroll
           for (int i = m - 1; i >= m - s; --i) {  // column tokens: prod_{i<t<=m} alpha_t
             f *= al[i + 1];
-            sm.B_lv[lv][blk * s + (i - (m - s))][ch] = QK::cvt(kv[i] * f);
+            lvo.B[lv][blk * s + (i - (m - s))][ch] = QK::cvt(kv[i] * f);
           }
         }
       }
@@ -255,8 +274,8 @@ __global__ void __launch_bounds__(V * 2, 2) kda_recurrent_tc_kernel(const Recurr
 #pragma unroll
       for (int kk = 0; kk < KK; ++kk) {
         uint32_t a[4], bq[2];
-        ldsm_x4(a, &sm.A_lv[lv][lane & 15][16 * kk + (lane >> 4) * 8]);
-        ldsm_x2(bq, &sm.B_lv[lv][lane & 7][16 * kk + ((lane >> 3) & 1) * 8]);
+        ldsm_x4(a, &lvo.A[lv][lane & 15][16 * kk + (lane >> 4) * 8]);
+        ldsm_x2(bq, &lvo.B[lv][lane & 7][16 * kk + ((lane >> 3) & 1) * 8]);
         mma16816<QK>(acc, a, bq[0], bq[1]);
       }
 #pragma unroll
@@ -296,10 +315,10 @@ __global__ void __launch_bounds__(V * 2, 2) kda_recurrent_tc_kernel(const Recurr
         float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
         mma16816<QK>(c0, a, bw[0], bw[1]);
         mma16816<QK>(c1, a, bw[2], bw[3]);
-        *reinterpret_cast<uint32_t*>(&sm.W[g][n0 + 2 * t]) = Bf16::pack(-c0[0], -c0[1]);
-        *reinterpret_cast<uint32_t*>(&sm.W[g + 8][n0 + 2 * t]) = Bf16::pack(-c0[2], -c0[3]);
-        *reinterpret_cast<uint32_t*>(&sm.W[g][n0 + 8 + 2 * t]) = Bf16::pack(-c1[0], -c1[1]);
-        *reinterpret_cast<uint32_t*>(&sm.W[g + 8][n0 + 8 + 2 * t]) = Bf16::pack(-c1[2], -c1[3]);
+        *reinterpret_cast<uint32_t*>(&st.W[g][n0 + 2 * t]) = Bf16::pack(-c0[0], -c0[1]);
+        *reinterpret_cast<uint32_t*>(&st.W[g + 8][n0 + 2 * t]) = Bf16::pack(-c0[2], -c0[3]);
+        *reinterpret_cast<uint32_t*>(&st.W[g][n0 + 8 + 2 * t]) = Bf16::pack(-c1[0], -c1[1]);
+        *reinterpret_cast<uint32_t*>(&st.W[g + 8][n0 + 8 + 2 * t]) = Bf16::pack(-c1[2], -c1[3]);
       }
       for (int blk = warp; blk < V / 16; blk += WARPS) {  // U~ (fp32 through a hi/lo split), 16 value channels
         const int n0 = 16 * blk;
@@ -310,117 +329,122 @@ __global__ void __launch_bounds__(V * 2, 2) kda_recurrent_tc_kernel(const Recurr
         mma16816<Bf16>(u0, alo, bv[0], bv[1]);
         mma16816<Bf16>(u1, ahi, bv[2], bv[3]);
         mma16816<Bf16>(u1, alo, bv[2], bv[3]);
-        sm.ut[n0 + 2 * t][g] = u0[0];
-        sm.ut[n0 + 2 * t + 1][g] = u0[1];
-        sm.ut[n0 + 2 * t][g + 8] = u0[2];
-        sm.ut[n0 + 2 * t + 1][g + 8] = u0[3];
-        sm.ut[n0 + 8 + 2 * t][g] = u1[0];
-        sm.ut[n0 + 8 + 2 * t + 1][g] = u1[1];
-        sm.ut[n0 + 8 + 2 * t][g + 8] = u1[2];
-        sm.ut[n0 + 8 + 2 * t + 1][g + 8] = u1[3];
-      }
-    }
-    float S[NT][4];
-    {  // the state, in the accumulator layout (its lines are in L2 by now)
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const float2 x = __ldcs(reinterpret_cast<const float2*>(S_slot + (r0 + g) * K + 8 * nt + 2 * t));
-        const float2 y = __ldcs(reinterpret_cast<const float2*>(S_slot + (r0 + g + 8) * K + 8 * nt + 2 * t));
-        S[nt][0] = x.x; S[nt][1] = x.y; S[nt][2] = y.x; S[nt][3] = y.y;
+        st.ut[n0 + 2 * t][g] = u0[0];
+        st.ut[n0 + 2 * t + 1][g] = u0[1];
+        st.ut[n0 + 2 * t][g + 8] = u0[2];
+        st.ut[n0 + 2 * t + 1][g + 8] = u0[3];
+        st.ut[n0 + 8 + 2 * t][g] = u1[0];
+        st.ut[n0 + 8 + 2 * t + 1][g] = u1[1];
+        st.ut[n0 + 8 + 2 * t][g + 8] = u1[2];
+        st.ut[n0 + 8 + 2 * t + 1][g + 8] = u1[3];
       }
     }
     __syncthreads();
 
-    // ---------------- chunk step on this warp's 16 value rows ----------------
-    float u[2][4], u2[2][4], o[2][4];
+    // ---------------- chunk step, one 16-row tile of the state at a time ----------------
+#pragma unroll 1
+    for (int mt = 0; mt < MT; ++mt) {
+      const int r0 = (warp + WARPS * mt) * 16;  // first value row of the tile
+      float S[NT][4];
+      {  // the state, in the accumulator layout (its lines are in L2 by now)
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const float2 x = *reinterpret_cast<const float2*>(&sm.ut[r0 + g][8 * nt + 2 * t]);
-      const float2 y = *reinterpret_cast<const float2*>(&sm.ut[r0 + g + 8][8 * nt + 2 * t]);
-      u[nt][0] = x.x; u[nt][1] = x.y; u[nt][2] = y.x; u[nt][3] = y.y;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) { u2[nt][e] = 0.f; o[nt][e] = 0.f; }
-    }
-    // U^T = U~^T + S^T (-W)^T ; O^T = S^T q_dec^T (S^T as bf16 A fragments, one
-    // k-step at a time: the accumulator layout of two n-tiles is the A layout)
-#pragma unroll
-    for (int kk = 0; kk < KK; ++kk) {
-      uint32_t sa[4];
-      sa[0] = Bf16::pack(S[2 * kk][0], S[2 * kk][1]);
-      sa[1] = Bf16::pack(S[2 * kk][2], S[2 * kk][3]);
-      sa[2] = Bf16::pack(S[2 * kk + 1][0], S[2 * kk + 1][1]);
-      sa[3] = Bf16::pack(S[2 * kk + 1][2], S[2 * kk + 1][3]);
-      const int row = ((lane >> 4) << 3) + (lane & 7);
-      const int col = 16 * kk + ((lane >> 3) & 1) * 8;
-      uint32_t bm[4];
-      ldsm_x4(bm, &sm.W[row][col]);
-      float (&acc)[2][4] = (kk & 1) ? u2 : u;
-      mma16816<Bf16>(acc[0], sa, bm[0], bm[1]);
-      mma16816<Bf16>(acc[1], sa, bm[2], bm[3]);
-      ldsm_x4(bm, &sm.qd[row][col]);
-      mma16816<Bf16>(o[0], sa, bm[0], bm[1]);
-      mma16816<Bf16>(o[1], sa, bm[2], bm[3]);
-    }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) u[nt][e] += u2[nt][e];
-    uint32_t ua[4];
-    ua[0] = F16::pack(u[0][0], u[0][1]);
-    ua[1] = F16::pack(u[0][2], u[0][3]);
-    ua[2] = F16::pack(u[1][0], u[1][1]);
-    ua[3] = F16::pack(u[1][2], u[1][3]);
-    // S^T = S^T diag(gamma) + U^T k_res
-#pragma unroll
-    for (int np = 0; np < KK; ++np) {
-      uint32_t bm[4];
-      ldsm_x4_trans(bm, &sm.kr[lane & 15][16 * np + (lane >> 4) * 8]);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int nt = 2 * np + half;
-        const float2 gm = *reinterpret_cast<const float2*>(&sm.gamma[8 * nt + 2 * t]);
-        S[nt][0] *= gm.x; S[nt][1] *= gm.y; S[nt][2] *= gm.x; S[nt][3] *= gm.y;
-        mma16816<F16>(S[nt], ua, bm[2 * half], bm[2 * half + 1]);
+        for (int nt = 0; nt < NT; ++nt) {
+          const float2 x = __ldcs(reinterpret_cast<const float2*>(S_slot + (r0 + g) * K + 8 * nt + 2 * t));
+          const float2 y = __ldcs(reinterpret_cast<const float2*>(S_slot + (r0 + g + 8) * K + 8 * nt + 2 * t));
+          S[nt][0] = x.x; S[nt][1] = x.y; S[nt][2] = y.x; S[nt][3] = y.y;
+        }
       }
-    }
-    // O^T += U^T Mqk^T
-    {
-      uint32_t bm[4];
-      const int row = ((lane >> 4) << 3) + (lane & 7);
-      ldsm_x4(bm, &sm.mqk[row][((lane >> 3) & 1) * 8]);
-      mma16816<F16>(o[0], ua, bm[0], bm[1]);
-      mma16816<F16>(o[1], ua, bm[2], bm[3]);
-    }
+
+      float u[2][4], u2[2][4], o[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const int tok = 8 * nt + 2 * t;
-      sm.ostage[tok][r0 + g] = __float2bfloat16_rn(o[nt][0]);
-      sm.ostage[tok + 1][r0 + g] = __float2bfloat16_rn(o[nt][1]);
-      sm.ostage[tok][r0 + g + 8] = __float2bfloat16_rn(o[nt][2]);
-      sm.ostage[tok + 1][r0 + g + 8] = __float2bfloat16_rn(o[nt][3]);
+      for (int nt = 0; nt < 2; ++nt) {
+        const float2 x = *reinterpret_cast<const float2*>(&st.ut[r0 + g][8 * nt + 2 * t]);
+        const float2 y = *reinterpret_cast<const float2*>(&st.ut[r0 + g + 8][8 * nt + 2 * t]);
+        u[nt][0] = x.x; u[nt][1] = x.y; u[nt][2] = y.x; u[nt][3] = y.y;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) { u2[nt][e] = 0.f; o[nt][e] = 0.f; }
+      }
+      // U^T = U~^T + S^T (-W)^T ; O^T = S^T q_dec^T (S^T as bf16 A fragments, one
+      // k-step at a time: the accumulator layout of two n-tiles is the A layout)
+#pragma unroll
+      for (int kk = 0; kk < KK; ++kk) {
+        uint32_t sa[4];
+        sa[0] = Bf16::pack(S[2 * kk][0], S[2 * kk][1]);
+        sa[1] = Bf16::pack(S[2 * kk][2], S[2 * kk][3]);
+        sa[2] = Bf16::pack(S[2 * kk + 1][0], S[2 * kk + 1][1]);
+        sa[3] = Bf16::pack(S[2 * kk + 1][2], S[2 * kk + 1][3]);
+        const int row = ((lane >> 4) << 3) + (lane & 7);
+        const int col = 16 * kk + ((lane >> 3) & 1) * 8;
+        uint32_t bm[4];
+        ldsm_x4(bm, &st.W[row][col]);
+        float (&acc)[2][4] = (kk & 1) ? u2 : u;
+        mma16816<Bf16>(acc[0], sa, bm[0], bm[1]);
+        mma16816<Bf16>(acc[1], sa, bm[2], bm[3]);
+        ldsm_x4(bm, &sm.qd[row][col]);
+        mma16816<Bf16>(o[0], sa, bm[0], bm[1]);
+        mma16816<Bf16>(o[1], sa, bm[2], bm[3]);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) u[nt][e] += u2[nt][e];
+      uint32_t ua[4];
+      ua[0] = F16::pack(u[0][0], u[0][1]);
+      ua[1] = F16::pack(u[0][2], u[0][3]);
+      ua[2] = F16::pack(u[1][0], u[1][1]);
+      ua[3] = F16::pack(u[1][2], u[1][3]);
+      // S^T = S^T diag(gamma) + U^T k_res
+#pragma unroll
+      for (int np = 0; np < KK; ++np) {
+        uint32_t bm[4];
+        ldsm_x4_trans(bm, &sm.kr[lane & 15][16 * np + (lane >> 4) * 8]);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          const int nt = 2 * np + half;
+          const float2 gm = *reinterpret_cast<const float2*>(&sm.gamma[8 * nt + 2 * t]);
+          S[nt][0] *= gm.x; S[nt][1] *= gm.y; S[nt][2] *= gm.x; S[nt][3] *= gm.y;
+          mma16816<F16>(S[nt], ua, bm[2 * half], bm[2 * half + 1]);
+        }
+      }
+      // O^T += U^T Mqk^T
+      {
+        uint32_t bm[4];
+        const int row = ((lane >> 4) << 3) + (lane & 7);
+        ldsm_x4(bm, &sm.mqk[row][((lane >> 3) & 1) * 8]);
+        mma16816<F16>(o[0], ua, bm[0], bm[1]);
+        mma16816<F16>(o[1], ua, bm[2], bm[3]);
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int tok = 8 * nt + 2 * t;
+        st.ostage[tok][r0 + g] = __float2bfloat16_rn(o[nt][0]);
+        st.ostage[tok + 1][r0 + g] = __float2bfloat16_rn(o[nt][1]);
+        st.ostage[tok][r0 + g + 8] = __float2bfloat16_rn(o[nt][2]);
+        st.ostage[tok + 1][r0 + g + 8] = __float2bfloat16_rn(o[nt][3]);
+      }
+      // The tile goes back to its slot after every chunk (each warp rereads only
+      // its own rows, after the next chunk's preparation): between chunks it is
+      // an L2 round trip instead of registers held across the preparation.
+      if (c + 1 < nch) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          __stcg(reinterpret_cast<float2*>(S_slot + (r0 + g) * K + 8 * nt + 2 * t), make_float2(S[nt][0], S[nt][1]));
+          __stcg(reinterpret_cast<float2*>(S_slot + (r0 + g + 8) * K + 8 * nt + 2 * t), make_float2(S[nt][2], S[nt][3]));
+        }
+      } else {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          __stcs(reinterpret_cast<float2*>(S_slot + (r0 + g) * K + 8 * nt + 2 * t), make_float2(S[nt][0], S[nt][1]));
+          __stcs(reinterpret_cast<float2*>(S_slot + (r0 + g + 8) * K + 8 * nt + 2 * t), make_float2(S[nt][2], S[nt][3]));
+        }
+      }
     }
     __syncthreads();
     for (int i = tid; i < ntok * (V / 8); i += NTHR) {
       const int row = i / (V / 8), v8 = i - row * (V / 8);
       __nv_bfloat16* dst =
           reinterpret_cast<__nv_bfloat16*>(p.o) + ((static_cast<size_t>(b) * T + tok0 + row) * p.HV + hv) * V + v8 * 8;
-      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&sm.ostage[row][v8 * 8]);
-    }
-    // The state goes back to its slot after every chunk (each warp rereads only
-    // its own rows, after the next chunk's preparation): between chunks it is
-    // an L2 round trip instead of registers held across the preparation.
-    if (c + 1 < nch) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        __stcg(reinterpret_cast<float2*>(S_slot + (r0 + g) * K + 8 * nt + 2 * t), make_float2(S[nt][0], S[nt][1]));
-        __stcg(reinterpret_cast<float2*>(S_slot + (r0 + g + 8) * K + 8 * nt + 2 * t), make_float2(S[nt][2], S[nt][3]));
-      }
-    } else {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        __stcs(reinterpret_cast<float2*>(S_slot + (r0 + g) * K + 8 * nt + 2 * t), make_float2(S[nt][0], S[nt][1]));
-        __stcs(reinterpret_cast<float2*>(S_slot + (r0 + g + 8) * K + 8 * nt + 2 * t), make_float2(S[nt][2], S[nt][3]));
-      }
+      *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&st.ostage[row][v8 * 8]);
     }
     __syncthreads();  // the next chunk's preparation reuses every buffer above
   }
@@ -438,7 +462,7 @@ cudaError_t launch_rtc_t(const RecurrentCall& c, cudaStream_t s) {
     attr = true;
   }
   const unsigned grid = static_cast<unsigned>(c.B) * static_cast<unsigned>(c.HV);
-  kda_recurrent_tc_kernel<K, V, L2N><<<grid, V * 2, smem, s>>>(c);
+  kda_recurrent_tc_kernel<K, V, L2N><<<grid, 128, smem, s>>>(c);
   return cudaGetLastError();
 }
 

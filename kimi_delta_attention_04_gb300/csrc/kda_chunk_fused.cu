@@ -6,14 +6,15 @@
 // split across CTAs as in "TileLang 实战：KDA 从零到一" §6.4). What changes is the
 // placement:
 //
-//  * CTA r of the cluster owns value rows [32r, 32r + 32) of the state. Its four
-//    recurrence warps are (16-row block) x (half of the key channels): each holds
-//    S^T[16 x 64] fp32 in registers as mma.sync accumulators. The U^T partial
-//    sums of the two key halves are exchanged through shared memory once per
-//    chunk (split-K), which halves the serial MMA chain per warp. Each warp's
-//    O^T partial (q_dec S over its key half, plus U^T Mqk^T on the first half)
-//    is computed behind the state update and staged in shared memory; an
-//    output warp adds the halves and stores o, off the serial path.
+//  * CTA r of the cluster owns value rows [32r, 32r + 32) of the state. Each of
+//    its four recurrence warps owns 8 of those value columns and all 128 key
+//    rows: S [128 x 8] fp32 in registers as eight m16n8 mma.sync accumulators,
+//    so every contraction over the keys stays inside the warp (no exchange
+//    between warps on the serial path). S and U reach the B-operand layout by
+//    movmatrix transposes of their accumulators; -W, q_dec and k_res are A
+//    operands loaded from the channel-major tiles. Each warp's O (q_dec S +
+//    Mqk U) is computed behind the state update and staged in shared memory;
+//    an output warp stores o, off the serial path.
 //  * The same CTA's prep warps prepare every 4th chunk (chunks c = r mod 4):
 //    gate, beta, L2 norm, decay products, L / Mqk, Neumann inverse, W and U~.
 //    Two groups of four warps take alternate ones, each loading its next
@@ -104,11 +105,10 @@ struct __align__(16) PrepScratch {
   float ghead[16];  // per-head log-decay of the chunk's tokens (KDA_GATE_HEAD_G)
 };
 
-constexpr int kOPitch = kRows + 4;  // padded row of an output partial (conflict-free both ways)
+constexpr int kOPitch = kRows + 4;  // padded row of the staged output (conflict-free reads)
 
 struct __align__(16) RecScratch {
-  float xch[2][2][2][32][8];              // [chunk parity][row block][key half][lane]: U^T partials
-  float opart[kRing][2][16][kOPitch];     // [stage][key half][token][value row]: O partials
+  float opart[kRing][16][kOPitch];  // [stage][token][value row]: O of the stage's chunk
 };
 
 template <typename Q>
@@ -226,20 +226,49 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
 
   if (warp < 4) {
     // ===================== recurrence warps =====================
-    const int dvb = warp >> 1, dkh = warp & 1;
+    // Warp w owns value columns [dv0, dv0 + 8) of the CTA's 32 and all 128 key
+    // rows: S [d_k x 8] fp32 as eight m16n8 accumulators, S[mi] = key rows
+    // 16 mi .. 16 mi + 15. Every contraction over d_k is then inside the warp.
     const int g = lane >> 2, t = lane & 3;
-    const int row0 = static_cast<int>(rank) * kRows + dvb * 16;  // first value row of this warp
-    const int kc0 = dkh * 64;                                    // first key channel of this warp
+    const int dvl = warp * 8;                                 // first value column within the CTA
+    const int dv0 = static_cast<int>(rank) * kRows + dvl;    // first value row of the stored state
+    // ldmatrix row addresses: A fragments [token][key] of a channel-major tile
+    // ([key][16 tokens]) come from .trans loads with lane matrix m = (key half
+    // m >> 1, token half m & 1); A fragments [key][token] (k_res^T) from plain
+    // loads with m = (key half m & 1, token half m >> 1).
+    const int at_row = (lane >> 4) * 8 + (lane & 7), at_half = (lane >> 3) & 1;
+    const int ak_row = ((lane >> 3) & 1) * 8 + (lane & 7), ak_half = lane >> 4;
+    const int mq_row = ((lane >> 3) & 1) * 8 + (lane & 7), mq_col = (lane >> 4) * 8;
     // Output pass: no recurrence; S holds the next chunk's entering state,
     // loaded from h_chunks one chunk ahead of its use.
     constexpr bool outp = MODE == 2;
     float S[8][4];
+    // element (key 16 mi + g (+8), value dv0 + 2t (+1)) of a stored [dv][dk] state
     auto load_state = [&](const float* src) {
+      const float* b0 = src + static_cast<size_t>(dv0 + 2 * t) * FD + g;
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const float2 x = __ldcs(reinterpret_cast<const float2*>(src + (row0 + g) * FD + kc0 + 8 * nt + 2 * t));
-        const float2 y = __ldcs(reinterpret_cast<const float2*>(src + (row0 + g + 8) * FD + kc0 + 8 * nt + 2 * t));
-        S[nt][0] = x.x; S[nt][1] = x.y; S[nt][2] = y.x; S[nt][3] = y.y;
+      for (int mi = 0; mi < 8; ++mi) {
+        S[mi][0] = __ldcs(b0 + 16 * mi);
+        S[mi][1] = __ldcs(b0 + FD + 16 * mi);
+        S[mi][2] = __ldcs(b0 + 16 * mi + 8);
+        S[mi][3] = __ldcs(b0 + FD + 16 * mi + 8);
+      }
+    };
+    auto store_state = [&](float* dst, bool streaming) {
+      float* b0 = dst + static_cast<size_t>(dv0 + 2 * t) * FD + g;
+#pragma unroll
+      for (int mi = 0; mi < 8; ++mi) {
+        if (streaming) {
+          __stcs(b0 + 16 * mi, S[mi][0]);
+          __stcs(b0 + FD + 16 * mi, S[mi][1]);
+          __stcs(b0 + 16 * mi + 8, S[mi][2]);
+          __stcs(b0 + FD + 16 * mi + 8, S[mi][3]);
+        } else {
+          b0[16 * mi] = S[mi][0];
+          b0[FD + 16 * mi] = S[mi][1];
+          b0[16 * mi + 8] = S[mi][2];
+          b0[FD + 16 * mi + 8] = S[mi][3];
+        }
       }
     };
     auto snapshot = [&](int cc) { return p.h_chunks + (static_cast<size_t>(cb + cc) * H + h) * FD * FD; };
@@ -247,151 +276,88 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       load_state(outp ? snapshot(0) : p.h0 + (static_cast<size_t>(n) * H + h) * FD * FD);
     } else {
 #pragma unroll
-      for (int nt = 0; nt < 8; ++nt) S[nt][0] = S[nt][1] = S[nt][2] = S[nt][3] = 0.f;
+      for (int mi = 0; mi < 8; ++mi) S[mi][0] = S[mi][1] = S[mi][2] = S[mi][3] = 0.f;
     }
     bool failed = false;
-    // O^T partial of the previous chunk, handed to the output warp once the
-    // next chunk's U^T MMAs are issued (its MMAs have completed by then)
-    float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // O of the previous chunk, handed to the output warp once the next chunk's
+    // U MMAs are issued (its MMAs have completed by then)
+    float o[4] = {0.f, 0.f, 0.f, 0.f};
     auto post_output = [&](int cc) {
-      float (*op)[kOPitch] = sm.rs.opart[cc & (kRing - 1)][dkh];
-      const int r = dvb * 16 + g;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        const int tok = 8 * nt + 2 * t;
-        op[tok][r] = o[nt][0];
-        op[tok + 1][r] = o[nt][1];
-        op[tok][r + 8] = o[nt][2];
-        op[tok + 1][r + 8] = o[nt][3];
-      }
+      float (*op)[kOPitch] = sm.rs.opart[cc & (kRing - 1)];
+      *reinterpret_cast<float2*>(&op[g][dvl + 2 * t]) = make_float2(o[0], o[1]);
+      *reinterpret_cast<float2*>(&op[g + 8][dvl + 2 * t]) = make_float2(o[2], o[3]);
       __syncwarp();
       if (lane == 0) mbar_arrive_local(&sm.ofull[cc & (kRing - 1)]);
     };
-    const int brow = ((lane >> 4) << 3) + (lane & 7);
-    const int bcol = ((lane >> 3) & 1) * 8;
-    // ldmatrix rows of the channel-major tiles. B fragments of a [K][N]-stored
-    // operand (W^T, q_dec^T: K = channel) come from .trans loads, lane matrix m =
-    // (n-tile m >> 1, k half m & 1); those of an [N][K]-stored one (k_res^T:
-    // N = channel) from plain loads, m = (n-tile m >> 1, token half m & 1).
-    const int tm_row = ((lane >> 3) & 1) * 8 + (lane & 7), tm_half = lane >> 4;
-    const int nm_row = (lane >> 4) * 8 + (lane & 7), nm_half = (lane >> 3) & 1;
-    uint32_t sa[4][4];  // S^T of this warp in bf16 A fragments
+    uint32_t sb[8][2];  // S as bf16 B fragments [key][value], one pair per k-step
     auto pack_state = [&] {
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        sa[kk][0] = Bf16::pack(S[2 * kk][0], S[2 * kk][1]);
-        sa[kk][1] = Bf16::pack(S[2 * kk][2], S[2 * kk][3]);
-        sa[kk][2] = Bf16::pack(S[2 * kk + 1][0], S[2 * kk + 1][1]);
-        sa[kk][3] = Bf16::pack(S[2 * kk + 1][2], S[2 * kk + 1][3]);
+      for (int kk = 0; kk < 8; ++kk) {
+        sb[kk][0] = movmatrix_trans(Bf16::pack(S[kk][0], S[kk][1]));
+        sb[kk][1] = movmatrix_trans(Bf16::pack(S[kk][2], S[kk][3]));
       }
     };
+    pack_state();
     // this CTA's 32 value rows of chunk cc's state: one contiguous 16 KB slab, pulled
     // into L2 kSnapAhead chunks before its loads
     constexpr int kSnapAhead = 4;
     auto prefetch_state = [&](int cc) {
       if (warp == 0 && lane == 0 && cc < nch) bulk_prefetch_l2(snapshot(cc) + rank * kRows * FD, kRows * FD * 4);
     };
-    pack_state();
     if (outp) {
       for (int cc = 2; cc < 2 + kSnapAhead; ++cc) prefetch_state(cc);
       if (nch > 1) load_state(snapshot(1));
     }
-    float* const snap = MODE != 1 ? nullptr
-                                  : p.h_chunks + (static_cast<size_t>(cb) * H + h) * FD * FD + (row0 + g) * FD + kc0 + 2 * t;
     for (int c = 0; c < nch; ++c) {
       const int s = c & (kRing - 1);
       const uint32_t par = static_cast<uint32_t>(c / kRing) & 1u;
-      if (MODE == 1) {  // the state entering chunk c, before its decay (streaming stores)
-        float* dst = snap + static_cast<size_t>(c) * H * FD * FD;
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-          __stcs(reinterpret_cast<float2*>(dst + 8 * nt), make_float2(S[nt][0], S[nt][1]));
-          __stcs(reinterpret_cast<float2*>(dst + 8 * FD + 8 * nt), make_float2(S[nt][2], S[nt][3]));
-        }
-      }
+      if (MODE == 1) store_state(snapshot(c), true);  // the state entering chunk c, before its decay
       if (!failed && !mbar_wait_bounded(smem_u32(&sm.full[s]), par, kWaitLimitNs)) {
         failed = true;
         if (lane == 0) set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
       }
       const Stage& st = sm.ring[s];
-      float u[2][4];
+      // U = U~ + (-W) S over all keys (the serial path), two accumulator chains
+      float u[4], u2[4] = {0.f, 0.f, 0.f, 0.f};
+      u[0] = st.ut[dvl + 2 * t][g];
+      u[1] = st.ut[dvl + 2 * t + 1][g];
+      u[2] = st.ut[dvl + 2 * t][g + 8];
+      u[3] = st.ut[dvl + 2 * t + 1][g + 8];
+      if (DELTA) {
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        if (dkh == 0) {
-          const float2 x = *reinterpret_cast<const float2*>(&st.ut[dvb * 16 + g][8 * nt + 2 * t]);
-          const float2 y = *reinterpret_cast<const float2*>(&st.ut[dvb * 16 + g + 8][8 * nt + 2 * t]);
-          u[nt][0] = x.x; u[nt][1] = x.y; u[nt][2] = y.x; u[nt][3] = y.y;
-        } else {
-          u[nt][0] = u[nt][1] = u[nt][2] = u[nt][3] = 0.f;
-        }
-      }
-      if (DELTA) {  // U^T partial over this key half: the serial path; two chains per n-tile
-        float u2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        uint32_t b[4][4];
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) ldsm_x4_trans(b[kk], &st.W[0][0] + cm_off(kc0 + 16 * kk + tm_row, tm_half));
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          float (&acc)[2][4] = (kk & 1) ? u2 : u;
-          mma16816<Bf16>(acc[0], sa[kk], b[kk][0], b[kk][1]);
-          mma16816<Bf16>(acc[1], sa[kk], b[kk][2], b[kk][3]);
+        for (int kk = 0; kk < 8; ++kk) {
+          uint32_t a[4];
+          ldsm_x4_trans(a, &st.W[0][0] + cm_off(16 * kk + at_row, at_half));
+          mma16816<Bf16>((kk & 1) ? u2 : u, a, sb[kk][0], sb[kk][1]);
         }
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) u[nt][e] += u2[nt][e];
+        for (int e = 0; e < 4; ++e) u[e] += u2[e];
       }
       if (c > 0) post_output(c - 1);
-      // operands of the state update, independent of U: loaded while U settles
-      uint32_t krb[4][4];
-      if (!outp) {
+      // U as B fragments [token][value]
+      const uint32_t ub0 = movmatrix_trans(ST2::pack(u[0], u[1]));
+      const uint32_t ub1 = movmatrix_trans(ST2::pack(u[2], u[3]));
+      // S = diag(gamma) S + k_res^T U, key rows 16 mi .. 16 mi + 15 at a time
 #pragma unroll
-        for (int np = 0; np < 4; ++np) ldsm_x4(krb[np], &st.kr[0][0] + cm_off(kc0 + 16 * np + nm_row, nm_half));
+      for (int mi = 0; mi < (outp ? 0 : 8); ++mi) {
+        uint32_t a[4];
+        ldsm_x4(a, &st.kr[0][0] + cm_off(16 * mi + ak_row, ak_half));
+        const float g0 = st.gamma[16 * mi + g], g1 = st.gamma[16 * mi + g + 8];
+        S[mi][0] *= g0; S[mi][1] *= g0; S[mi][2] *= g1; S[mi][3] *= g1;
+        mma16816<ST2>(S[mi], a, ub0, ub1);
       }
-      // Exchange the two key halves' U^T partial sums (split-K).
+      // O = q_dec S_old + Mqk U behind the state update in the tensor pipe
+      o[0] = o[1] = o[2] = o[3] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        uint32_t a[4];
+        ldsm_x4_trans(a, &st.qd[0][0] + cm_off(16 * kk + at_row, at_half));
+        mma16816<Bf16>(o, a, sb[kk][0], sb[kk][1]);
+      }
       {
-        float* mine = sm.rs.xch[c & 1][dvb][dkh][lane];
-        *reinterpret_cast<float4*>(mine + 0) = make_float4(u[0][0], u[0][1], u[0][2], u[0][3]);
-        *reinterpret_cast<float4*>(mine + 4) = make_float4(u[1][0], u[1][1], u[1][2], u[1][3]);
-        named_bar_sync(2 + dvb, 64);
-        const float* other = sm.rs.xch[c & 1][dvb][dkh ^ 1][lane];
-        const float4 a0 = *reinterpret_cast<const float4*>(other + 0);
-        const float4 a1 = *reinterpret_cast<const float4*>(other + 4);
-        u[0][0] += a0.x; u[0][1] += a0.y; u[0][2] += a0.z; u[0][3] += a0.w;
-        u[1][0] += a1.x; u[1][1] += a1.y; u[1][2] += a1.z; u[1][3] += a1.w;
-      }
-      uint32_t ua[4];
-      ua[0] = ST2::pack(u[0][0], u[0][1]);
-      ua[1] = ST2::pack(u[0][2], u[0][3]);
-      ua[2] = ST2::pack(u[1][0], u[1][1]);
-      ua[3] = ST2::pack(u[1][2], u[1][3]);
-      // state update on this warp's key half: S^T = S^T diag(gamma) + U^T k_res
-#pragma unroll
-      for (int np = 0; np < (outp ? 0 : 4); ++np) {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int nt = 2 * np + half;
-          const float2 gm = *reinterpret_cast<const float2*>(&st.gamma[kc0 + 8 * nt + 2 * t]);
-          S[nt][0] *= gm.x; S[nt][1] *= gm.y; S[nt][2] *= gm.x; S[nt][3] *= gm.y;
-          mma16816<ST2>(S[nt], ua, krb[np][2 * half], krb[np][2 * half + 1]);
-        }
-      }
-      // O^T of this chunk behind the state update in the tensor pipe: q_dec S_old
-      // over this key half (S_old is still in sa), plus U^T Mqk^T on the first half
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        uint32_t b[4];
-        ldsm_x4_trans(b, &st.qd[0][0] + cm_off(kc0 + 16 * kk + tm_row, tm_half));
-        mma16816<Bf16>(o[0], sa[kk], b[0], b[1]);
-        mma16816<Bf16>(o[1], sa[kk], b[2], b[3]);
-      }
-      if (dkh == 0) {
-        uint32_t b[4];
-        ldsm_x4(b, &st.mqk[brow][bcol]);
-        mma16816<ST2>(o[0], ua, b[0], b[1]);
-        mma16816<ST2>(o[1], ua, b[2], b[3]);
+        uint32_t a[4];
+        ldsm_x4(a, &st.mqk[mq_row][mq_col]);
+        mma16816<ST2>(o, a, ub0, ub1);
       }
       pack_state();
       if (outp) {
@@ -402,15 +368,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       if (lane == 0) mbar_arrive_local(&sm.empty[s]);
     }
     if (nch > 0) post_output(nch - 1);
-    if (ok && p.hT != nullptr && !outp) {
-      float* dst = p.hT + (static_cast<size_t>(n) * H + h) * FD * FD;
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        *reinterpret_cast<float2*>(dst + (row0 + g) * FD + kc0 + 8 * nt + 2 * t) = make_float2(S[nt][0], S[nt][1]);
-        *reinterpret_cast<float2*>(dst + (row0 + g + 8) * FD + kc0 + 8 * nt + 2 * t) =
-            make_float2(S[nt][2], S[nt][3]);
-      }
-    }
+    if (ok && p.hT != nullptr && !outp) store_state(p.hT + (static_cast<size_t>(n) * H + h) * FD * FD, false);
   } else if (warp < 12) {
     // ===================== prep warps =====================
     // Chunk c is prepared in shared memory (pout), then copied into global slot
@@ -789,8 +747,8 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     }
   } else {
     // ===================== output warp =====================
-    // Adds the two key halves' O partials of each chunk, stores the chunk's
-    // 16 x 32 block of o (lane: one token, 16 value rows) and releases the stage.
+    // Stores each chunk's 16 x 32 block of o (lane: one token, 16 value rows)
+    // from the staged O and releases the stage.
     const int tok = lane >> 1, hv = lane & 1;
     bool failed = false;
     for (int c = 0; c < nch; ++c) {
@@ -800,15 +758,13 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         failed = true;
         if (lane == 0) set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
       }
-      const float* p0 = &sm.rs.opart[s][0][tok][hv * 16];
-      const float* p1 = &sm.rs.opart[s][1][tok][hv * 16];
+      const float* p0 = &sm.rs.opart[s][tok][hv * 16];
       uint32_t pk[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float4 x = *reinterpret_cast<const float4*>(p0 + 4 * i);
-        const float4 y = *reinterpret_cast<const float4*>(p1 + 4 * i);
-        pk[2 * i] = Bf16::pack(x.x + y.x, x.y + y.y);
-        pk[2 * i + 1] = Bf16::pack(x.z + y.z, x.w + y.w);
+        pk[2 * i] = Bf16::pack(x.x, x.y);
+        pk[2 * i + 1] = Bf16::pack(x.z, x.w);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive_local(&sm.empty[s]);

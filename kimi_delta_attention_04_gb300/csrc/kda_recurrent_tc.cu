@@ -53,8 +53,8 @@ struct RtcSmem {
     __nv_bfloat16 v[16][V];
   };
   struct Lv {
-    Q A[4][16][K + 8];  // per level: rows 0-7 k*F, rows 8-15 q*F of the row tokens
-    Q B[4][8][K + 8];   // per level: k*F of the column tokens
+    Q A[4][K][16];  // per level, channel-major: rows 0-7 k*F, rows 8-15 q*F of the row tokens
+    Q B[4][K][8];   // per level, channel-major: k*F of the column tokens
   };
   struct St {
     __nv_bfloat16 W[16][K + 8];  // -W = -(INV diag(beta) k_dec), [token][channel]
@@ -62,10 +62,11 @@ struct RtcSmem {
     __nv_bfloat16 ostage[16][V + 8];
   };
   __align__(16) unsigned char region[rt_max(sizeof(In), rt_max(sizeof(Lv), sizeof(St)))];
-  __align__(16) Q kdec[16][K + 8];
-  __align__(16) __nv_bfloat16 vs[16][V + 8];
-  __align__(16) __nv_bfloat16 qd[16][K + 8];  // scale q e^{G}
-  __align__(16) __half kr[16][K + 8];         // k e^{G_last - G}
+  // channel-major [channel][16 tokens] tiles (halves swizzled, rt_cm_off)
+  __align__(16) Q kdec[K][16];
+  __align__(16) __nv_bfloat16 vs[V][16];
+  __align__(16) __nv_bfloat16 qd[K][16];  // scale q e^{G}
+  __align__(16) __half kr[K][16];         // k e^{G_last - G}
   __align__(16) __half mqk[16][24];
   __align__(16) float gamma[K];
   float Lm[16][17];
@@ -76,6 +77,12 @@ struct RtcSmem {
   __device__ __forceinline__ Lv& lv() { return *reinterpret_cast<Lv*>(region); }
   __device__ __forceinline__ St& st() { return *reinterpret_cast<St*>(region); }
 };
+
+// Channel-major 16-bit tiles [channel][16 tokens]: a channel's 16 tokens are one
+// 32-byte row, written by the thread that owns the channel with two 16-byte
+// stores; the two halves (tokens 0-7, 8-15) are swapped on rows whose bit 2 is
+// set, so the eight rows of one ldmatrix 8x8 load fall on distinct banks.
+__device__ __forceinline__ int rt_cm_off(int row, int half) { return row * 16 + ((half ^ (row >> 2)) & 1) * 8; }
 
 __device__ __forceinline__ int rt_row_tok(int s, int r) { return (r / s) * 2 * s + s + (r % s); }
 __device__ __forceinline__ int rt_col_tok(int s, int r) { return (r / s) * 2 * s + (r % s); }
@@ -203,9 +210,15 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
         sm.red[warp][32 + j] = t3;
       }
     }
-    if (vown) {
+    if (vown) {  // v rows into the channel-major tile (raw bf16 bits, two tokens per word)
+      uint32_t w[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) sm.vs[i][tid] = in.v[i][tid];
+      for (int i = 0; i < 8; ++i)
+        w[i] = static_cast<uint32_t>(__bfloat16_as_ushort(in.v[2 * i][tid])) |
+               (static_cast<uint32_t>(__bfloat16_as_ushort(in.v[2 * i + 1][tid])) << 16);
+      uint16_t* tile = reinterpret_cast<uint16_t*>(&sm.vs[0][0]);
+      *reinterpret_cast<uint4*>(tile + rt_cm_off(tid, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(tile + rt_cm_off(tid, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
     }
     __syncthreads();
     if (tid < 16) {
@@ -236,16 +249,28 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
       Rs[15] = 1.f;
 #pragma unroll
       for (int i = 14; i >= 0; --i) Rs[i] = Rs[i + 1] * al[i + 1];
+      // channel ch's 16 tokens of each channel-major tile, two 16-byte stores each
+      auto put16 = [&](void* tile, const uint32_t (&w)[8]) {
+        uint16_t* base = reinterpret_cast<uint16_t*>(tile);
+        *reinterpret_cast<uint4*>(base + rt_cm_off(ch, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(base + rt_cm_off(ch, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+      };
+      uint32_t w[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        sm.qd[i][ch] = __float2bfloat16_rn(p.scale * qv[i] * P[i]);
-        sm.kr[i][ch] = __float2half_rn(kv[i] * Rs[i]);
-        sm.kdec[i][ch] = QK::cvt(kv[i] * P[i]);
-      }
+      for (int i = 0; i < 8; ++i)
+        w[i] = Bf16::pack(p.scale * qv[2 * i] * P[2 * i], p.scale * qv[2 * i + 1] * P[2 * i + 1]);
+      put16(&sm.qd[0][0], w);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = F16::pack(kv[2 * i] * Rs[2 * i], kv[2 * i + 1] * Rs[2 * i + 1]);
+      put16(&sm.kr[0][0], w);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w[i] = QK::pack(kv[2 * i] * P[2 * i], kv[2 * i + 1] * P[2 * i + 1]);
+      put16(&sm.kdec[0][0], w);
       sm.gamma[ch] = P[15];
 #pragma unroll
       for (int lv = 0; lv < 4; ++lv) {
         const int s = 8 >> lv;
+        float ar[16], bc[8];  // this channel's row (k rows 0-7, q rows 8-15) and column operands
 #pragma unroll
         for (int blk = 0; blk < 8 / s; ++blk) {
           const int m = blk * 2 * s + s;  // anchor: first row of the upper half
@@ -254,16 +279,21 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
           for (int i = m; i < m + s; ++i) {  // row tokens: prod_{m<t<=i} alpha_t
             if (i > m) f *= al[i];
             const int r = blk * s + (i - m);
-            lvo.A[lv][r][ch] = QK::cvt(kv[i] * f);
-            lvo.A[lv][8 + r][ch] = QK::cvt(qv[i] * f);
+            ar[r] = kv[i] * f;
+            ar[8 + r] = qv[i] * f;
           }
           f = 1.f;
 #pragma unroll
           for (int i = m - 1; i >= m - s; --i) {  // column tokens: prod_{i<t<=m} alpha_t
             f *= al[i + 1];
-            lvo.B[lv][blk * s + (i - (m - s))][ch] = QK::cvt(kv[i] * f);
+            bc[blk * s + (i - (m - s))] = kv[i] * f;
           }
         }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = QK::pack(ar[2 * i], ar[2 * i + 1]);
+        put16(&lvo.A[lv][0][0], w);
+        *reinterpret_cast<uint4*>(&lvo.B[lv][ch][0]) =
+            make_uint4(QK::pack(bc[0], bc[1]), QK::pack(bc[2], bc[3]), QK::pack(bc[4], bc[5]), QK::pack(bc[6], bc[7]));
       }
     }
     __syncthreads();
@@ -274,8 +304,10 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
 #pragma unroll
       for (int kk = 0; kk < KK; ++kk) {
         uint32_t a[4], bq[2];
-        ldsm_x4(a, &lvo.A[lv][lane & 15][16 * kk + (lane >> 4) * 8]);
-        ldsm_x2(bq, &lvo.B[lv][lane & 7][16 * kk + ((lane >> 3) & 1) * 8]);
+        // A and B are stored [channel][row]: .trans loads; lane matrix m of A =
+        // (row half m & 1, channel half m >> 1)
+        ldsm_x4_trans(a, &lvo.A[lv][0][0] + rt_cm_off(16 * kk + (lane >> 4) * 8 + (lane & 7), (lane >> 3) & 1));
+        ldsm_x2_trans(bq, &lvo.B[lv][16 * kk + (lane & 15)][0]);
         mma16816<QK>(acc, a, bq[0], bq[1]);
       }
 #pragma unroll
@@ -311,7 +343,7 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
       for (int blk = warp; blk < K / 16; blk += WARPS) {  // -W, 16 key channels per block
         const int n0 = 16 * blk;
         uint32_t bw[4];
-        ldsm_x4_trans(bw, &sm.kdec[lane & 15][n0 + (lane >> 4) * 8]);
+        ldsm_x4(bw, &sm.kdec[0][0] + rt_cm_off(n0 + (lane >> 4) * 8 + (lane & 7), (lane >> 3) & 1));
         float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
         mma16816<QK>(c0, a, bw[0], bw[1]);
         mma16816<QK>(c1, a, bw[2], bw[3]);
@@ -323,7 +355,7 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
       for (int blk = warp; blk < V / 16; blk += WARPS) {  // U~ (fp32 through a hi/lo split), 16 value channels
         const int n0 = 16 * blk;
         uint32_t bv[4];
-        ldsm_x4_trans(bv, &sm.vs[lane & 15][n0 + (lane >> 4) * 8]);
+        ldsm_x4(bv, &sm.vs[0][0] + rt_cm_off(n0 + (lane >> 4) * 8 + (lane & 7), (lane >> 3) & 1));
         float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};
         mma16816<Bf16>(u0, ahi, bv[0], bv[1]);
         mma16816<Bf16>(u0, alo, bv[0], bv[1]);
@@ -380,7 +412,7 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
         float (&acc)[2][4] = (kk & 1) ? u2 : u;
         mma16816<Bf16>(acc[0], sa, bm[0], bm[1]);
         mma16816<Bf16>(acc[1], sa, bm[2], bm[3]);
-        ldsm_x4(bm, &sm.qd[row][col]);
+        ldsm_x4_trans(bm, &sm.qd[0][0] + rt_cm_off(16 * kk + ((lane >> 3) & 1) * 8 + (lane & 7), lane >> 4));
         mma16816<Bf16>(o[0], sa, bm[0], bm[1]);
         mma16816<Bf16>(o[1], sa, bm[2], bm[3]);
       }
@@ -397,7 +429,7 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
 #pragma unroll
       for (int np = 0; np < KK; ++np) {
         uint32_t bm[4];
-        ldsm_x4_trans(bm, &sm.kr[lane & 15][16 * np + (lane >> 4) * 8]);
+        ldsm_x4(bm, &sm.kr[0][0] + rt_cm_off(16 * np + (lane >> 4) * 8 + (lane & 7), (lane >> 3) & 1));
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           const int nt = 2 * np + half;

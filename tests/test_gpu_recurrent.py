@@ -28,7 +28,7 @@ def _run(wl, err=None):
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in wl.items()}
     pool = d["state_pool"].clone()
     o = kda.kda_recurrent_step(d["q"], d["k"], d["v"], d["a"], d["b"], d["A_log"], d["dt_bias"], pool, d["indices"],
-                               scale=wl["scale"], err=err)
+                               scale=wl["scale"], err=err, l2norm_qk=wl.get("l2norm", True))
     torch.cuda.synchronize()
     return o, pool
 
@@ -36,7 +36,7 @@ def _run(wl, err=None):
 def _oracle(wl):
     return ko.kda_recurrent_pool(np64(wl["q"]), np64(wl["k"]), np64(wl["v"]), np64(wl["a"]), np64(wl["b"]),
                                  np64(wl["A_log"]), np64(wl["dt_bias"]), np64(wl["state_pool"]),
-                                 wl["indices"].numpy(), scale=wl["scale"])
+                                 wl["indices"].numpy(), scale=wl["scale"], l2norm_qk=wl.get("l2norm", True))
 
 
 def _check(wl):
@@ -152,3 +152,36 @@ def test_check_indices_flag(entry):
     dup[valid[-1]] = dup[valid[3]]  # rows far apart (different check tiles) share a slot
     e2, _, _ = call(dup, True)
     assert e2 == 1
+
+
+@pytest.mark.parametrize("T", [4, 12, 40])
+def test_recurrent_without_l2norm(T):
+    """KDA_FLAG_L2NORM_QK off (q, k used as given, drawn with std K^-1/2): the
+    per-token kernel (T = 4) and the chunk-form kernel (T = 12, 40; bf16 level
+    operands) against the oracle."""
+    wl = W.recurrent_workload(seed=160 + T, B=6, T=T, H=2, HV=4, K=128, V=64, num_slots=9, pad_frac=0.2)
+    s = 128 ** -0.5
+    wl["q"] = (wl["q"].float() * s).to(torch.bfloat16)
+    wl["k"] = (wl["k"].float() * s).to(torch.bfloat16)
+    wl["l2norm"] = False
+    _check(wl)
+
+
+def test_decode_without_l2norm():
+    """The packed decode with KDA_FLAG_L2NORM_QK off against the oracle's decode."""
+    wl = W.decode_workload(seed=171, B=12, H=2, HV=4, K=64, V=128, num_slots=20, pad_frac=0.2)
+    B, H, HV, K, V = wl["B"], wl["H"], wl["HV"], wl["K"], wl["V"]
+    packed = wl["packed_qkv"].float()
+    packed[:, : 2 * H * K] *= K ** -0.5
+    packed = packed.to(torch.bfloat16)
+    pool = wl["state_pool"].cuda().clone()
+    o = kda.kda_decode_step(packed.cuda(), wl["a"].cuda(), wl["b"].cuda(), wl["A_log"].cuda(), wl["dt_bias"].cuda(),
+                            pool, wl["indices"].cuda(), H=H, HV=HV, K=K, V=V, scale=wl["scale"], l2norm_qk=False)
+    torch.cuda.synchronize()
+    o_ref, pool_ref = ko.kda_decode(np64(packed), np64(wl["a"]), np64(wl["b"]), np64(wl["A_log"]),
+                                    np64(wl["dt_bias"]), np64(wl["state_pool"]), wl["indices"].numpy(), H=H, HV=HV,
+                                    K=K, V=V, scale=wl["scale"], l2norm_qk=False)
+    valid = (wl["indices"] >= 0).nonzero().flatten()
+    slots = wl["indices"][valid].long()
+    assert_close("decode o (no l2norm)", np64(o)[valid.numpy()], o_ref[valid.numpy()], torch.bfloat16)
+    assert_close("decode state (no l2norm)", np64(pool[slots.cuda()]), pool_ref[slots.numpy()], torch.bfloat16)

@@ -363,6 +363,16 @@ kda_status kda_chunk_fwd_noalloc(const kda_chunk_args* args, kda_stream_t stream
 /* Version string of the library, e.g. "kda-gb300 0.1.0 sm_103a". */
 const char* kda_version(void);
 
+/*
+ * Diagnostic: exercises the bounded device-side wait that every mbarrier wait
+ * of the fused chunk kernel uses. One thread waits on a shared-memory mbarrier
+ * that nothing arrives on, gives up after limit_ns nanoseconds (1e3 .. 1e10)
+ * and writes KDA_ERR_TIMEOUT to *err (device int32, 4-byte aligned); the
+ * kernel then returns and the context stays usable. Tests use it to check the
+ * failure path without a fault or a hang.
+ */
+kda_status kda_selftest_bounded_wait(int32_t* err, uint64_t limit_ns, kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -98,7 +98,8 @@ class RmsNormArgs(ctypes.Structure):
 
 
 EXPORTS = ("kda_chunk_fwd", "kda_chunk_output", "kda_chunk_fwd_noalloc", "kda_chunk_workspace_size", "kda_decode_step",
-           "kda_decode_conv_step", "kda_recurrent_step", "kda_head_rmsnorm", "kda_version")
+           "kda_decode_conv_step", "kda_recurrent_step", "kda_head_rmsnorm", "kda_version",
+           "kda_selftest_bounded_wait")
 
 
 def lib_path() -> Path:
@@ -134,12 +135,23 @@ def load() -> ctypes.CDLL:
         lib.kda_chunk_fwd_noalloc.argtypes = [ctypes.POINTER(ChunkArgs), ctypes.c_void_p]
         lib.kda_version.restype = ctypes.c_char_p
         lib.kda_version.argtypes = []
+        lib.kda_selftest_bounded_wait.restype = ctypes.c_int
+        lib.kda_selftest_bounded_wait.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
         _lib = lib
         return lib
 
 
 def version() -> str:
     return load().kda_version().decode()
+
+
+def selftest_bounded_wait(err, limit_ns, stream=None):
+    """Run the bounded-wait self-test kernel: it waits on an mbarrier that nothing
+    arrives on, gives up after limit_ns and writes KDA_ERR_TIMEOUT to err
+    (a device int32 tensor). See include/kda.h."""
+    st = load().kda_selftest_bounded_wait(_ptr(err), ctypes.c_uint64(int(limit_ns)), _stream_ptr(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_selftest_bounded_wait")
 
 
 def _ptr(t):

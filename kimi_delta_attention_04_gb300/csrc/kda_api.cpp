@@ -315,4 +315,11 @@ kda_status kda_head_rmsnorm(const kda_rmsnorm_args* a, kda_stream_t stream) {
 
 const char* kda_version(void) { return "kda-gb300 0.1.0 sm_103a"; }
 
+kda_status kda_selftest_bounded_wait(int32_t* err, uint64_t limit_ns, kda_stream_t stream) {
+  if (err == nullptr || !aligned(err, 4)) return KDA_ERR_INVALID_ARG;
+  if (limit_ns < 1000 || limit_ns > UINT64_C(10000000000)) return KDA_ERR_INVALID_ARG;
+  const cudaError_t e = kda::launch_wait_selftest(err, limit_ns, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 }  // extern "C"

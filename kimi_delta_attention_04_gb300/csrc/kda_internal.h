@@ -111,6 +111,7 @@ cudaError_t launch_chunk_fused(const ChunkCall& c, cudaStream_t s);  // bf16, dk
 size_t fused_smem_bytes();
 size_t fused_workspace_bytes();  // pool of per-cluster global rings (fixed size)
 cudaError_t launch_decode(const DecodeCall& c, cudaStream_t s);
+cudaError_t launch_wait_selftest(int32_t* err, unsigned long long limit_ns, cudaStream_t s);
 cudaError_t launch_check_indices(const int32_t* idx, int B, int num_slots, int32_t* err, cudaStream_t s);
 cudaError_t launch_recurrent(const RecurrentCall& c, cudaStream_t s);
 cudaError_t launch_recurrent_tc(const RecurrentCall& c, cudaStream_t s);  // T tokens as chunks, tensor cores

@@ -170,6 +170,15 @@ def test_chunk_validation_rejects(lib, over, status):
     assert lib.kda_chunk_output(ctypes.byref(a), ctypes.c_void_p(FAKE), ctypes.c_size_t(1 << 40), None) == status
 
 
+def test_selftest_bounded_wait_validation(lib):
+    """The wait self-test needs an aligned status word and a limit in [1 us, 10 s]."""
+    f = lib.kda_selftest_bounded_wait
+    assert f(None, 1_000_000, None) == _lib.KDA_ERR_INVALID_ARG
+    assert f(ctypes.c_void_p(FAKE + 2), 1_000_000, None) == _lib.KDA_ERR_INVALID_ARG
+    assert f(ctypes.c_void_p(FAKE), 999, None) == _lib.KDA_ERR_INVALID_ARG
+    assert f(ctypes.c_void_p(FAKE), 10_000_000_001, None) == _lib.KDA_ERR_INVALID_ARG
+
+
 def test_chunk_output_needs_states(lib):
     """The chunk-parallel output pass reads h_chunks: without it the call is refused."""
     a = _chunk()

@@ -266,3 +266,21 @@ def test_prefill_state_feeds_decode():
                              np64(dw["dt_bias"]), pool_ref_in, np.array([1]), H=2, HV=2, K=128, V=128,
                              scale=dref["scale"])
     assert_close("prefill->decode o", np64(o), o_ref, torch.bfloat16)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """The bounded device-side wait (used by every mbarrier wait of the fused
+    kernel) gives up on a barrier nothing arrives on, reports KDA_ERR_TIMEOUT
+    through err and returns; the context then runs a chunk forward normally."""
+    from kimi_delta_attention_04_gb300 import _lib
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _lib.selftest_bounded_wait(err, 2_000_000)  # 2 ms
+    torch.cuda.synchronize()
+    assert int(err.item()) == _lib.KDA_ERR_TIMEOUT
+    wl = W.prefill(T=64, H=2)
+    err2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o, hT = gpu_chunk(wl, err=err2)
+    torch.cuda.synchronize()
+    assert int(err2.item()) == 0
+    o_ref, h_ref = oracle_chunk(wl)
+    assert_close("after timeout o", np64(o), o_ref, wl["dtype"])

@@ -17,6 +17,10 @@
 //   * the two dot products of each row (S~ k and S~ q) are reduced for 8 rows
 //     at once with a transpose reduction (16 shuffles for 16 sums); the output
 //     uses o_r = S~_r q + u_r (k q), so no second pass over the updated row.
+// With the causal conv1d + SiLU in front (CONV), the CTA first asks L2 for its
+// slot, its 128 threads convolve the row's q/k channels once between them
+// (shared through shared memory) and each thread its own v channel; then the
+// state stream runs as above.
 #include "kda_cluster.cuh"
 #include "kda_common.cuh"
 

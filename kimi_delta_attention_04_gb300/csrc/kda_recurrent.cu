@@ -17,6 +17,8 @@
 // per token. The tokens' normalised q and k, their decay factors, beta, k.q and
 // the value rows are prepared once per CTA in shared memory (warp w prepares
 // tokens w, w + 4, ...), where every row group reads them.
+// The per-token work grows with T: from 8 tokens per row the entry point runs
+// the chunk-form kernel of kda_recurrent_tc.cu instead.
 #include "kda_common.cuh"
 
 namespace kda {

@@ -788,12 +788,10 @@ template <bool DELTA, bool L2N, int MODE>
 cudaError_t launch_fused_t(const ChunkCall& c, cudaStream_t s) {
   using QK = std::conditional_t<L2N, F16, Bf16>;
   const size_t smem = sizeof(FusedSmem<typename QK::T>);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(kda_chunk_fused_kernel<DELTA, L2N, MODE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  static std::atomic<uint64_t> smem_set{0};
+  {
+    const cudaError_t e = set_smem_limit_once(kda_chunk_fused_kernel<DELTA, L2N, MODE>, smem, smem_set);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const unsigned grid = static_cast<unsigned>(c.geo.N) * static_cast<unsigned>(c.geo.H) * kCtas;
   if (grid == 0) return cudaSuccess;

@@ -599,12 +599,10 @@ cudaError_t launch_recur_t(const ChunkCall& c, cudaStream_t s) {
   using ST2 = std::conditional_t<DELTA, F16, Bf16>;
   using Smem = RecSmem<D, WARPS, typename ST2::T>;
   const size_t smem = sizeof(Smem);
-  static bool attr_set = false;  // per instantiation; the attribute is per device-function
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kda_recur_tc_kernel<D, WARPS, DELTA, PAR>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  static std::atomic<uint64_t> smem_set{0};  // per instantiation and device
+  {
+    const cudaError_t e = set_smem_limit_once(kda_recur_tc_kernel<D, WARPS, DELTA, PAR>, smem, smem_set);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const unsigned units = PAR ? static_cast<unsigned>(c.geo.max_chunks) : static_cast<unsigned>(c.geo.N);
   if (units == 0) return cudaSuccess;

@@ -8,9 +8,27 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "kda_internal.h"
 
 namespace kda {
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` once per device: the
+// attribute belongs to each device's context, so a process driving several
+// GPUs must set it on each. `done` is the kernel's record of the devices
+// already set (ids 0-63; beyond that every call sets it).
+template <typename Kernel>
+inline cudaError_t set_smem_limit_once(Kernel kernel, size_t bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t{1} << dev) : 0;
+  if (bit != 0 && (done.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // ---------------------------------------------------------------------------
 // Element types of MMA operands

@@ -204,12 +204,10 @@ __global__ void __launch_bounds__(kThreads) kda_recurrent_kernel(const Recurrent
 
 template <int K, int V>
 cudaError_t launch_recurrent_t(const RecurrentCall& c, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e = cudaFuncSetAttribute(kda_recurrent_kernel<K, V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(recurrent_smem_bytes(kMaxT, K, V)));
+  static std::atomic<uint64_t> smem_set{0};
+  {
+    const cudaError_t e = set_smem_limit_once(kda_recurrent_kernel<K, V>, recurrent_smem_bytes(kMaxT, K, V), smem_set);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const unsigned grid = static_cast<unsigned>(c.B) * static_cast<unsigned>(c.HV);
   kda_recurrent_kernel<K, V><<<grid, kThreads, recurrent_smem_bytes(c.T, K, V), s>>>(c);

@@ -486,12 +486,10 @@ template <int K, int V, bool L2N>
 cudaError_t launch_rtc_t(const RecurrentCall& c, cudaStream_t s) {
   using Q = typename std::conditional_t<L2N, F16, Bf16>::T;
   constexpr size_t smem = sizeof(RtcSmem<K, V, Q>);
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e = cudaFuncSetAttribute(kda_recurrent_tc_kernel<K, V, L2N>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  static std::atomic<uint64_t> smem_set{0};
+  {
+    const cudaError_t e = set_smem_limit_once(kda_recurrent_tc_kernel<K, V, L2N>, smem, smem_set);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const unsigned grid = static_cast<unsigned>(c.B) * static_cast<unsigned>(c.HV);
   kda_recurrent_tc_kernel<K, V, L2N><<<grid, 128, smem, s>>>(c);

@@ -809,8 +809,6 @@ cudaError_t launch_fused_t(const ChunkCall& c, cudaStream_t s) {
 static_assert(sizeof(FusedSmem<__half>) <= 227 * 1024 && sizeof(FusedSmem<__nv_bfloat16>) <= 227 * 1024,
               "fused kernel shared memory");
 
-size_t fused_smem_bytes() { return sizeof(FusedSmem<__half>); }
-
 size_t fused_workspace_bytes() { return kPoolHeader + static_cast<size_t>(kPool) * kRingBytes; }
 
 template <int MODE>

@@ -83,29 +83,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
-// Arrive and add `bytes` to the expected transaction count of a cluster mbarrier.
-__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cluster_bar),
-               "r"(bytes)
-               : "memory");
-}
-
-// Bulk copy from this CTA's shared memory into (possibly another CTA's) shared
-// memory; completion is counted on the destination CTA's mbarrier. Both
-// addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_copy_s2s(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
-                                              uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst_cluster),
-      "r"(src_cta), "r"(bytes), "r"(bar_cluster)
-      : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-// Waits until the source reads of all committed bulk copies are done.
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -188,13 +165,6 @@ __device__ __forceinline__ int ld_shared_cluster_s32(uint32_t cluster_addr) {
   int v;
   asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
   return v;
-}
-
-// 16-byte cp.async with zero fill when src_bytes == 0.
-__device__ __forceinline__ void cp_async16_zfill(void* smem, const void* gmem, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(static_cast<uint32_t>(
-                   __cvta_generic_to_shared(smem))),
-               "l"(gmem), "r"(src_bytes));
 }
 
 }  // namespace kda

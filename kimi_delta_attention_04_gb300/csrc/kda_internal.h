@@ -108,7 +108,6 @@ cudaError_t launch_chunk_tc(const ChunkCall& c, cudaStream_t s);
 cudaError_t launch_chunk_output_tc(const ChunkCall& c, cudaStream_t s);  // chunk-parallel o from h_chunks
 cudaError_t launch_chunk_f32(const ChunkCall& c, cudaStream_t s);
 cudaError_t launch_chunk_fused(const ChunkCall& c, cudaStream_t s);  // bf16, dk = dv = 128
-size_t fused_smem_bytes();
 size_t fused_workspace_bytes();  // pool of per-cluster global rings (fixed size)
 cudaError_t launch_decode(const DecodeCall& c, cudaStream_t s);
 cudaError_t launch_wait_selftest(int32_t* err, unsigned long long limit_ns, cudaStream_t s);

@@ -185,6 +185,19 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(values, device):
+    """The element-wise maximum of `values` (floats) over the ranks of the
+    default process group (NCCL on GPUs, gloo on CPU); the values themselves
+    with one rank. Every rank gets the result."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def oracle_sample(T_sample=None, budget_s=20.0, chunk_size=None):
     """Time the fp64 oracle (as it stands: the token recurrence, or with
     chunk_size its chunked form) on the first tokens of the prefill workload,
@@ -222,7 +235,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    budget = max(3.0, 60.0 / max(args.steps + args.warmup, 1))
+    budget = max(1.0, args.ref_budget / max(args.steps + args.warmup, 1))
     vals = []
     sample = ""
     for i in range(args.warmup + args.steps):
@@ -547,10 +560,7 @@ def run_gpu(args):
     t_chunk = sum(chunk_ms) / 1000.0
     t_dec = sum(dec_ms) / 1000.0
     t_total = total_ms / 1000.0
-    vals = torch.tensor([t_chunk, t_dec, t_total, e2e_s], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(vals, op=dist.ReduceOp.MAX)
-    t_chunk, t_dec, t_total, e2e_s = vals.tolist()
+    t_chunk, t_dec, t_total, e2e_s = max_over_ranks([t_chunk, t_dec, t_total, e2e_s], dev)
     tokens = T * K * world
     value = tokens / t_chunk if t_chunk > 0 else 0.0
 
@@ -637,6 +647,8 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=60.0,
+                    help="seconds of oracle work for the whole --impl reference run (spread over its steps)")
     ap.add_argument("--only", choices=["all", "chunk", "decode"], default="all",
                     help="time only one part (profiling runs; the benchmark line uses all)")
     ap.add_argument("--seq-len", type=int, default=PREFILL_T, help="prefill tokens (profiling runs use fewer)")

@@ -1,0 +1,73 @@
+"""The N > 1 host path on CPU with gloo, world size 2 (no GPU): the timing
+reduction bench.py applies across ranks, and the reference arm under torchrun
+(rank 0 runs and prints one JSON line, the other rank exits 0 without work).
+The GPU path itself runs independent replicas per rank, with no collective
+beyond this reduction."""
+
+import json
+import os
+import socket
+import subprocess
+import sys
+from pathlib import Path
+
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _reduce_worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    sys.path.insert(0, str(ROOT))
+    import bench
+
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        vals = bench.max_over_ranks([1.0 + rank, 10.0 - rank, 0.5 * rank], "cpu")
+        out[rank] = torch.tensor(vals)
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world_size_2():
+    world = 2
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        out = m.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_reduce_worker, args=(r, world, port, out)) for r in range(world)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        for r in range(world):
+            assert out[r].tolist() == [2.0, 10.0, 0.5]
+
+
+def test_max_over_ranks_single_process_is_identity():
+    sys.path.insert(0, str(ROOT))
+    import bench
+
+    assert bench.max_over_ranks([3.0, 1.5], "cpu") == [3.0, 1.5]
+
+
+def test_reference_arm_under_torchrun_world_size_2():
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference",
+           "--gpus", "2", "--steps", "1", "--warmup", "3", "--ref-budget", "2"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1  # rank 0 alone prints
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle"

@@ -142,27 +142,65 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_tc_kernel(const ChunkCa
     sm.beta[tid] = bt;
   }
 
+  // ---- the chunk's rows of q, k, v and the per-channel gate, staged in shared
+  // memory with 16-byte cp.async (the level-operand buffers are free until the
+  // operands are written, two barriers later); rows past the chunk are zeroed ----
+  struct StagedIn {
+    __nv_bfloat16 q[16][D];
+    __nv_bfloat16 k[16][D];
+    __nv_bfloat16 v[16][D];
+    float g[16][D];  // g (gate mode 1) or the gate input a (mode 2)
+  };
+  static_assert(sizeof(StagedIn) <= sizeof(sm.A_lv) + sizeof(sm.B_lv), "staging fits the level buffers");
+  StagedIn& in = *reinterpret_cast<StagedIn*>(&sm.A_lv[0][0][0]);
+  const bool gate_rows = p.gate_mode == 1 || p.gate_mode == 2;
+  {
+    const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(p.q);
+    const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(p.k);
+    const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(p.v);
+    const float* gb = p.gate_mode == 1 ? p.g : p.a;
+    constexpr int V8 = D / 8, V4 = D / 4;  // 16-byte vectors per bf16 / fp32 row
+    for (int i = tid; i < 16 * V8; i += kPrepThreads) {
+      const int row = i / V8, c8 = i - row * V8;
+      if (row < pos.ntok) {
+        const size_t off = (static_cast<size_t>(pos.tok0 + row) * H + h) * D + c8 * 8;
+        cp_async16(&in.q[row][c8 * 8], qb + off);
+        cp_async16(&in.k[row][c8 * 8], kb + off);
+        cp_async16(&in.v[row][c8 * 8], vb + off);
+      } else {
+        *reinterpret_cast<uint4*>(&in.q[row][c8 * 8]) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(&in.k[row][c8 * 8]) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(&in.v[row][c8 * 8]) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    if (gate_rows) {
+      for (int i = tid; i < 16 * V4; i += kPrepThreads) {
+        const int row = i / V4, c4 = i - row * V4;
+        if (row < pos.ntok) cp_async16(&in.g[row][c4 * 4], gb + (static_cast<size_t>(pos.tok0 + row) * H + h) * D + c4 * 4);
+        else *reinterpret_cast<float4*>(&in.g[row][c4 * 4]) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+  }
+  __syncthreads();
+
   // ---- per-channel columns of the chunk (thread ch owns key channel ch) ----
-  const size_t row_stride = static_cast<size_t>(H) * D;
-  const size_t base = (static_cast<size_t>(pos.tok0) * H + h) * D + ch;
-  const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(p.q) + base;
-  const __nv_bfloat16* kp = reinterpret_cast<const __nv_bfloat16*>(p.k) + base;
-  const __nv_bfloat16* vp = reinterpret_cast<const __nv_bfloat16*>(p.v) + base;
   float qv[16], kv[16], al[16], vv[16];
   const float Aexp = (p.gate_mode == 2) ? expf(p.A_log[h]) : 0.f;
   const float dtb = (p.gate_mode == 2 && own) ? p.dt_bias[h * D + ch] : 0.f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const bool valid = own && i < pos.ntok;
-    qv[i] = valid ? __bfloat162float(qp[i * row_stride]) : 0.f;
-    kv[i] = valid ? __bfloat162float(kp[i * row_stride]) : 0.f;
-    vv[i] = valid ? __bfloat162float(vp[i * row_stride]) : 0.f;
+    qv[i] = valid ? __bfloat162float(in.q[i][ch]) : 0.f;
+    kv[i] = valid ? __bfloat162float(in.k[i][ch]) : 0.f;
+    vv[i] = valid ? __bfloat162float(in.v[i][ch]) : 0.f;
     float a = 1.f;
     if (valid) {
       if (p.gate_mode == 1) {
-        a = expf(p.g[base + i * row_stride]);
+        a = expf(in.g[i][ch]);
       } else if (p.gate_mode == 2) {
-        const float x = p.a[base + i * row_stride] + dtb;
+        const float x = in.g[i][ch] + dtb;
         a = expf(-Aexp * softplus_f(x));
       } else if (p.gate_mode == 3) {  // one decay per token and head
         a = expf(p.g[(static_cast<size_t>(pos.tok0) + i) * H + h]);

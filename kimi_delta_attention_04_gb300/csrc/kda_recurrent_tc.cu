@@ -13,17 +13,17 @@
 // k_res^T U"), so the state work runs as mma.sync m16n8k16 with fp32
 // accumulation instead of per-token FMA loops. One CTA of 4 warps per
 // (row, value head), four CTAs per SM:
-//  * the CTA first asks L2 for the row's 64 KiB slot (bulk prefetch), then
-//    prepares a chunk in shared memory with one thread per key channel (L2
-//    norms, decay products, the anchored level split of L and Mqk, each warp
+//  * the CTA first asks L2 for the row's 64 KiB slot (bulk prefetch), stages
+//    the chunk's q, k, a and v rows with 16-byte cp.async, then prepares the
+//    chunk with one thread per key channel (L2 norms, decay products, the
+//    anchored level split of L and Mqk into channel-major tiles, each warp
 //    forming the inverse in registers for its columns of W and U~);
 //  * each warp owns V / 4 value rows of the state and steps them 16 at a
-//    time, S^T [16 x K] fp32 in
-//    registers as MMA accumulators, loaded after the chunk's preparation and
-//    stored back after its step (between chunks of a long T the rows make an
-//    L2 round trip rather than stay live across the next preparation):
-//    U^T = U~^T - S^T W^T, O^T = S^T q_dec^T + U^T Mqk^T, S^T = S^T diag(gamma)
-//    + U^T k_res;
+//    time, S^T [16 x K] fp32 in registers as MMA accumulators, loaded after
+//    the chunk's preparation and stored back after its step (between chunks
+//    of a long T the rows make an L2 round trip rather than stay live across
+//    the next preparation): U^T = U~^T - S^T W^T, O^T = S^T q_dec^T + U^T
+//    Mqk^T, S^T = S^T diag(gamma) + U^T k_res;
 //  * o is staged in shared memory and written as 16-byte rows.
 // Operand precision as in the chunk forward: S, W, q_dec bf16; U, k_res, Mqk
 // fp16; L/Mqk/INV operands fp16 (q, k normalised) or bf16; U~ fp32.

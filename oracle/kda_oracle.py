@@ -31,7 +31,7 @@ The oracle works on the math state S[K, V] internally: S_t = S_{t-1} decayed on
 its key rows, o_t = scale * S_t^T q_t ([TL] §1 gives the transposed (d_v, d_k)
 form; [FKDA] 背景 gives the same recurrence with the state read as k^T S).
 
-Readings of points the pages leave open (each is also listed in the design doc):
+Readings of points the pages leave open:
   * softplus is the plain definition log(1 + e^x); kernels may switch to x above
     a threshold, the difference there is below 2.1e-9.
   * the L2 norm is x / sqrt(sum x^2 + 1e-6) ([PR] kernel source).

@@ -275,7 +275,7 @@ def run_gpu(args):
     # --- inputs (replica per rank: seeds differ, shapes identical) ---
     T = args.seq_len
     wl = W.prefill(seed=2 + 100 * rank, T=T)
-    dw = W.decode(seed=4 + 100 * rank) if args.only != "chunk" else W.decode(seed=4, B=8, num_slots=16)
+    dw = W.decode(seed=4 + 100 * rank) if args.only in ("all", "decode") else W.decode(seed=4, B=8, num_slots=16)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in wl.items()}
     dd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in dw.items()}
     o = torch.empty(1, T, PREFILL_H, D, dtype=torch.bfloat16, device=dev)
@@ -288,14 +288,14 @@ def run_gpu(args):
     n_valid = int((dw["indices"] >= 0).sum())
 
     def chunk_step():
-        if args.only == "decode":
+        if args.only not in ("all", "chunk"):
             return
         kda.kda_chunk_fwd(d["q"], d["k"], d["v"], scale=d["scale"], a=d["a"], dt_bias=d["dt_bias"],
                           A_log=d["A_log"], b=d["b"], h0=d["h0"], l2norm_qk=True, o=o, hT=hT, workspace=ws,
                           stream=stream)
 
     def decode_step():
-        if args.only == "chunk":
+        if args.only not in ("all", "decode"):
             return
         kda.kda_decode_step(dd["packed_qkv"], dd["a"], dd["b"], dd["A_log"], dd["dt_bias"], pool, dd["indices"],
                             H=dw["H"], HV=dw["HV"], K=dw["K"], V=dw["V"], scale=dw["scale"], o=od, stream=stream)
@@ -330,7 +330,7 @@ def run_gpu(args):
     # --- decode launch overheads: host wall-clock per step including the launch,
     # and the same steps replayed from a CUDA graph ---
     dec_wall = dec_graph = None
-    if args.only != "chunk":
+    if args.only in ("all", "decode"):
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
         for _ in range(K):
@@ -366,7 +366,7 @@ def run_gpu(args):
     hT_hs = [torch.empty(hT.shape, dtype=hT.dtype).pin_memory() for _ in range(2)]
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     d2h = o_hs[0].numel() * o_hs[0].element_size() + hT_hs[0].numel() * hT_hs[0].element_size()
-    e2e_steps = max(4, min(K, 10)) if args.only != "decode" else 0
+    e2e_steps = max(4, min(K, 10)) if args.only in ("all", "chunk") else 0
     e2e_s = 0.0
     if e2e_steps:
         h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -509,7 +509,7 @@ def run_gpu(args):
                              "algorithmic_bytes": rbytes, "kernel": kernel}}
 
     rec = rec_long = None
-    if args.only == "all":
+    if args.only in ("all", "recurrent"):
         rec = recurrent_field(RECURRENT_B, RECURRENT_T, RECURRENT_SLOTS)
         rec_long = recurrent_field(RECURRENT_LONG_B, RECURRENT_LONG_T, 2 * RECURRENT_LONG_B)
 
@@ -607,8 +607,8 @@ def run_gpu(args):
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                     "note": "copies on their own streams, two buffers each way: step i+1's inputs in and step "
                             "i-1's o and hT out while step i computes"},
-            "gpu_launches": (CHUNK_LAUNCHES_PER_STEP if args.only != "decode" else 0) * K
-                            + (DECODE_LAUNCHES_PER_STEP if args.only != "chunk" else 0) * K,
+            "gpu_launches": (CHUNK_LAUNCHES_PER_STEP if args.only in ("all", "chunk") else 0) * K
+                            + (DECODE_LAUNCHES_PER_STEP if args.only in ("all", "decode") else 0) * K,
             "clocks": clk,
         }
         if var is not None:
@@ -649,7 +649,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=60.0,
                     help="seconds of oracle work for the whole --impl reference run (spread over its steps)")
-    ap.add_argument("--only", choices=["all", "chunk", "decode"], default="all",
+    ap.add_argument("--only", choices=["all", "chunk", "decode", "recurrent"], default="all",
                     help="time only one part (profiling runs; the benchmark line uses all)")
     ap.add_argument("--seq-len", type=int, default=PREFILL_T, help="prefill tokens (profiling runs use fewer)")
     args = ap.parse_args()

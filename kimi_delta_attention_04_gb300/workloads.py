@@ -43,7 +43,7 @@ def _uniform(gen, shape, lo, hi, dtype=torch.float32):
 
 def chunk_workload(*, seed=2, B=1, T=8192, H=32, K=128, V=128, dtype=torch.bfloat16,
                    gate="inputs", beta="logits", l2norm=True, delta=True,
-                   A_log_hi=2.0, h0_std=0.1, lengths=None, qkv_std=1.0, scale=None):
+                   A_log_hi=2.0, h0_std=0.1, lengths=None, qkv_std=1.0, scale=None, v_std=None):
     """Inputs of one KDA chunk-forward call.
 
     Draw order: [lengths], q, k, v, gate inputs (a, dt_bias, A_log) or log-decay g,
@@ -53,10 +53,15 @@ def chunk_workload(*, seed=2, B=1, T=8192, H=32, K=128, V=128, dtype=torch.bfloa
     gate: "inputs" (a ~ N(0,1) fp32 [B, T, H*K], dt_bias ~ U(-1,1) [H*K],
           A_log ~ U(0, A_log_hi) [H]), "g" (a log-decay g = -U(0.01, 3) fp32
           [B, T, H, K], drawn directly), "head" (Gated DeltaNet: one log-decay
-          per token and head, g_head = -U(0.01, 3) fp32 [B, T, H]), or "none".
+          per token and head, g_head = -U(0.01, 3) fp32 [B, T, H]),
+          "g_extreme" (a per-(head, channel) coin, then g = -U(8, 20) on the
+          channels whose coin came up and -U(0.01, 0.5) on the others: every
+          16-token chunk then spans a log-decay far beyond the fp32 range of
+          e^{-G} on half of the channels), or "none".
     beta: "logits" (b ~ N(0,1)), "values" (beta ~ U(0,1)), both in the input dtype.
     h0_std: standard deviation of the fp32 initial state, or None for no h0.
     scale: output scale; defaults to K^-0.5.
+    v_std: standard deviation of v (defaults to qkv_std).
     """
     gen = _gen(seed)
     cu_seqlens = None
@@ -72,7 +77,7 @@ def chunk_workload(*, seed=2, B=1, T=8192, H=32, K=128, V=128, dtype=torch.bfloa
         cu_seqlens = torch.tensor(cu, dtype=torch.int32)
     q = _randn(gen, (B, T, H, K), dtype, qkv_std)
     k = _randn(gen, (B, T, H, K), dtype, qkv_std)
-    v = _randn(gen, (B, T, H, V), dtype, qkv_std)
+    v = _randn(gen, (B, T, H, V), dtype, qkv_std if v_std is None else v_std)
     out = dict(q=q, k=k, v=v, g=None, g_head=None, a=None, dt_bias=None, A_log=None, beta=None, b=None,
                h0=None, cu_seqlens=cu_seqlens, N=N, B=B, T=T, H=H, K=K, V=V, dtype=dtype,
                gate=gate, beta_mode=beta, l2norm=l2norm, delta=delta,
@@ -85,6 +90,12 @@ def chunk_workload(*, seed=2, B=1, T=8192, H=32, K=128, V=128, dtype=torch.bfloa
         out["g"] = -_uniform(gen, (B, T, H, K), 0.01, 3.0)
     elif gate == "head":
         out["g_head"] = -_uniform(gen, (B, T, H), 0.01, 3.0)
+    elif gate == "g_extreme":
+        fast = torch.rand(H, K, generator=gen) < 0.5
+        hi = -_uniform(gen, (B, T, H, K), 8.0, 20.0)
+        lo = -_uniform(gen, (B, T, H, K), 0.01, 0.5)
+        out["g"] = torch.where(fast, hi, lo)
+        out["gate"] = "g"
     elif gate != "none":
         raise ValueError(f"unknown gate mode {gate!r}")
     if beta == "logits":
@@ -149,12 +160,12 @@ def decode_conv_workload(*, seed=6, W=4, bias=True, **kw):
 
 
 def recurrent_workload(*, seed=5, B=64, T=8, H=32, HV=32, K=128, V=128, num_slots=128,
-                       pad_frac=0.1, state_std=0.1, scale=None):
+                       pad_frac=0.1, state_std=0.1, scale=None, A_log_range=(0.0, 2.0)):
     """Inputs of one short-T recurrent step (T tokens per row on a slot pool).
 
     Draw order: q, k (bf16 [B, T, H, K] ~ N(0,1)), v (bf16 [B, T, HV, V] ~ N(0,1)),
     a (bf16 [B, T, HV*K] ~ N(0,1)), b (bf16 [B, T, HV] ~ N(0,1)), A_log (fp32 [HV]
-    ~ U(0,2)), dt_bias (fp32 [HV*K] ~ U(-1,1)), state pool (fp32 [num_slots, HV,
+    ~ U(A_log_range), default U(0,2)), dt_bias (fp32 [HV*K] ~ U(-1,1)), state pool (fp32 [num_slots, HV,
     V, K] ~ state_std N(0,1)), slot indices (randperm(num_slots)[:B]), pad
     positions (randperm(B)[:round(pad_frac*B + 0.5)] set to -1).
     """
@@ -164,7 +175,7 @@ def recurrent_workload(*, seed=5, B=64, T=8, H=32, HV=32, K=128, V=128, num_slot
     v = _randn(gen, (B, T, HV, V), torch.bfloat16)
     a = _randn(gen, (B, T, HV * K), torch.bfloat16)
     b = _randn(gen, (B, T, HV), torch.bfloat16)
-    A_log = _uniform(gen, (HV,), 0.0, 2.0)
+    A_log = _uniform(gen, (HV,), float(A_log_range[0]), float(A_log_range[1]))
     dt_bias = _uniform(gen, (HV * K,), -1.0, 1.0)
     pool = _randn(gen, (num_slots, HV, V, K), torch.float32, state_std)
     if B > num_slots:

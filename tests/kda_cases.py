@@ -17,6 +17,48 @@ BF16_MAX_ABS = 2e-2  # max abs error, bf16 inputs
 FP32_MAX_ABS = 1e-4  # max abs error, fp32 inputs
 
 
+GUARD_BYTES = 256   # canary band on each side of an output (a multiple of 16: keeps the output aligned)
+SENTINEL = 0xA5     # byte pattern of the bands
+
+
+class Canary:
+    """Output buffers with a band of GUARD_BYTES sentinel bytes on each side.
+
+    compute-sanitizer is not used on this hardware, so the tests catch stores
+    that land just outside an output this way: every output a test passes to the
+    library comes from here, and check() asserts, after the GPU work, that no
+    band byte changed (a ragged tail, a varlen boundary or an empty sequence
+    writing one row or one chunk too far would show up)."""
+
+    def __init__(self):
+        self._bufs = []
+
+    def empty(self, shape, dtype, device="cuda", name="out"):
+        el = torch.empty((), dtype=dtype).element_size()
+        n = 1
+        for x in shape:
+            n *= int(x)
+        pad = GUARD_BYTES // el
+        buf = torch.empty(n + 2 * pad, dtype=dtype, device=device)
+        buf.view(torch.uint8).fill_(SENTINEL)
+        self._bufs.append((name, buf, n * el))
+        return buf[pad:pad + n].view(*shape)
+
+    def clone(self, src, name="out"):
+        t = self.empty(tuple(src.shape), src.dtype, src.device, name)
+        t.copy_(src)
+        return t
+
+    def check(self):
+        torch.cuda.synchronize()
+        for name, buf, nbytes in self._bufs:
+            raw = buf.view(torch.uint8)
+            lo, hi = raw[:GUARD_BYTES], raw[GUARD_BYTES + nbytes:]
+            assert hi.numel() == GUARD_BYTES
+            assert bool((lo == SENTINEL).all()), f"{name}: bytes written before the start of the output"
+            assert bool((hi == SENTINEL).all()), f"{name}: bytes written past the end of the output"
+
+
 def np64(t):
     return None if t is None else t.detach().to("cpu", torch.float64).numpy()
 
@@ -30,12 +72,22 @@ def to_dev(wl, device="cuda"):
 
 
 def gpu_chunk(wl, *, h0=True, final_state=True, err=None, workspace=None, o=None, hT=None):
+    """The chunk forward through the C ABI. Outputs the caller does not pass come
+    with canary bands, checked (after a synchronize) before returning."""
     d = to_dev(wl)
-    return kda.kda_chunk_fwd(
+    cn = Canary()
+    N = (d["cu_seqlens"].numel() - 1) if d["cu_seqlens"] is not None else d["q"].shape[0]
+    if o is None:
+        o = cn.empty(tuple(d["q"].shape[:3]) + (d["v"].shape[-1],), d["q"].dtype, name="o")
+    if hT is None and final_state:
+        hT = cn.empty((N, d["q"].shape[2], d["v"].shape[-1], d["q"].shape[-1]), torch.float32, name="hT")
+    out = kda.kda_chunk_fwd(
         d["q"], d["k"], d["v"], scale=d["scale"], g=d["g"], a=d["a"], dt_bias=d["dt_bias"], A_log=d["A_log"],
         beta=d["beta"], b=d["b"], h0=d["h0"] if h0 else None, cu_seqlens=d["cu_seqlens"],
         l2norm_qk=d["l2norm"], delta=d["delta"], output_final_state=final_state, err=err, workspace=workspace,
         o=o, hT=hT, g_head=d.get("g_head"))
+    cn.check()
+    return out
 
 
 def oracle_chunk(wl, *, h0=True, chunk_size=None):

@@ -10,7 +10,7 @@ import kimi_delta_attention_04_gb300 as kda
 from kimi_delta_attention_04_gb300 import workloads as W
 from oracle import kda_oracle as ko
 
-from kda_cases import assert_close, np64, subset_heads, to_dev
+from kda_cases import Canary, assert_close, np64, subset_heads, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -37,9 +37,13 @@ def test_chunk_states_and_parallel_output(K, B, T, lengths, gate):
     wl = W.chunk_workload(seed=140 + K + (T or 7), B=B, T=T or 1, H=3, K=K, V=K, lengths=lengths, gate=gate)
     d = to_dev(wl)
     nc = kda.chunk_count(wl["B"], wl["T"], wl["cu_seqlens"])
-    hc = torch.full((nc, wl["H"], K, K), float("nan"), dtype=torch.float32, device="cuda")
-    o, hT = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], h0=d["h0"], h_chunks=hc, **_kw(d))
-    torch.cuda.synchronize()
+    cn = Canary()
+    hc = cn.empty((nc, wl["H"], K, K), torch.float32, name="h_chunks")
+    hc.fill_(float("nan"))
+    o = cn.empty(tuple(d["q"].shape[:3]) + (K,), torch.bfloat16, name="o")
+    hT = cn.empty((wl["N"], wl["H"], K, K), torch.float32, name="hT")
+    kda.kda_chunk_fwd(d["q"], d["k"], d["v"], h0=d["h0"], h_chunks=hc, o=o, hT=hT, **_kw(d))
+    cn.check()
     o_ref, h_ref, s_ref = ko.kda_forward(
         np64(wl["q"]), np64(wl["k"]), np64(wl["v"]), scale=wl["scale"], g=np64(wl["g"]), a=np64(wl["a"]),
         dt_bias=np64(wl["dt_bias"]), A_log=np64(wl["A_log"]), beta=np64(wl["beta"]), b=np64(wl["b"]),
@@ -50,8 +54,9 @@ def test_chunk_states_and_parallel_output(K, B, T, lengths, gate):
     assert_close("o (snapshot path)", np64(o), o_ref, torch.bfloat16)
     assert_close("hT (snapshot path)", np64(hT), h_ref, torch.bfloat16)
     # every chunk's output again, in parallel, from its snapshot
-    o2 = kda.kda_chunk_output(d["q"], d["k"], d["v"], hc, **_kw(d))
-    torch.cuda.synchronize()
+    o2 = cn.empty(tuple(o.shape), torch.bfloat16, name="o (output pass)")
+    kda.kda_chunk_output(d["q"], d["k"], d["v"], hc, o=o2, **_kw(d))
+    cn.check()
     assert_close("o (chunk-parallel pass)", np64(o2), o_ref, torch.bfloat16)
 
 
@@ -78,11 +83,15 @@ def test_chunk_states_full_size_sampled_heads():
     wl = W.prefill()
     d = to_dev(wl)
     nc = kda.chunk_count(1, wl["T"])
-    hc = torch.empty(nc, wl["H"], 128, 128, dtype=torch.float32, device="cuda")
-    o, hT = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], h0=d["h0"], h_chunks=hc, **_kw(d))
-    o2 = kda.kda_chunk_output(d["q"], d["k"], d["v"], hc, **_kw(d))
+    cn = Canary()
+    hc = cn.empty((nc, wl["H"], 128, 128), torch.float32, name="h_chunks")
+    o = cn.empty((1, wl["T"], wl["H"], 128), torch.bfloat16, name="o")
+    hT = cn.empty((1, wl["H"], 128, 128), torch.float32, name="hT")
+    o2 = cn.empty((1, wl["T"], wl["H"], 128), torch.bfloat16, name="o (output pass)")
+    kda.kda_chunk_fwd(d["q"], d["k"], d["v"], h0=d["h0"], h_chunks=hc, o=o, hT=hT, **_kw(d))
+    kda.kda_chunk_output(d["q"], d["k"], d["v"], hc, o=o2, **_kw(d))
     o_plain, _ = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], h0=d["h0"], **_kw(d))
-    torch.cuda.synchronize()
+    cn.check()
     assert_close("snapshot forward vs plain forward", np64(o), np64(o_plain), torch.bfloat16)
     heads = [2, 29]
     sub = subset_heads(wl, heads)

@@ -10,7 +10,7 @@ import kimi_delta_attention_04_gb300 as kda
 from kimi_delta_attention_04_gb300 import workloads as W
 from oracle import kda_oracle as ko
 
-from kda_cases import assert_close, np64
+from kda_cases import Canary, assert_close, np64
 
 pytestmark = pytest.mark.gpu
 
@@ -24,13 +24,15 @@ def _built():
 
 def _run(wl, in_place):
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in wl.items()}
-    pool = d["state_pool"].clone()
-    cs_in = d["conv_state"].clone()
-    cs_out = cs_in if in_place else cs_in.clone()
-    o = kda.kda_decode_conv_step(d["packed_qkv"], cs_in, d["conv_weight"], d["conv_bias"], d["a"], d["b"],
-                                 d["A_log"], d["dt_bias"], pool, d["indices"], H=wl["H"], HV=wl["HV"], K=wl["K"],
-                                 V=wl["V"], scale=wl["scale"], conv_state_out=cs_out)
-    torch.cuda.synchronize()
+    cn = Canary()
+    pool = cn.clone(d["state_pool"], "state pool")
+    cs_in = cn.clone(d["conv_state"], "conv state")
+    cs_out = cs_in if in_place else cn.clone(cs_in, "conv state out")
+    o = cn.empty((d["packed_qkv"].shape[0], wl["HV"], wl["V"]), torch.bfloat16, name="o")
+    kda.kda_decode_conv_step(d["packed_qkv"], cs_in, d["conv_weight"], d["conv_bias"], d["a"], d["b"],
+                             d["A_log"], d["dt_bias"], pool, d["indices"], H=wl["H"], HV=wl["HV"], K=wl["K"],
+                             V=wl["V"], scale=wl["scale"], conv_state_out=cs_out, o=o)
+    cn.check()
     return o, pool, cs_out
 
 

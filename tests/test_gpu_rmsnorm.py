@@ -10,7 +10,7 @@ import kimi_delta_attention_04_gb300 as kda
 from kimi_delta_attention_04_gb300 import workloads as W
 from oracle import kda_oracle as ko
 
-from kda_cases import gpu_chunk, np64
+from kda_cases import Canary, gpu_chunk, np64
 
 pytestmark = pytest.mark.gpu
 
@@ -35,8 +35,10 @@ def test_rmsnorm_random_rows(V):
     x[5, 1] = 0  # an all-zero row stays zero
     w = torch.rand(V, generator=gen) * 2 - 0.5
     xd, wd = x.cuda(), w.cuda()
-    y = kda.kda_head_rmsnorm(xd, wd, eps=1e-6)
-    torch.cuda.synchronize()
+    cn = Canary()
+    y = cn.empty(tuple(x.shape), torch.bfloat16, name="y")
+    kda.kda_head_rmsnorm(xd, wd, eps=1e-6, out=y)
+    cn.check()
     _check(y, x, w, 1e-6)
     assert torch.all(y[5, 1] == 0)
     kda.kda_head_rmsnorm(xd, wd, eps=1e-6, out=xd)  # in place

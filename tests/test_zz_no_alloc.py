@@ -4,9 +4,10 @@ Callers that may not allocate device memory when they run attention (graph
 recording or a fixed memory plan, runtimes that own every device byte, bindings
 without an allocator) use this entry point instead of kda_chunk_fwd with a
 workspace. These tests call it through the C ABI (via the ctypes binding) and
-check, on two calls in a row, that it gives what kda_chunk_fwd gives, within
-the tolerances of the parity tests. The file is named so that pytest collects
-it last; it also passes on its own in a fresh process.
+check, on two calls in a row, that it gives what kda_chunk_fwd gives and what
+the fp64 oracle gives, within the tolerances of the parity tests, with the
+device status word still clear. The file is named so that pytest collects it
+last; it also passes on its own in a fresh process.
 """
 
 import ctypes
@@ -19,7 +20,7 @@ import kimi_delta_attention_04_gb300 as kda
 from kimi_delta_attention_04_gb300 import _lib
 from kimi_delta_attention_04_gb300 import workloads as W
 
-from kda_cases import BF16_MAX_ABS, BF16_REL_F, FP32_MAX_ABS, max_abs, np64, rel_f, to_dev
+from kda_cases import BF16_MAX_ABS, BF16_REL_F, FP32_MAX_ABS, max_abs, np64, oracle_chunk, rel_f, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -37,7 +38,8 @@ def _kwargs(d):
 
 
 def _close(x, ref, dtype):
-    x, ref = np64(x), np64(ref)
+    x = np64(x) if isinstance(x, torch.Tensor) else x
+    ref = np64(ref) if isinstance(ref, torch.Tensor) else ref
     if dtype == torch.float32:
         assert max_abs(x, ref) <= FP32_MAX_ABS
     else:
@@ -57,13 +59,19 @@ CASES = {
 def test_noalloc_matches_workspace_entry_point(name):
     wl = CASES[name]()
     d = to_dev(wl)
-    o_ref, h_ref = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], **_kwargs(d))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o_ref, h_ref = kda.kda_chunk_fwd(d["q"], d["k"], d["v"], err=err, **_kwargs(d))
     torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    o_or, h_or = oracle_chunk(wl)
     for _ in range(2):  # two calls in a row share (and reuse) the one scratch buffer
-        o, h = kda.kda_chunk_fwd_noalloc(d["q"], d["k"], d["v"], **_kwargs(d))
+        o, h = kda.kda_chunk_fwd_noalloc(d["q"], d["k"], d["v"], err=err, **_kwargs(d))
         torch.cuda.synchronize()
+        assert int(err.item()) == 0
         _close(o, o_ref, wl["dtype"])
         _close(h, h_ref, wl["dtype"])
+        _close(o, o_or, wl["dtype"])  # and the fp64 oracle itself
+        _close(h, h_or, wl["dtype"])
         assert torch.isfinite(o.float()).all()
 
 

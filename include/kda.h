@@ -11,6 +11,7 @@
  *   kda_head_rmsnorm          output-side per-head RMSNorm of attention outputs
  *   kda_chunk_fwd_noalloc     kda_chunk_fwd on a library-owned scratch buffer (no allocation)
  *   kda_version               library version string
+ *   kda_selftest_*            diagnostics: bounded-wait failure path, tcgen05 round trip
  *
  * What is computed (per sequence n and head h; math state S is [dk, dv], stored
  * transposed as [dv, dk] with dk contiguous):
@@ -167,7 +168,11 @@ size_t kda_chunk_workspace_size(const kda_chunk_args* args);
 /*
  * Chunkwise KDA forward. Writes o (and hT when non-NULL). `workspace` is device
  * memory of at least kda_chunk_workspace_size(args) bytes, 256-byte aligned.
- * Returns KDA_OK once the work is enqueued.
+ * Returns KDA_OK once the work is enqueued. For bf16 with dk = dv = 128 the
+ * first call on a device also checks that the device cannot hold more of the
+ * fused kernel's 4-CTA clusters at once than the workspace has rings (40; a
+ * GB300 holds 38) and returns KDA_ERR_UNSUPPORTED, launching nothing, where it
+ * could.
  */
 kda_status kda_chunk_fwd(const kda_chunk_args* args, void* workspace, size_t workspace_bytes,
                          kda_stream_t stream);
@@ -356,6 +361,9 @@ kda_status kda_head_rmsnorm(const kda_rmsnorm_args* args, kda_stream_t stream);
  * All calls on a device share the one buffer: calls whose GPU work overlaps
  * (different streams, or other threads) race and corrupt each other; order
  * them on one stream or synchronise between them.
+ * The looked-up address is kept for the life of the process: do not use this
+ * entry point on a device after cudaDeviceReset (or any other destruction of
+ * its primary context) in the same process.
  */
 #define KDA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20) /* 16 MiB */
 kda_status kda_chunk_fwd_noalloc(const kda_chunk_args* args, kda_stream_t stream);
@@ -372,6 +380,43 @@ const char* kda_version(void);
  * failure path without a fault or a hang.
  */
 kda_status kda_selftest_bounded_wait(int32_t* err, uint64_t limit_ns, kda_stream_t stream);
+
+/*
+ * Diagnostic: one MMA of the 5th-generation tensor cores (tcgen05.mma,
+ * kind::f16, bf16 operands, fp32 accumulator in tensor memory) and its round
+ * trip. The method's pages have no counterpart; the chunk kernels use
+ * warp-level mma.sync, and this call measures what the tensor-memory path
+ * would cost them.
+ *
+ * One CTA computes d [128 x N] (fp32, row-major) = a [128 x K] * b^T, with a
+ * and b bf16 row-major device arrays ([128, K] and [N, K]). The operands are
+ * placed in shared memory in a K-major layout (no swizzle, or the 128-byte
+ * swizzle), A optionally copied on into tensor memory (a_from_tmem) and read
+ * from there; the result is read back with tcgen05.ld. Then `reps` round trips
+ * (issue -> commit seen on an mbarrier -> the first 16 columns in registers)
+ * are timed one by one, and `reps` MMA groups back to back under one commit.
+ *
+ * cycles (device int64[7], nullable) receives: [0] summed SM cycles from issue
+ * to the completion being seen, [1] summed cycles from issue to the data in
+ * registers, [2] cycles of the back-to-back burst (every group on the same
+ * accumulator), [3] reps, [4] cycles of a second burst of `reps` groups that
+ * rotates over [5] independent accumulators (0 when N leaves room for one),
+ * [6] cycles the issuing thread took to issue the first burst.
+ * K is 16, 32, 64 or 128; N a multiple of 16 in 16..256; layout 0 (none) or
+ * 1 (128-byte swizzle); 0 <= reps <= 4096. Pointers 16-byte aligned (err:
+ * 4-byte, may be NULL). Every wait is bounded: a wait that runs out writes
+ * KDA_ERR_TIMEOUT to *err and the kernel returns after freeing its tensor
+ * memory. Uses all of one SM's tensor memory while it runs.
+ */
+typedef struct kda_tcgen05_probe_args {
+  int32_t K, N, layout, a_from_tmem, reps;
+  const void* a;       /* bf16 [128, K] */
+  const void* b;       /* bf16 [N, K] */
+  float* d;            /* fp32 [128, N], written */
+  long long* cycles;   /* int64 [7] or NULL */
+  int32_t* err;        /* or NULL */
+} kda_tcgen05_probe_args;
+kda_status kda_selftest_tcgen05(const kda_tcgen05_probe_args* args, kda_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -97,9 +97,17 @@ class RmsNormArgs(ctypes.Structure):
     ]
 
 
+class Tcgen05ProbeArgs(ctypes.Structure):
+    _fields_ = [
+        ("K", ctypes.c_int32), ("N", ctypes.c_int32), ("layout", ctypes.c_int32), ("a_from_tmem", ctypes.c_int32),
+        ("reps", ctypes.c_int32), ("a", ctypes.c_void_p), ("b", ctypes.c_void_p), ("d", ctypes.c_void_p),
+        ("cycles", ctypes.c_void_p), ("err", ctypes.c_void_p),
+    ]
+
+
 EXPORTS = ("kda_chunk_fwd", "kda_chunk_output", "kda_chunk_fwd_noalloc", "kda_chunk_workspace_size", "kda_decode_step",
            "kda_decode_conv_step", "kda_recurrent_step", "kda_head_rmsnorm", "kda_version",
-           "kda_selftest_bounded_wait")
+           "kda_selftest_bounded_wait", "kda_selftest_tcgen05")
 
 
 def lib_path() -> Path:
@@ -137,6 +145,8 @@ def load() -> ctypes.CDLL:
         lib.kda_version.argtypes = []
         lib.kda_selftest_bounded_wait.restype = ctypes.c_int
         lib.kda_selftest_bounded_wait.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]
+        lib.kda_selftest_tcgen05.restype = ctypes.c_int
+        lib.kda_selftest_tcgen05.argtypes = [ctypes.POINTER(Tcgen05ProbeArgs), ctypes.c_void_p]
         _lib = lib
         return lib
 
@@ -149,9 +159,33 @@ def selftest_bounded_wait(err, limit_ns, stream=None):
     """Run the bounded-wait self-test kernel: it waits on an mbarrier that nothing
     arrives on, gives up after limit_ns and writes KDA_ERR_TIMEOUT to err
     (a device int32 tensor). See include/kda.h."""
-    st = load().kda_selftest_bounded_wait(_ptr(err), ctypes.c_uint64(int(limit_ns)), _stream_ptr(stream))
+    with _on_device(err):
+        st = load().kda_selftest_bounded_wait(_ptr(err), ctypes.c_uint64(int(limit_ns)), _stream_ptr(stream, err.device))
     if st != KDA_OK:
         raise KdaError(st, "kda_selftest_bounded_wait")
+
+
+def selftest_tcgen05(a, b, *, layout=0, a_from_tmem=False, reps=0, err=None, stream=None):
+    """One tcgen05 MMA, d [128, N] = a [128, K] @ b[N, K]^T (bf16 in, fp32 out),
+    and its timed round trips (see include/kda.h). Returns (d, cycles) with
+    cycles an int64 CUDA tensor [7]: summed issue->done and issue->data cycles
+    over `reps` round trips, the cycles of a burst of `reps` back-to-back
+    groups on one accumulator, reps, the cycles of a burst over independent
+    accumulators and their count, and the issuing thread's own cycles for the
+    first burst."""
+    K, N = int(a.shape[1]), int(b.shape[0])
+    if a.shape[0] != 128 or b.shape[1] != K or a.dtype != torch.bfloat16 or b.dtype != torch.bfloat16:
+        raise ValueError("expects bf16 a [128, K] and b [N, K]")
+    d = torch.empty(128, N, dtype=torch.float32, device=a.device)
+    cycles = torch.zeros(7, dtype=torch.int64, device=a.device)
+    args = Tcgen05ProbeArgs()
+    args.K, args.N, args.layout, args.a_from_tmem, args.reps = K, N, int(layout), int(bool(a_from_tmem)), int(reps)
+    args.a, args.b, args.d, args.cycles, args.err = _ptr(a), _ptr(b), _ptr(d), _ptr(cycles), _ptr(err)
+    with _on_device(a):
+        st = load().kda_selftest_tcgen05(ctypes.byref(args), _stream_ptr(stream, a.device))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_selftest_tcgen05")
+    return d, cycles
 
 
 def _ptr(t):
@@ -166,10 +200,21 @@ def _ptr(t):
     return t.data_ptr()
 
 
-def _stream_ptr(stream):
+def _stream_ptr(stream, device=None):
+    """The stream to enqueue on: the given one, else the current stream of
+    `device` (the device of the call's tensors)."""
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _on_device(t):
+    """Context in which a C call runs: the device of tensor t is made current,
+    so the library's per-device state (kernel attributes, the no-allocation
+    scratch address) and its launches refer to the device that holds the data."""
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("libkda works on CUDA tensors only (no CPU fallback)")
+    return torch.cuda.device(t.device)
 
 
 def _dtype_code(dt: torch.dtype) -> int:
@@ -246,12 +291,14 @@ def kda_chunk_fwd(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log=None, b
                            h0=h0, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk, delta=delta, o=o, hT=hT,
                            err=err, g_head=g_head, h_chunks=h_chunks)
     need = int(lib.kda_chunk_workspace_size(ctypes.byref(args)))
-    if need == 0:
-        st = lib.kda_chunk_fwd(ctypes.byref(args), None, 0, _stream_ptr(stream))
-        raise KdaError(st if st != KDA_OK else KDA_ERR_INVALID_ARG, "kda_chunk_fwd")
-    if workspace is None or workspace.numel() * workspace.element_size() < need:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    st = lib.kda_chunk_fwd(ctypes.byref(args), ctypes.c_void_p(_ptr(workspace)), need, _stream_ptr(stream))
+    with _on_device(q):
+        if need == 0:
+            st = lib.kda_chunk_fwd(ctypes.byref(args), None, 0, _stream_ptr(stream, q.device))
+            raise KdaError(st if st != KDA_OK else KDA_ERR_INVALID_ARG, "kda_chunk_fwd")
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        st = lib.kda_chunk_fwd(ctypes.byref(args), ctypes.c_void_p(_ptr(workspace)), need,
+                               _stream_ptr(stream, q.device))
     if st != KDA_OK:
         raise KdaError(st, "kda_chunk_fwd")
     return o, hT
@@ -275,7 +322,8 @@ def kda_chunk_fwd_noalloc(q, k, v, *, scale, g=None, a=None, dt_bias=None, A_log
     args = make_chunk_args(q, k, v, scale=scale, g=g, a=a, dt_bias=dt_bias, A_log=A_log, beta=beta, b=b,
                            h0=h0, cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk, delta=delta, o=o, hT=hT,
                            err=err, g_head=g_head, h_chunks=h_chunks)
-    st = lib.kda_chunk_fwd_noalloc(ctypes.byref(args), _stream_ptr(stream))
+    with _on_device(q):
+        st = lib.kda_chunk_fwd_noalloc(ctypes.byref(args), _stream_ptr(stream, q.device))
     if st != KDA_OK:
         raise KdaError(st, "kda_chunk_fwd_noalloc")
     return o, hT
@@ -305,7 +353,8 @@ def kda_decode_step(packed_qkv, a, b, A_log, dt_bias, state_pool, indices, *, H,
         o = torch.empty(packed_qkv.shape[0], HV, V, dtype=torch.bfloat16, device=packed_qkv.device)
     args = make_decode_args(packed_qkv, a, b, A_log, dt_bias, state_pool, indices, H=H, HV=HV, K=K, V=V,
                             scale=scale, l2norm_qk=l2norm_qk, o=o, err=err, check_indices=check_indices)
-    st = lib.kda_decode_step(ctypes.byref(args), _stream_ptr(stream))
+    with _on_device(packed_qkv):
+        st = lib.kda_decode_step(ctypes.byref(args), _stream_ptr(stream, packed_qkv.device))
     if st != KDA_OK:
         raise KdaError(st, "kda_decode_step")
     return o
@@ -335,7 +384,8 @@ def kda_recurrent_step(q, k, v, a, b, A_log, dt_bias, state_pool, indices, *, sc
         o = torch.empty(q.shape[0], q.shape[1], v.shape[2], v.shape[3], dtype=torch.bfloat16, device=q.device)
     args = make_recurrent_args(q, k, v, a, b, A_log, dt_bias, state_pool, indices, scale=scale,
                                l2norm_qk=l2norm_qk, o=o, err=err, check_indices=check_indices)
-    st = lib.kda_recurrent_step(ctypes.byref(args), _stream_ptr(stream))
+    with _on_device(q):
+        st = lib.kda_recurrent_step(ctypes.byref(args), _stream_ptr(stream, q.device))
     if st != KDA_OK:
         raise KdaError(st, "kda_recurrent_step")
     return o
@@ -352,7 +402,8 @@ def kda_head_rmsnorm(x, weight, *, eps, out=None, stream=None):
     args.R = int(x.numel() // max(args.V, 1))
     args.eps = float(eps)
     args.x, args.weight, args.y = _ptr(x), _ptr(weight), _ptr(out)
-    st = lib.kda_head_rmsnorm(ctypes.byref(args), _stream_ptr(stream))
+    with _on_device(x):
+        st = lib.kda_head_rmsnorm(ctypes.byref(args), _stream_ptr(stream, x.device))
     if st != KDA_OK:
         raise KdaError(st, "kda_head_rmsnorm")
     return out
@@ -376,7 +427,8 @@ def kda_decode_conv_step(mixed_qkv, conv_state_in, conv_weight, conv_bias, a, b,
     args.conv_state_in = _ptr(conv_state_in)
     args.conv_state_out = _ptr(conv_state_in if conv_state_out is None else conv_state_out)
     args.conv_weight, args.conv_bias = _ptr(conv_weight), _ptr(conv_bias)
-    st = lib.kda_decode_conv_step(ctypes.byref(args), _stream_ptr(stream))
+    with _on_device(mixed_qkv):
+        st = lib.kda_decode_conv_step(ctypes.byref(args), _stream_ptr(stream, mixed_qkv.device))
     if st != KDA_OK:
         raise KdaError(st, "kda_decode_conv_step")
     return o
@@ -403,12 +455,14 @@ def kda_chunk_output(q, k, v, h_chunks, *, scale, g=None, a=None, dt_bias=None, 
                            cu_seqlens=cu_seqlens, l2norm_qk=l2norm_qk, delta=delta, o=o, err=err, g_head=g_head,
                            h_chunks=h_chunks)
     need = int(lib.kda_chunk_workspace_size(ctypes.byref(args)))
-    if need == 0:
-        st = lib.kda_chunk_output(ctypes.byref(args), None, 0, _stream_ptr(stream))
-        raise KdaError(st if st != KDA_OK else KDA_ERR_INVALID_ARG, "kda_chunk_output")
-    if workspace is None or workspace.numel() * workspace.element_size() < need:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    st = lib.kda_chunk_output(ctypes.byref(args), ctypes.c_void_p(_ptr(workspace)), need, _stream_ptr(stream))
+    with _on_device(q):
+        if need == 0:
+            st = lib.kda_chunk_output(ctypes.byref(args), None, 0, _stream_ptr(stream, q.device))
+            raise KdaError(st if st != KDA_OK else KDA_ERR_INVALID_ARG, "kda_chunk_output")
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        st = lib.kda_chunk_output(ctypes.byref(args), ctypes.c_void_p(_ptr(workspace)), need,
+                                  _stream_ptr(stream, q.device))
     if st != KDA_OK:
         raise KdaError(st, "kda_chunk_output")
     return o

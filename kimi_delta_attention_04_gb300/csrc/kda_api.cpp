@@ -142,9 +142,15 @@ kda_status run_chunk(const kda_chunk_args* args, void* workspace, size_t ws_byte
   cudaError_t e = cudaSuccess;
   if (geo.cu_seqlens != nullptr) e = kda::launch_plan(c, s);
   if (e == cudaSuccess) {
-    if (uses_fused(*args)) e = kda::launch_chunk_fused(c, s);
-    else if (output_pass) e = kda::launch_chunk_output_tc(c, s);
-    else e = args->dtype == KDA_DTYPE_BF16 ? kda::launch_chunk_tc(c, s) : kda::launch_chunk_f32(c, s);
+    if (uses_fused(*args)) {
+      e = kda::launch_chunk_fused(c, s);
+      // the fused kernel's ring pool is too small for this device's residency
+      if (e == cudaErrorNotSupported) return KDA_ERR_UNSUPPORTED;
+    } else if (output_pass) {
+      e = kda::launch_chunk_output_tc(c, s);
+    } else {
+      e = args->dtype == KDA_DTYPE_BF16 ? kda::launch_chunk_tc(c, s) : kda::launch_chunk_f32(c, s);
+    }
   }
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
@@ -319,6 +325,22 @@ kda_status kda_selftest_bounded_wait(int32_t* err, uint64_t limit_ns, kda_stream
   if (err == nullptr || !aligned(err, 4)) return KDA_ERR_INVALID_ARG;
   if (limit_ns < 1000 || limit_ns > UINT64_C(10000000000)) return KDA_ERR_INVALID_ARG;
   const cudaError_t e = kda::launch_wait_selftest(err, limit_ns, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_selftest_tcgen05(const kda_tcgen05_probe_args* a, kda_stream_t stream) {
+  if (a == nullptr) return KDA_ERR_INVALID_ARG;
+  if (a->K != 16 && a->K != 32 && a->K != 64 && a->K != 128) return KDA_ERR_INVALID_ARG;
+  if (a->N < 16 || a->N > 256 || a->N % 16 != 0) return KDA_ERR_INVALID_ARG;
+  if (a->layout != 0 && a->layout != 1) return KDA_ERR_INVALID_ARG;
+  if (a->a_from_tmem != 0 && a->a_from_tmem != 1) return KDA_ERR_INVALID_ARG;
+  if (a->reps < 0 || a->reps > 4096) return KDA_ERR_INVALID_ARG;
+  if (!a->a || !a->b || !a->d) return KDA_ERR_INVALID_ARG;
+  if (!aligned(a->a, 16) || !aligned(a->b, 16) || !aligned(a->d, 16)) return KDA_ERR_INVALID_ARG;
+  if (a->cycles && !aligned(a->cycles, 8)) return KDA_ERR_INVALID_ARG;
+  if (a->err && !aligned(a->err, 4)) return KDA_ERR_INVALID_ARG;
+  const cudaError_t e = kda::launch_tc05_probe(a->a, a->b, a->d, a->K, a->N, a->layout, a->a_from_tmem, a->reps,
+                                               a->cycles, a->err, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -150,9 +150,10 @@ __device__ __forceinline__ uint32_t smem_u32(const void* ptr) {
 }
 
 // Takes a free ring of the workspace pool (a 64-bit map, cleared before the
-// launch). At most ~38 clusters of this kernel are resident at once, fewer
-// than kPool, so a ring frees up at the latest when a running cluster ends; the
-// wait is bounded all the same. Returns -1 (and reports a timeout) on failure.
+// launch). The launcher has checked that at most kPool clusters of this kernel
+// can be resident at once (~38 on GB300), so a ring is free whenever a cluster
+// starts; the wait is bounded all the same. Returns -1 (and reports a timeout)
+// on failure.
 __device__ int claim_ring(unsigned char* pool, int32_t* err) {
   unsigned int* bits = reinterpret_cast<unsigned int*>(pool);
   const uint64_t t0 = global_timer_ns();
@@ -784,13 +785,44 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
   }
 }
 
+// The workspace holds kPool rings and every resident cluster holds one, so at
+// most kPool clusters of the kernel may be resident at once (a cluster that
+// found no free ring would wait out its bounded claim and report a timeout).
+// Checked once per device with the occupancy calculator; a device that could
+// hold more is refused with cudaErrorNotSupported (KDA_ERR_UNSUPPORTED).
+template <typename Kernel>
+cudaError_t check_cluster_residency_once(Kernel kernel, size_t smem, std::atomic<uint64_t>& ok_devs,
+                                         std::atomic<uint64_t>& bad_devs) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t{1} << dev) : 0;
+  if (bit != 0 && (ok_devs.load(std::memory_order_acquire) & bit) != 0) return cudaSuccess;
+  if (bit != 0 && (bad_devs.load(std::memory_order_acquire) & bit) != 0) return cudaErrorNotSupported;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kCtas * 64, 1, 1);
+  cfg.blockDim = dim3(kFusedThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;  // the cluster shape is the kernel's compile-time one
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+  if (e != cudaSuccess) return e;
+  if (clusters > kPool) {
+    bad_devs.fetch_or(bit, std::memory_order_acq_rel);
+    return cudaErrorNotSupported;
+  }
+  ok_devs.fetch_or(bit, std::memory_order_acq_rel);
+  return cudaSuccess;
+}
+
 template <bool DELTA, bool L2N, int MODE>
 cudaError_t launch_fused_t(const ChunkCall& c, cudaStream_t s) {
   using QK = std::conditional_t<L2N, F16, Bf16>;
   const size_t smem = sizeof(FusedSmem<typename QK::T>);
-  static std::atomic<uint64_t> smem_set{0};
+  static std::atomic<uint64_t> smem_set{0}, resident_ok{0}, resident_bad{0};
   {
-    const cudaError_t e = set_smem_limit_once(kda_chunk_fused_kernel<DELTA, L2N, MODE>, smem, smem_set);
+    cudaError_t e = set_smem_limit_once(kda_chunk_fused_kernel<DELTA, L2N, MODE>, smem, smem_set);
+    if (e != cudaSuccess) return e;
+    e = check_cluster_residency_once(kda_chunk_fused_kernel<DELTA, L2N, MODE>, smem, resident_ok, resident_bad);
     if (e != cudaSuccess) return e;
   }
   const unsigned grid = static_cast<unsigned>(c.geo.N) * static_cast<unsigned>(c.geo.H) * kCtas;

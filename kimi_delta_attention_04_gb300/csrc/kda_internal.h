@@ -116,5 +116,7 @@ cudaError_t launch_recurrent(const RecurrentCall& c, cudaStream_t s);
 cudaError_t launch_recurrent_tc(const RecurrentCall& c, cudaStream_t s);  // T tokens as chunks, tensor cores
 cudaError_t launch_recurrent_fma(const RecurrentCall& c, cudaStream_t s);  // T tokens one by one, CUDA cores
 cudaError_t launch_rmsnorm(const RmsNormCall& c, cudaStream_t s);
+cudaError_t launch_tc05_probe(const void* a, const void* b, float* d, int K, int N, int layout, int a_tmem,
+                              int reps, long long* cycles, int32_t* err, cudaStream_t s);
 
 }  // namespace kda

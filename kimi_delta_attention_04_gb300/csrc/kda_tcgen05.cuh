@@ -1,0 +1,118 @@
+// 5th-generation tensor-core (tcgen05) primitives for sm_103a: tensor-memory
+// (TMEM) allocation, shared-memory matrix descriptors, the instruction
+// descriptor of kind::f16, the MMA itself (operands from shared memory, or A
+// from tensor memory), commit to an mbarrier, and TMEM loads and stores.
+//
+// Conventions (PTX ISA, tcgen05 family):
+//  * an MMA of shape M x N x 16 (bf16 / f16 operands) is issued by ONE thread;
+//    D lives in TMEM: for M = 128 and cta_group::1, row i of D is TMEM lane i
+//    and column j is TMEM column (base + j), fp32;
+//  * warp w of the CTA may load / store only TMEM lanes 32 (w % 4) .. + 31;
+//  * shared-memory operands are described by 64-bit descriptors; this file
+//    writes K-major layouts only, either without swizzle (8 x 16-byte core
+//    matrices, LBO = stride between core matrices along K, SBO = stride between
+//    8-row groups) or with the 128-byte swizzle (rows of 128 bytes, 16-byte
+//    chunk c of row r stored at chunk c ^ (r % 8) of a 1024-byte-aligned atom,
+//    SBO = 1024);
+//  * writes to shared memory by ordinary stores reach the tensor core only after
+//    fence.proxy.async.shared::cta and a barrier with the issuing thread.
+#pragma once
+
+#include <stdint.h>
+
+#include "kda_common.cuh"
+
+namespace kda {
+namespace tc05 {
+
+constexpr uint32_t kSwizzleNone = 0;
+constexpr uint32_t kSwizzle128B = 2;
+
+// Shared-memory matrix descriptor: start address, LBO and SBO in 16-byte units;
+// bits 46-47 = 1 (descriptor version of the sm_100 family); bits 61-63 layout.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t smem_addr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                              uint32_t layout) {
+  uint64_t d = static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= uint64_t{1} << 46;
+  d |= static_cast<uint64_t>(layout & 7u) << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16 with fp32 accumulation and K-major A and
+// B: bits 4-5 D format (1 = f32), 7-9 A format and 10-12 B format (0 = f16,
+// 1 = bf16), 17-22 N / 8, 24-28 M / 16.
+__host__ __device__ constexpr uint32_t idesc_f16kind(int M, int N, bool bf16) {
+  return (1u << 4) | (bf16 ? (1u << 7) | (1u << 10) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// TMEM allocation: executed by one whole warp; the base address is written to
+// *dst (shared memory). ncols is a power of two, 32 .. 512.
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void fence_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D (+)= A B^T with A [M x 16] and B [N x 16] both from shared memory.
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// The same with A [M x 16] read from tensor memory (lane = row, 8 columns of
+// packed 16-bit pairs).
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives (once) on a shared-memory mbarrier when every MMA this thread issued
+// before has completed.
+__device__ __forceinline__ void commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+// 16 consecutive 32-bit columns of this warp's 32 lanes, waited for in the same
+// statement (so no use of the registers can be scheduled before the wait).
+__device__ __forceinline__ void ld16_wait(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// 8 consecutive 32-bit columns of this warp's 32 lanes, waited for.
+__device__ __forceinline__ void st8_wait(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n"
+      "tcgen05.wait::st.sync.aligned;\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
+
+}  // namespace tc05
+}  // namespace kda

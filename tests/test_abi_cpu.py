@@ -53,6 +53,7 @@ def test_struct_layout_matches_c(tmp_path):
     fields_r = [f for f, _ in _lib.RecurrentArgs._fields_]
     fields_n = [f for f, _ in _lib.RmsNormArgs._fields_]
     fields_c2 = [f for f, _ in _lib.DecodeConvArgs._fields_]
+    fields_p = [f for f, _ in _lib.Tcgen05ProbeArgs._fields_]
     lines = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void){"]
     lines.append('printf("chunk %zu\\n", sizeof(kda_chunk_args));')
     for f in fields_c:
@@ -70,6 +71,9 @@ def test_struct_layout_matches_c(tmp_path):
         lines.append(f'printf("dc.{f} %zu\\n", offsetof(kda_decode_conv_args, {f}));')
     for f in fields_n:
         lines.append(f'printf("n.{f} %zu\\n", offsetof(kda_rmsnorm_args, {f}));')
+    lines.append('printf("probe %zu\\n", sizeof(kda_tcgen05_probe_args));')
+    for f in fields_p:
+        lines.append(f'printf("p.{f} %zu\\n", offsetof(kda_tcgen05_probe_args, {f}));')
     lines.append("return 0;}")
     src.write_text("\n".join(lines))
     exe = tmp_path / "layout"
@@ -92,6 +96,9 @@ def test_struct_layout_matches_c(tmp_path):
         assert int(got[f"dc.{f}"]) == getattr(_lib.DecodeConvArgs, f).offset, f
     for f in fields_n:
         assert int(got[f"n.{f}"]) == getattr(_lib.RmsNormArgs, f).offset, f
+    assert int(got["probe"]) == ctypes.sizeof(_lib.Tcgen05ProbeArgs)
+    for f in fields_p:
+        assert int(got[f"p.{f}"]) == getattr(_lib.Tcgen05ProbeArgs, f).offset, f
 
 
 # --- host-side validation, exercised with fake (never dereferenced) pointers ---
@@ -177,6 +184,26 @@ def test_selftest_bounded_wait_validation(lib):
     assert f(ctypes.c_void_p(FAKE + 2), 1_000_000, None) == _lib.KDA_ERR_INVALID_ARG
     assert f(ctypes.c_void_p(FAKE), 999, None) == _lib.KDA_ERR_INVALID_ARG
     assert f(ctypes.c_void_p(FAKE), 10_000_000_001, None) == _lib.KDA_ERR_INVALID_ARG
+
+
+def _probe(**over):
+    a = _lib.Tcgen05ProbeArgs()
+    a.K, a.N, a.layout, a.a_from_tmem, a.reps = 16, 64, 0, 0, 10
+    a.a = a.b = a.d = a.cycles = a.err = FAKE
+    for k, v in over.items():
+        setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("over", [dict(K=8), dict(K=48), dict(K=256), dict(N=8), dict(N=24), dict(N=272),
+                                  dict(layout=2), dict(a_from_tmem=2), dict(reps=-1), dict(reps=4097),
+                                  dict(a=None), dict(b=None), dict(d=None), dict(a=FAKE + 8), dict(d=FAKE + 4),
+                                  dict(cycles=FAKE + 4), dict(err=FAKE + 2)])
+def test_selftest_tcgen05_validation(lib, over):
+    """The tcgen05 probe checks its shape, layout and pointers before launching."""
+    a = _probe(**over)
+    assert lib.kda_selftest_tcgen05(ctypes.byref(a), None) == _lib.KDA_ERR_INVALID_ARG
+    assert lib.kda_selftest_tcgen05(None, None) == _lib.KDA_ERR_INVALID_ARG
 
 
 def test_chunk_output_needs_states(lib):

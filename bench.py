@@ -13,9 +13,12 @@ host buffers, the oracle's CPU throughput and the clocks seen while timing.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
---impl reference times the fp64 CPU oracle on a bounded sample of the same
-workload (the reference arm of this benchmark). Under torchrun each rank runs
-its own replica of the workload (weak scaling; the path needs no collective).
+--impl reference times the fp64 CPU oracle as it stands (the reference arm
+of this benchmark): whole steps of the same workload (the full prefill forward,
+then the full decode step), spread over every host core by a process pool
+(prefill by heads, decode by rows). cpu_baseline in the GPU arm's line is the
+same oracle on the same cores. Under torchrun each rank runs its own replica
+of the workload (weak scaling; the path needs no collective).
 """
 
 from __future__ import annotations
@@ -198,6 +201,162 @@ def max_over_ranks(values, device):
     return t.tolist()
 
 
+def bench_config(world):
+    """The `config` object of the benchmark line, the same for both arms."""
+    return {"workload": WORKLOAD, "global_batch": world, "seq_len": PREFILL_T,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (prefill 403 MB, decode ~964 MB touched); no flush",
+            "step": "one chunk forward (prefill) then one decode step (B=256)"}
+
+
+# --- the fp64 oracle on the host cores: a process pool over heads (prefill) and
+# rows (decode). Workers are started with `spawn` (safe after CUDA is in use)
+# and run numpy/torch single-threaded, one worker per core. ---
+
+def _pool_init():
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    sys.path.insert(0, str(ROOT))
+    import torch
+    torch.set_num_threads(1)
+
+
+_SHM = {}  # worker side: shared arrays attached once, by name
+
+
+def _shared(spec):
+    """Worker: numpy view of a shared-memory array (name, shape, dtype)."""
+    import numpy as np
+    from multiprocessing import shared_memory
+    name, shape, dtype = spec
+    if name not in _SHM:
+        shm = shared_memory.SharedMemory(name=name)
+        _SHM[name] = (shm, np.ndarray(shape, dtype=dtype, buffer=shm.buf))
+    return _SHM[name][1]
+
+
+def _oracle_prefill_part(task):
+    """Worker: the token-recurrence oracle on some heads of the prefill; seconds."""
+    from oracle import kda_oracle as ko
+    specs, heads, scale = task
+    q, k, v, a, dt_bias, A_log, b, h0 = (_shared(x) for x in specs)
+    T, H, K = q.shape[1], q.shape[2], q.shape[3]
+    t0 = time.perf_counter()
+    ko.kda_forward(q[:, :, heads], k[:, :, heads], v[:, :, heads], scale=scale,
+                   a=a.reshape(1, T, H, K)[:, :, heads].reshape(1, T, -1),
+                   dt_bias=dt_bias.reshape(H, K)[heads].reshape(-1), A_log=A_log[heads], b=b[:, :, heads],
+                   h0=h0[:, heads], l2norm_qk=True)
+    return time.perf_counter() - t0
+
+
+def _oracle_decode_part(task):
+    """Worker: the decode oracle on some rows (their slots compacted); seconds."""
+    from oracle import kda_oracle as ko
+    specs, rows, local, dims = task
+    packed, a, b, A_log, dt_bias, pool, idx = (_shared(x) for x in specs)
+    slots = idx[rows]
+    sub = pool[slots[slots >= 0]]
+    t0 = time.perf_counter()
+    ko.kda_decode(packed[rows], a[rows], b[rows], A_log, dt_bias, sub, local, **dims)
+    return time.perf_counter() - t0
+
+
+class OracleCpu:
+    """The oracle spread over `cores` worker processes: prefill by heads, decode
+    by rows. Inputs are the benchmark's own seeded workloads (first T tokens),
+    placed once in shared memory, so a timed map only sends indices."""
+
+    def __init__(self, T=PREFILL_T, cores=None, with_decode=True):
+        import multiprocessing as mp
+
+        import numpy as np
+        from multiprocessing import shared_memory
+
+        from kimi_delta_attention_04_gb300 import workloads as W
+        self.cores = int(cores or os.cpu_count() or 1)
+        self.T = T
+        self._shm = []
+
+        def put(t):
+            x = np.ascontiguousarray(t.float().numpy() if t.dtype != __import__("torch").int32 else t.numpy())
+            shm = shared_memory.SharedMemory(create=True, size=max(x.nbytes, 1))
+            np.ndarray(x.shape, dtype=x.dtype, buffer=shm.buf)[...] = x
+            self._shm.append(shm)
+            return (shm.name, x.shape, x.dtype.str)
+
+        wl = W.prefill(T=T)
+        pspecs = tuple(put(wl[n]) for n in ("q", "k", "v", "a", "dt_bias", "A_log", "b", "h0"))
+        H = wl["H"]
+        self.prefill_tasks = [(pspecs, list(range(H))[i::self.cores], wl["scale"])
+                              for i in range(min(self.cores, H))]
+        self.decode_tasks = []
+        self.decode_rows = 0
+        if with_decode:
+            dw = W.decode()
+            dspecs = tuple(put(dw[n]) for n in ("packed_qkv", "a", "b", "A_log", "dt_bias", "state_pool", "indices"))
+            dims = dict(H=dw["H"], HV=dw["HV"], K=dw["K"], V=dw["V"], scale=dw["scale"])
+            idx = dw["indices"].tolist()
+            for i in range(self.cores):
+                rows = list(range(dw["B"]))[i::self.cores]
+                if not rows:
+                    continue
+                local, j = [], 0
+                for r in rows:  # slots renumbered over the rows' compacted pool
+                    local.append(j if idx[r] >= 0 else -1)
+                    j += idx[r] >= 0
+                self.decode_tasks.append((dspecs, rows, np.array(local), dims))
+                self.decode_rows += len(rows)
+            del dw
+        del wl
+        self.pool = mp.get_context("spawn").Pool(self.cores, initializer=_pool_init)
+
+    def prefill_seconds(self):
+        t0 = time.perf_counter()
+        self.pool.map(_oracle_prefill_part, self.prefill_tasks, chunksize=1)
+        return time.perf_counter() - t0
+
+    def decode_seconds(self):
+        if not self.decode_tasks:
+            return 0.0
+        t0 = time.perf_counter()
+        self.pool.map(_oracle_decode_part, self.decode_tasks, chunksize=1)
+        return time.perf_counter() - t0
+
+    def close(self):
+        self.pool.close()
+        self.pool.join()
+        for shm in self._shm:
+            shm.close()
+            shm.unlink()
+        self._shm = []
+
+
+def oracle_parallel_baseline(budget_s=20.0):
+    """cpu_baseline: the token-recurrence oracle on all host cores over the full
+    prefill (all 8192 tokens, all 32 heads), or its first tokens if one run would
+    exceed budget_s. Returns (tokens/s, sample text, cores)."""
+    cores = int(os.cpu_count() or 1)
+    T = PREFILL_T
+    # calibrate on 64 tokens in parallel, then size the run to the budget
+    cal = OracleCpu(T=64, cores=cores, with_decode=False)
+    try:
+        cal.prefill_seconds()  # warm the workers (imports)
+        per_tok = cal.prefill_seconds() / 64
+    finally:
+        cal.close()
+    T = int(max(256, min(PREFILL_T, budget_s / max(per_tok, 1e-9))))
+    T -= T % 16
+    oc = OracleCpu(T=T, cores=cores, with_decode=False)
+    try:
+        oc.prefill_seconds()
+        dt = oc.prefill_seconds()
+    finally:
+        oc.close()
+    sample = (f"fp64 token-recurrence oracle, first {T} of 8192 tokens of the prefill workload, all 32 heads "
+              f"split over {cores} worker processes (one per host core, one thread each), {dt:.2f} s wall")
+    return T / dt, sample, cores
+
+
 def oracle_sample(T_sample=None, budget_s=20.0, chunk_size=None):
     """Time the fp64 oracle (as it stands: the token recurrence, or with
     chunk_size its chunked form) on the first tokens of the prefill workload,
@@ -232,25 +391,44 @@ def oracle_sample(T_sample=None, budget_s=20.0, chunk_size=None):
 
 
 def run_reference(args):
+    """The reference arm: the fp64 oracle as it stands, on the host cores of this
+    machine, timing whole steps of the same workload (one full prefill forward
+    and one full decode step per step), with the GPU arm's config."""
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    budget = max(1.0, args.ref_budget / max(args.steps + args.warmup, 1))
-    vals = []
-    sample = ""
-    for i in range(args.warmup + args.steps):
-        v, sample, cores = oracle_sample(budget_s=budget)
-        if i >= args.warmup:
-            vals.append(v)
-    value = statistics.median(vals)
+    T = args.ref_seq_len
+    oc = OracleCpu(T=T)
+    try:
+        oc.prefill_seconds()  # start the workers, import and attach the inputs (not timed)
+        oc.decode_seconds()
+        pre, dec = [], []
+        for i in range(args.warmup + args.steps):
+            tp = oc.prefill_seconds()
+            td = oc.decode_seconds()
+            if i >= args.warmup:
+                pre.append(tp)
+                dec.append(td)
+    finally:
+        oc.close()
+    t_pre = statistics.median(pre)
+    value = T / t_pre
+    step_ms = [1000.0 * (a + b) for a, b in zip(pre, dec)]
+    sample = (f"whole steps: the fp64 token-recurrence oracle over {T} of 8192 tokens x 32 heads of the prefill, "
+              f"then the fp64 decode oracle over all {oc.decode_rows} rows, split over {oc.cores} worker "
+              f"processes (one per host core, one thread each)")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * PREFILL_T / value,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": statistics.mean(step_ms),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "impl": "fp64 CPU oracle (token recurrence)"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "data": "synthetic", "config": bench_config(world),
+        "reference": {"what": "fp64 CPU oracle (oracle/kda_oracle.py) as it stands", "timed": "every step",
+                      "prefill_s_median": t_pre, "decode_us_per_step": 1e6 * statistics.median(dec)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oc.cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    if T != PREFILL_T:
+        line["config"]["partial"] = f"ref_seq_len={T}: a test run, not the benchmark line"
     print(json.dumps(line), flush=True)
     return 0
 
@@ -434,6 +612,35 @@ def run_gpu(args):
                "algorithmic_bytes": vbytes, "achieved_gbs": vbytes / v_avg / 1e9,
                "launches_per_call": 2, "note": "kda_plan_kernel + kda_chunk_fused_kernel"}
 
+    # --- the prefill with the log-decay g given (fp32 [1, T, 32, 128], KDA_GATE_G;
+    # drawn directly, same bytes as the gate inputs a): its own timed region ---
+    gate_g = None
+    if args.only == "all":
+        gw = W.prefill(seed=7 + 100 * rank, T=T, gate="g")
+        gd = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in gw.items()}
+        go = torch.empty_like(o)
+        ghT = torch.empty_like(hT)
+
+        def g_step():
+            kda.kda_chunk_fwd(gd["q"], gd["k"], gd["v"], scale=gd["scale"], g=gd["g"], b=gd["b"], h0=gd["h0"],
+                              l2norm_qk=True, o=go, hT=ghT, workspace=ws, stream=stream)
+        for _ in range(args.warmup):
+            g_step()
+        q0, q1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        q0.record(stream)
+        for _ in range(K):
+            g_step()
+        q1.record(stream)
+        torch.cuda.synchronize(dev)
+        g_avg = q0.elapsed_time(q1) / 1000.0 / K
+        gbytes = prefill_algorithmic_bytes(T) - PARAM_BYTES
+        gate_g = {"ms": 1000.0 * g_avg, "tokens_per_s": T / g_avg, "algorithmic_bytes": gbytes,
+                  "achieved_gbs": gbytes / g_avg / 1e9, "kernel": "kda_chunk_fused_kernel (KDA_GATE_G)",
+                  "inputs": "g = -U(0.01, 3) fp32 drawn directly (one exp per element in the kernel instead of "
+                            "the gate's exp, log and exp)"}
+        del gd, gw
+
     # --- decode with the causal conv1d + SiLU fused in front (its own timed region) ---
     dconv = None
     if args.only == "all":
@@ -582,13 +789,11 @@ def run_gpu(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
             "ms_per_step": 1000.0 * t_total / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": PREFILL_T,
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "inputs larger than L2 (prefill 403 MB, decode ~964 MB touched); no flush",
-                       "step": "one chunk forward (prefill) then one decode step (B=256)"},
+            "config": bench_config(world),
             "chunk_fwd": {"ms": 1000.0 * chunk_avg, "tokens_per_s": value,
                           "roofline_time_us": 1e6 * t_roof, "frac_of_roofline": t_roof / chunk_avg if chunk_avg > 0 else 0.0},
             "varlen": var,
+            "prefill_gate_g": gate_g,
             "head_rmsnorm": rms,
             "decode_conv": dconv,
             "recurrent": rec,
@@ -613,6 +818,8 @@ def run_gpu(args):
         }
         if var is not None:
             var["frac_of_roofline"] = var["achieved_gbs"] / hbm
+        if gate_g is not None:
+            gate_g["frac_of_roofline"] = gate_g["achieved_gbs"] / hbm
         if rms is not None:
             rms["frac_of_hbm"] = rms["achieved_gbs"] / hbm
         if dconv is not None:
@@ -628,11 +835,11 @@ def run_gpu(args):
         if args.only != "all" or T != PREFILL_T:
             line["config"]["partial"] = f"only={args.only}, seq_len={T}: a profiling run, not the benchmark line"
         if world == 1 and not args.no_cpu_baseline:
-            v, sample, cores = oracle_sample(budget_s=args.cpu_budget)
+            v, sample, cores = oracle_parallel_baseline(budget_s=args.cpu_budget)
             line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
-            v, sample, cores = oracle_sample(budget_s=args.cpu_budget / 3, chunk_size=16)
-            line["cpu_baseline_chunked"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                            "sample": sample}
+            v, sample, cores = oracle_sample(budget_s=args.cpu_budget / 3)
+            line["cpu_baseline_1core"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                          "sample": sample}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -647,8 +854,8 @@ def main():
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-budget", type=float, default=60.0,
-                    help="seconds of oracle work for the whole --impl reference run (spread over its steps)")
+    ap.add_argument("--ref-seq-len", type=int, default=PREFILL_T,
+                    help="prefill tokens of each --impl reference step (tests use fewer; the line is then partial)")
     ap.add_argument("--only", choices=["all", "chunk", "decode", "recurrent"], default="all",
                     help="time only one part (profiling runs; the benchmark line uses all)")
     ap.add_argument("--seq-len", type=int, default=PREFILL_T, help="prefill tokens (profiling runs use fewer)")

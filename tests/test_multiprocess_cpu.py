@@ -63,11 +63,12 @@ def test_max_over_ranks_single_process_is_identity():
 def test_reference_arm_under_torchrun_world_size_2():
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes", "1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), "bench.py", "--impl", "reference",
-           "--gpus", "2", "--steps", "1", "--warmup", "3", "--ref-budget", "2"]
+           "--gpus", "2", "--steps", "1", "--warmup", "3", "--ref-seq-len", "64"]
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1  # rank 0 alone prints
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
-    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["config"]["partial"].startswith("ref_seq_len=64")

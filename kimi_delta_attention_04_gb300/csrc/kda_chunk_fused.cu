@@ -103,6 +103,7 @@ struct __align__(16) PrepScratch {
   float red[4][48];
   float rnq[16], rnk[16], beta[16];
   float ghead[16];  // per-head log-decay of the chunk's tokens (KDA_GATE_HEAD_G)
+  uint4 inv[32][3];  // INV' = (I + L)^{-1} diag(beta) from warp 0: per lane its A fragments (operand type, bf16 hi, lo)
 };
 
 constexpr int kOPitch = kRows + 4;  // padded row of the staged output (conflict-free reads)
@@ -383,8 +384,9 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     const uint32_t bar_id = grp == 0 ? 1u : 4u;
     auto prep_bar = [bar_id] { named_bar_sync(bar_id, 128); };
     PrepScratch<Q>& ps = sm.ps[grp];
+    constexpr float kLog2e = 1.4426950408889634f;
     const float Aexp = (p.gate_mode == 2) ? expf(p.A_log[h]) : 0.f;
-    const float dtb = (p.gate_mode == 2) ? p.dt_bias[h * FD + pt] : 0.f;
+    const float dtb2 = (p.gate_mode == 2) ? p.dt_bias[h * FD + pt] * kLog2e : 0.f;  // dt_bias in log2 units
     bool failed = false;
     int c = static_cast<int>(rank) + kCtas * grp;
     // beta is loaded one step of this group ahead and kept as raw bits until
@@ -461,40 +463,45 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       const PrepIn& in = sm.pin[buf];
       float qv[16], kv[16], al[16], vv[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {  // rows past the sequence end belong to another sequence: zero them
-        qv[i] = i < ntok ? __bfloat162float(in.q[i][pt]) : 0.f;
-        kv[i] = i < ntok ? __bfloat162float(in.k[i][pt]) : 0.f;
-        vv[i] = i < ntok ? __bfloat162float(in.v[i][pt]) : 0.f;
+      for (int i = 0; i < 16; ++i) {
+        qv[i] = __bfloat162float(in.q[i][pt]);
+        kv[i] = __bfloat162float(in.k[i][pt]);
+        vv[i] = __bfloat162float(in.v[i][pt]);
       }
       // One branch for the gate mode around the whole token loop, so the 16
-      // independent exp/log chains interleave; padded tokens select alpha = 1.
+      // independent exp/log chains interleave.
       if (p.gate_mode == 2) {
-        // alpha = e^{-A softplus(x)} = 2^{-A log2(1 + 2^{x log2 e})}, branch free:
-        // the exponent is clamped and x itself selected above the threshold 20.
-        constexpr float kLog2e = 1.4426950408889634f;
+        // alpha = e^{-A softplus(x)} = 2^{-A log2(1 + 2^y)}, y = x log2 e. Above the
+        // threshold x > 20 softplus(x) is x itself: log2(1 + 2^y) >= y always, and
+        // with the exponent clamped at 20 log2 e the log stays below y there, so
+        // max(log2(1 + 2^min(y, 20 log2 e)), y) is the thresholded softplus.
+        constexpr float kClamp = 20.f * kLog2e;
         const float nA = -Aexp;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float x = in.a[i][pt] + dtb;
-          const float l2 = lg2_approx(1.f + ex2_approx(fminf(x, 20.f) * kLog2e));
-          const float sp2 = x > 20.f ? x * kLog2e : l2;  // softplus(x) in log2 units
-          const float a = ex2_approx(nA * sp2);
-          al[i] = i < ntok ? a : 1.f;
+          const float y = fmaf(in.a[i][pt], kLog2e, dtb2);
+          const float sp2 = fmaxf(lg2_approx(1.f + ex2_approx(fminf(y, kClamp))), y);
+          al[i] = ex2_approx(nA * sp2);
         }
       } else if (p.gate_mode == 3) {
-        constexpr float kLog2e = 1.4426950408889634f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) al[i] = i < ntok ? ex2_approx(ps.ghead[i] * kLog2e) : 1.f;
+        for (int i = 0; i < 16; ++i) al[i] = ex2_approx(ps.ghead[i] * kLog2e);
       } else if (p.gate_mode == 1) {
-        constexpr float kLog2e = 1.4426950408889634f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a = ex2_approx(in.a[i][pt] * kLog2e);
-          al[i] = i < ntok ? a : 1.f;
-        }
+        for (int i = 0; i < 16; ++i) al[i] = ex2_approx(in.a[i][pt] * kLog2e);
       } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i) al[i] = 1.f;
+      }
+      if (ntok < 16) {  // the last chunk of a sequence (uniform across the CTA): rows past
+                        // its end belong to another sequence or lie past the tensor
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (i >= ntok) {
+            qv[i] = kv[i] = vv[i] = 0.f;
+            al[i] = 1.f;
+          }
+        }
       }
       {
         float red[16];
@@ -637,23 +644,37 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         po.mqk[e >> 4][e & 15] = *reinterpret_cast<const uint16_t*>(&v);
       }
       if (DELTA) {
-        // every prep warp forms INV' = (I + L)^{-1} diag(beta) in registers
+        // warp 0 forms INV' = (I + L)^{-1} diag(beta) in registers and hands its
+        // three A-fragment forms (in the operand type, and bf16 hi + lo) to the
+        // other warps through shared memory
         const int g = lane >> 2, t = lane & 3;
-        Frag16 inv = neumann_inverse16<QK>(&ps.Lm[0][0], 17, lane);
-        Frag16 ihi, ilo;
+        if (pw == 0) {
+          Frag16 inv = neumann_inverse16<QK>(&ps.Lm[0][0], 17, lane);
+          Frag16 ihi, ilo;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+          for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float v = inv.c[nt][e] * ps.beta[8 * nt + 2 * t + (e & 1)];
-            inv.c[nt][e] = v;
-            ihi.c[nt][e] = __bfloat162float(__float2bfloat16_rn(v));
-            ilo.c[nt][e] = v - ihi.c[nt][e];
-          }
+            for (int e = 0; e < 4; ++e) {
+              const float v = inv.c[nt][e] * ps.beta[8 * nt + 2 * t + (e & 1)];
+              inv.c[nt][e] = v;
+              ihi.c[nt][e] = __bfloat162float(__float2bfloat16_rn(v));
+              ilo.c[nt][e] = v - ihi.c[nt][e];
+            }
+          uint32_t f[3][4];
+          frag_as_a<QK>(inv, f[0]);
+          frag_as_a<Bf16>(ihi, f[1]);
+          frag_as_a<Bf16>(ilo, f[2]);
+#pragma unroll
+          for (int j = 0; j < 3; ++j) ps.inv[lane][j] = make_uint4(f[j][0], f[j][1], f[j][2], f[j][3]);
+        }
+        prep_bar();
         uint32_t a[4], ahi[4], alo[4];
-        frag_as_a<QK>(inv, a);
-        frag_as_a<Bf16>(ihi, ahi);
-        frag_as_a<Bf16>(ilo, alo);
+        {
+          const uint4 x0 = ps.inv[lane][0], x1 = ps.inv[lane][1], x2 = ps.inv[lane][2];
+          a[0] = x0.x; a[1] = x0.y; a[2] = x0.z; a[3] = x0.w;
+          ahi[0] = x1.x; ahi[1] = x1.y; ahi[2] = x1.z; ahi[3] = x1.w;
+          alo[0] = x2.x; alo[1] = x2.y; alo[2] = x2.z; alo[3] = x2.w;
+        }
 #pragma unroll
         for (int pp = 0; pp < 2; ++pp) {
           const int n0 = pw * 32 + 16 * pp;

@@ -56,13 +56,17 @@ constexpr int kFusedThreads = 480;   // 4 recurrence warps, 2 x 4 prep warps, mo
 __device__ __forceinline__ int cm_off(int row, int half) { return row * 16 + ((half ^ (row >> 2)) & 1) * 8; }
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+// The chunk operands are those of the unnormalised q, k (the L2 norm is folded
+// in, see the prep): U' = diag(rk) U is the U operand, o_i = sr_i O'_i with
+// O' = qd S + mqk U' and sr_i = scale rq_i.
 struct __align__(16) Stage {
-  uint16_t W[FD][16];      // bf16, -W^T = -(INV diag(beta) k_dec)^T, channel-major
-  uint16_t qd[FD][16];     // bf16, (scale q e^{G})^T, channel-major
+  uint16_t W[FD][16];      // bf16, -W'^T = -(diag(rk) INV diag(beta rk) k_dec)^T, channel-major
+  uint16_t qd[FD][16];     // bf16, (q e^{G})^T, channel-major
   uint16_t kr[FD][16];     // st2, (k e^{G_last - G})^T, channel-major
-  uint16_t mqk[16][24];    // st2
+  uint16_t mqk[16][24];    // st2, raw q_i . k_j e^{G_i - G_j} (j <= i)
   float gamma[FD];         // e^{G_last}
-  float ut[kRows][16];     // U~ rows of this CTA (transposed)
+  float sr[16];            // output factor of each token: scale rq_i
+  float ut[kRows][16];     // U~' rows of this CTA (transposed)
 };
 constexpr uint32_t kSharedBytes = offsetof(Stage, ut);
 constexpr uint32_t kUtSliceBytes = sizeof(float) * kRows * 16;
@@ -75,6 +79,7 @@ struct __align__(16) PrepOut {
   uint16_t kr[FD][16];
   uint16_t mqk[16][24];
   float gamma[FD];
+  float sr[16];
   float ut[FD][16];  // all value rows
 };
 static_assert(offsetof(PrepOut, ut) == kSharedBytes, "prep-out and stage share the layout");
@@ -100,9 +105,9 @@ struct __align__(16) PrepScratch {
   __nv_bfloat16 vs[FD][16];   // channel-major
   float Lm[16][17];
   float Mq[16][17];
-  float red[4][48];
-  float rnq[16], rnk[16], beta[16];
-  float ghead[16];  // per-head log-decay of the chunk's tokens (KDA_GATE_HEAD_G)
+  float red[4][48];     // per warp: partial sums of q.q, k.k and q.k of the 16 tokens
+  float beta[2][16];    // beta of the group's current / next chunk
+  float ghead[2][16];   // per-head log-decay (KDA_GATE_HEAD_G) of the current / next chunk
   uint4 inv[32][3];  // INV' = (I + L)^{-1} diag(beta) from warp 0: per lane its A fragments (operand type, bf16 hi, lo)
 };
 
@@ -389,27 +394,31 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     const float dtb2 = (p.gate_mode == 2) ? p.dt_bias[h * FD + pt] * kLog2e : 0.f;  // dt_bias in log2 units
     bool failed = false;
     int c = static_cast<int>(rank) + kCtas * grp;
-    // beta is loaded one step of this group ahead and kept as raw bits until
-    // it is used (converting right after the load would wait for it there);
-    // its sigmoid is taken when it is stored, off the load's latency.
+    // beta and the per-head gate of the group's chunks: lanes 0-15 of the
+    // group's warp 1 load the raw values one chunk of the group ahead and, while
+    // warp 0 forms the current chunk's inverse, turn them into
+    // ps.beta / ps.ghead [buffer of that chunk].
+    const int bl = pt - 32;  // token handled by warp 1's lanes 0-15
+    const bool bown = bl >= 0 && bl < 16;
     unsigned short beta_next = 0;
-    auto load_beta = [&](int cc) {
-      unsigned short raw = 0;
-      const int tk0 = ts + cc * kChunk;
-      if (DELTA && pt < 16 && tk0 + pt < te)
-        raw = reinterpret_cast<const unsigned short*>(p.beta)[static_cast<size_t>(tk0 + pt) * H + h];
-      return raw;
-    };
-    if (c < nch) beta_next = load_beta(c);
-    // Per-head gate (Gated DeltaNet): one log-decay per token, prefetched like beta.
     float gh_next = 0.f;
-    auto load_gh = [&](int cc) {
-      float x = 0.f;
+    auto load_next = [&](int cc) {
       const int tk0 = ts + cc * kChunk;
-      if (p.gate_mode == 3 && pt < 16 && tk0 + pt < te) x = p.g[static_cast<size_t>(tk0 + pt) * H + h];
-      return x;
+      beta_next = 0;
+      gh_next = 0.f;
+      if (bown && tk0 + bl < te) {
+        if (DELTA) beta_next = reinterpret_cast<const unsigned short*>(p.beta)[static_cast<size_t>(tk0 + bl) * H + h];
+        if (p.gate_mode == 3) gh_next = p.g[static_cast<size_t>(tk0 + bl) * H + h];
+      }
     };
-    if (c < nch) gh_next = load_gh(c);
+    auto stage_next = [&](int bufi, int cc) {
+      if (bown) {
+        const float raw = __bfloat162float(__ushort_as_bfloat16(beta_next));
+        const float bt = (p.beta_mode == 1) ? sigmoid_f(raw) : raw;
+        ps.beta[bufi][bl] = (DELTA && ts + cc * kChunk + bl < te) ? bt : 0.f;
+        ps.ghead[bufi][bl] = gh_next;
+      }
+    };
     // Each group loads its own input tiles with TMA: the first chunk's now,
     // chunk c + 8's as soon as chunk c's are in registers.
     if (pt == 0) {
@@ -419,6 +428,17 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       if (p.gate_mode == 1 || p.gate_mode == 2) asm volatile("prefetch.tensormap [%0];" ::"l"(&maps.a) : "memory");
       if (c < nch) issue_inputs(maps, sm.pin[grp], &sm.pinbar[grp], h, ts + c * kChunk, p.gate_mode);
     }
+    // the first chunk's beta and gate, and clear L / Mqk scratch (ordered by the
+    // loop's first barrier)
+    if (c < nch) {
+      load_next(c);
+      stage_next(0, c);
+    }
+    if (c + 2 * kCtas < nch) load_next(c + 2 * kCtas);
+    for (int i = pt; i < 16 * 17; i += 128) {
+      (&ps.Lm[0][0])[i] = 0.f;
+      (&ps.Mq[0][0])[i] = 0.f;
+    }
     // The hand-off of a written chunk to the publisher (a release at CTA scope)
     // is made after the next chunk's first barrier: right after the slot
     // stores it would wait for their L2 acknowledgements.
@@ -427,14 +447,21 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       if (pt == 0 && sig_pending >= 0) mbar_arrive_local(&sm.sig[sig_pending % (kGRing / kCtas)]);
       sig_pending = -1;
     };
+    // The L2 norm is folded into the chunk's small matrices instead of scaling
+    // q and k: everything below uses the raw q~, k~ of the tokens, with
+    // rq_i = 1 / |q~_i|, rk_i = 1 / |k~_i| (1 without the norm). Then
+    //   L = diag(beta rk) (k~ k~^T . decay) diag(rk)       (the L of unit q, k)
+    //   U' = diag(rk) U = INV_U v - INV_W k~_dec S,  INV_U = diag(rk) INV diag(beta),
+    //                                                INV_W = INV_U diag(rk)
+    //   S <- gamma S + k~_res^T U',   o_i = scale rq_i (q~_dec S + Mqk~ U')_i,
+    // where Mqk~ holds the raw q~_i . k~_j decay products: exactly the
+    // recurrence of unit q, k, with no pass over the 16 x 128 tiles for the norm
+    // and no barrier waiting for it.
     for (int j = grp; c < nch; j += 2, c += 2 * kCtas) {
       const int buf = grp;
+      const int jb = (j >> 1) & 1;  // beta / gate buffer of this chunk
       const int tok0 = ts + c * kChunk;
       const int ntok = min(kChunk, te - tok0);
-      const float beta_cur = __bfloat162float(__ushort_as_bfloat16(beta_next));
-      if (c + 2 * kCtas < nch) beta_next = load_beta(c + 2 * kCtas);
-      const float gh_cur = gh_next;
-      if (c + 2 * kCtas < nch) gh_next = load_gh(c + 2 * kCtas);
       if (!failed && !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pinbar[buf])),
                                         static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs)) {
         failed = true;
@@ -449,16 +476,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
       }
       PrepOut& po = *reinterpret_cast<PrepOut*>(gring + static_cast<size_t>(gs) * kSlotBytes);
-      for (int i = pt; i < 16 * 17; i += 128) {
-        (&ps.Lm[0][0])[i] = 0.f;
-        (&ps.Mq[0][0])[i] = 0.f;
-      }
-      if (pt < 16) {
-        const float bt = (p.beta_mode == 1) ? sigmoid_f(beta_cur) : beta_cur;
-        ps.beta[pt] = (DELTA && pt < ntok) ? bt : 0.f;
-        ps.ghead[pt] = gh_cur;
-      }
-      prep_bar();
+      prep_bar();  // (A) this chunk's beta and gate staged, L / Mqk scratch clear
       signal_written();
       const PrepIn& in = sm.pin[buf];
       float qv[16], kv[16], al[16], vv[16];
@@ -485,7 +503,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         }
       } else if (p.gate_mode == 3) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) al[i] = ex2_approx(ps.ghead[i] * kLog2e);
+        for (int i = 0; i < 16; ++i) al[i] = ex2_approx(ps.ghead[jb][i] * kLog2e);
       } else if (p.gate_mode == 1) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) al[i] = ex2_approx(in.a[i][pt] * kLog2e);
@@ -503,7 +521,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           }
         }
       }
-      {
+      {  // this warp's partial sums of q~.q~, k~.k~, q~.k~ over its 32 channels
         float red[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) red[i] = qv[i] * qv[i];
@@ -521,30 +539,6 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           ps.red[pw][32 + jj] = t3;
         }
       }
-      fence_proxy_async_smem();  // the reads of pin[buf] precede the next TMA write into it
-      prep_bar();
-      if (pt == 0 && c + 2 * kCtas < nch)
-        issue_inputs(maps, sm.pin[buf], &sm.pinbar[buf], h, ts + (c + 2 * kCtas) * kChunk, p.gate_mode);
-      if (pt < 16) {
-        float sq = 0.f, sk = 0.f, sqk = 0.f;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          sq += ps.red[w][pt];
-          sk += ps.red[w][16 + pt];
-          sqk += ps.red[w][32 + pt];
-        }
-        const float rq = L2N ? rsqrtf(sq + 1e-6f) : 1.f;
-        const float rk = L2N ? rsqrtf(sk + 1e-6f) : 1.f;
-        ps.rnq[pt] = rq;
-        ps.rnk[pt] = rk;
-        ps.Mq[pt][pt] = p.scale * sqk * rq * rk;
-      }
-      prep_bar();
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        qv[i] *= ps.rnq[i];
-        kv[i] *= ps.rnk[i];
-      }
       float P[16], Rs[16];
       P[0] = al[0];
 #pragma unroll
@@ -560,8 +554,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         };
         uint32_t w[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-          w[i] = Bf16::pack(p.scale * qv[2 * i] * P[2 * i], p.scale * qv[2 * i + 1] * P[2 * i + 1]);
+        for (int i = 0; i < 8; ++i) w[i] = Bf16::pack(qv[2 * i] * P[2 * i], qv[2 * i + 1] * P[2 * i + 1]);
         put16(&po.qd[0][0], w);
 #pragma unroll
         for (int i = 0; i < 8; ++i) w[i] = ST2::pack(kv[2 * i] * Rs[2 * i], kv[2 * i + 1] * Rs[2 * i + 1]);
@@ -575,11 +568,6 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           put16(reinterpret_cast<uint16_t*>(&ps.vs[0][0]), w);
         }
         po.gamma[pt] = P[15];
-        if (!DELTA) {
-          float4* ut = reinterpret_cast<float4*>(&po.ut[pt][0]);
-#pragma unroll
-          for (int i = 0; i < 16; i += 4) ut[i / 4] = make_float4(vv[i], vv[i + 1], vv[i + 2], vv[i + 3]);
-        }
 #pragma unroll
         for (int lv = 0; lv < 4; ++lv) {
           const int s = 8 >> lv;
@@ -609,8 +597,11 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
               make_uint4(QK::pack(bc[0], bc[1]), QK::pack(bc[2], bc[3]), QK::pack(bc[4], bc[5]), QK::pack(bc[6], bc[7]));
         }
       }
-      prep_bar();
-      {  // level pw of the anchored split: L (rows 0-7) and Mqk (rows 8-15)
+      fence_proxy_async_smem();  // the reads of pin[buf] precede the next TMA write into it
+      prep_bar();  // (D) tiles, level operands and norm partial sums written
+      if (pt == 0 && c + 2 * kCtas < nch)
+        issue_inputs(maps, sm.pin[buf], &sm.pinbar[buf], h, ts + (c + 2 * kCtas) * kChunk, p.gate_mode);
+      {  // level pw of the anchored split: raw L (rows 0-7, times beta) and Mqk (rows 8-15)
         const int lv = pw;
         const int s = 8 >> lv;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -632,42 +623,84 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           if (rr / s != cidx / s) continue;
           const int i = row_tok_f(s, rr), jx = col_tok_f(s, cidx);
           if (r < 8) {
-            if (DELTA) ps.Lm[i][jx] = ps.beta[i] * acc[e];
+            if (DELTA) ps.Lm[i][jx] = ps.beta[jb][i] * acc[e];
           } else {
-            ps.Mq[i][jx] = p.scale * acc[e];
+            ps.Mq[i][jx] = acc[e];
           }
         }
+        if (pw == 0 && lane < 16)  // the diagonal of Mqk: q~_i . k~_i
+          ps.Mq[lane][lane] = ps.red[0][32 + lane] + ps.red[1][32 + lane] + ps.red[2][32 + lane] + ps.red[3][32 + lane];
       }
-      prep_bar();
-      for (int e = pt; e < 256; e += 128) {
-        const typename ST2::T v = ST2::cvt(ps.Mq[e >> 4][e & 15]);
-        po.mqk[e >> 4][e & 15] = *reinterpret_cast<const uint16_t*>(&v);
+      prep_bar();  // (E) raw L and Mqk complete
+      // the norm factors of the 16 tokens: lane i < 16 of every warp holds token i's
+      float rq_l = 1.f, rk_l = 1.f;
+      if (L2N && lane < 16) {
+        float sq = 0.f, sk = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          sq += ps.red[w][lane];
+          sk += ps.red[w][16 + lane];
+        }
+        rq_l = rsqrtf(sq + 1e-6f);
+        rk_l = rsqrtf(sk + 1e-6f);
       }
-      if (DELTA) {
-        // warp 0 forms INV' = (I + L)^{-1} diag(beta) in registers and hands its
-        // three A-fragment forms (in the operand type, and bf16 hi + lo) to the
-        // other warps through shared memory
-        const int g = lane >> 2, t = lane & 3;
-        if (pw == 0) {
-          Frag16 inv = neumann_inverse16<QK>(&ps.Lm[0][0], 17, lane);
-          Frag16 ihi, ilo;
+      if (pw == 0) {
+        if (lane < 16) po.sr[lane] = p.scale * rq_l;
+        if (DELTA) {
+          // X = -L = -diag(beta rk) raw diag(rk) in registers, then INV' forms
+          const int g = lane >> 2, t = lane & 3;
+          const float rkr[2] = {__shfl_sync(0xffffffffu, rk_l, g), __shfl_sync(0xffffffffu, rk_l, g + 8)};
+          float rkc[2][2], bcol[2][2];
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              rkc[nt][e] = __shfl_sync(0xffffffffu, rk_l, 8 * nt + 2 * t + e);
+              bcol[nt][e] = ps.beta[jb][8 * nt + 2 * t + e];
+            }
+          Frag16 X;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              X.c[nt][e] = -ps.Lm[g + 8 * (e >> 1)][8 * nt + 2 * t + (e & 1)] * rkr[e >> 1] * rkc[nt][e & 1];
+          __syncwarp();
+          for (int i = lane; i < 16 * 17; i += 32) (&ps.Lm[0][0])[i] = 0.f;  // clear for the next chunk
+          const Frag16 inv = neumann_inverse16_frag<QK>(X, lane);
+          Frag16 iw, ihi, ilo;
 #pragma unroll
           for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float v = inv.c[nt][e] * ps.beta[8 * nt + 2 * t + (e & 1)];
-              inv.c[nt][e] = v;
-              ihi.c[nt][e] = __bfloat162float(__float2bfloat16_rn(v));
-              ilo.c[nt][e] = v - ihi.c[nt][e];
+              const float u = inv.c[nt][e] * bcol[nt][e & 1] * rkr[e >> 1];  // INV_U
+              iw.c[nt][e] = u * rkc[nt][e & 1];                                // INV_W
+              ihi.c[nt][e] = __bfloat162float(__float2bfloat16_rn(u));
+              ilo.c[nt][e] = u - ihi.c[nt][e];
             }
           uint32_t f[3][4];
-          frag_as_a<QK>(inv, f[0]);
+          frag_as_a<QK>(iw, f[0]);
           frag_as_a<Bf16>(ihi, f[1]);
           frag_as_a<Bf16>(ilo, f[2]);
 #pragma unroll
-          for (int j = 0; j < 3; ++j) ps.inv[lane][j] = make_uint4(f[j][0], f[j][1], f[j][2], f[j][3]);
+          for (int jj = 0; jj < 3; ++jj) ps.inv[lane][jj] = make_uint4(f[jj][0], f[jj][1], f[jj][2], f[jj][3]);
         }
-        prep_bar();
+      } else {
+        // warps 1-3: Mqk~ into the slot, clearing its scratch for the next chunk
+        for (int e = pt - 32; e < 256; e += 96) {
+          const float x = ps.Mq[e >> 4][e & 15];
+          ps.Mq[e >> 4][e & 15] = 0.f;
+          const typename ST2::T v = ST2::cvt(x);
+          po.mqk[e >> 4][e & 15] = *reinterpret_cast<const uint16_t*>(&v);
+        }
+        // and the group's next chunk's beta and gate into the other buffer
+        if (c + 2 * kCtas < nch) {
+          stage_next(jb ^ 1, c + 2 * kCtas);
+          if (c + 4 * kCtas < nch) load_next(c + 4 * kCtas);
+        }
+      }
+      prep_bar();  // (F) INV' fragments, Mqk~, the next chunk's beta, clear scratch
+      if (DELTA) {
+        const int g = lane >> 2, t = lane & 3;
         uint32_t a[4], ahi[4], alo[4];
         {
           const uint4 x0 = ps.inv[lane][0], x1 = ps.inv[lane][1], x2 = ps.inv[lane][2];
@@ -683,7 +716,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
           mma16816<QK>(c0, a, b[0], b[1]);
           mma16816<QK>(c1, a, b[2], b[3]);
-          // -W blocks (tokens x 8 channels) transposed in registers into -W^T rows
+          // -W' blocks (tokens x 8 channels) transposed in registers into -W'^T rows
           uint16_t* wt = &po.W[0][0];
           *reinterpret_cast<uint32_t*>(wt + cm_off(n0 + g, 0) + 2 * t) = movmatrix_trans(Bf16::pack(-c0[0], -c0[1]));
           *reinterpret_cast<uint32_t*>(wt + cm_off(n0 + g, 1) + 2 * t) = movmatrix_trans(Bf16::pack(-c0[2], -c0[3]));
@@ -704,8 +737,16 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           po.ut[n0 + 8 + 2 * t][g + 8] = u1[2];
           po.ut[n0 + 8 + 2 * t + 1][g + 8] = u1[3];
         }
+      } else {
+        // delta rule off: U' = diag(rk) v, value channel pt of the 16 tokens
+        float uv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) uv[i] = vv[i] * __shfl_sync(0xffffffffu, rk_l, i);
+        float4* ut = reinterpret_cast<float4*>(&po.ut[pt][0]);
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) ut[i / 4] = make_float4(uv[i], uv[i + 1], uv[i + 2], uv[i + 3]);
       }
-      prep_bar();  // every store into the slot precedes the hand-off
+      prep_bar();  // (G) every store into the slot precedes the hand-off
       sig_pending = j;
     }
     signal_written();
@@ -781,12 +822,13 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         if (lane == 0) set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
       }
       const float* p0 = &sm.rs.opart[s][tok][hv * 16];
+      const float sr = sm.ring[s].sr[tok];  // scale rq of the token (the stage is held until the release below)
       uint32_t pk[8];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float4 x = *reinterpret_cast<const float4*>(p0 + 4 * i);
-        pk[2 * i] = Bf16::pack(x.x, x.y);
-        pk[2 * i + 1] = Bf16::pack(x.z, x.w);
+        pk[2 * i] = Bf16::pack(sr * x.x, sr * x.y);
+        pk[2 * i + 1] = Bf16::pack(sr * x.z, sr * x.w);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive_local(&sm.empty[s]);

@@ -223,10 +223,22 @@ __device__ __forceinline__ Frag16 frag_plus_identity(Frag16 m, int lane) {
   return m;
 }
 
-// (I + L)^{-1} for a strictly lower-triangular 16x16 L (row stride `ld` floats in
-// shared memory): the Neumann series of X = -L, which is exact because L^16 = 0,
-// summed as (I + X)(I + X^2)(I + X^4)(I + X^8). Independent products are paired
-// so the dependent chain is four products deep. One warp; operands rounded to Op.
+// (I + L)^{-1} for a strictly lower-triangular 16x16 L, from X = -L in
+// registers (accumulator layout): the Neumann series of X, which is exact
+// because L^16 = 0, summed as (I + X)(I + X^2)(I + X^4)(I + X^8). Independent
+// products are paired so the dependent chain is four products deep. One warp;
+// operands rounded to Op.
+template <typename Op>
+__device__ __forceinline__ Frag16 neumann_inverse16_frag(const Frag16& X, int lane) {
+  const Frag16 X2 = frag_mm<Op>(X, X);
+  const Frag16 X4 = frag_mm<Op>(X2, X2);
+  const Frag16 P1 = frag_mm<Op>(frag_plus_identity(X, lane), frag_plus_identity(X2, lane));
+  const Frag16 X8 = frag_mm<Op>(X4, X4);
+  const Frag16 P2 = frag_mm<Op>(P1, frag_plus_identity(X4, lane));
+  return frag_mm<Op>(P2, frag_plus_identity(X8, lane));
+}
+
+// The same with L read from shared memory (row stride `ld` floats).
 template <typename Op>
 __device__ __forceinline__ Frag16 neumann_inverse16(const float* L, int ld, int lane) {
   const int g = lane >> 2, t = lane & 3;
@@ -235,12 +247,7 @@ __device__ __forceinline__ Frag16 neumann_inverse16(const float* L, int ld, int 
   for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) X.c[nt][e] = -L[(g + 8 * (e >> 1)) * ld + 8 * nt + 2 * t + (e & 1)];
-  const Frag16 X2 = frag_mm<Op>(X, X);
-  const Frag16 X4 = frag_mm<Op>(X2, X2);
-  const Frag16 P1 = frag_mm<Op>(frag_plus_identity(X, lane), frag_plus_identity(X2, lane));
-  const Frag16 X8 = frag_mm<Op>(X4, X4);
-  const Frag16 P2 = frag_mm<Op>(P1, frag_plus_identity(X4, lane));
-  return frag_mm<Op>(P2, frag_plus_identity(X8, lane));
+  return neumann_inverse16_frag<Op>(X, lane);
 }
 
 // 2^x and log2(x) straight from the special-function unit (PTX ex2.approx /

@@ -83,6 +83,7 @@ def decode_algorithmic_bytes(n_valid, H=32, HV=32, K=128, V=128, B=256):
 # figure is only reported while these files are unchanged).
 CHUNK_KERNEL_SOURCES = ["kda_chunk_fused.cu", "kda_common.cuh", "kda_cluster.cuh", "kda_tma.h", "kda_tma.cpp"]
 DECODE_KERNEL_SOURCES = ["kda_decode.cu", "kda_common.cuh"]
+RECURRENT_KERNEL_SOURCES = ["kda_recurrent_tc.cu", "kda_common.cuh", "kda_cluster.cuh"]
 RECURRENT_B, RECURRENT_T, RECURRENT_SLOTS = 128, 8, 256  # speculative-style step: 128 rows x 8 tokens
 RECURRENT_LONG_B, RECURRENT_LONG_T = 64, 64              # the longest T the entry point takes
 CHUNK_LAUNCHES_PER_STEP = 1   # kda_chunk_fused_kernel (bf16, d = 128, no cu_seqlens)
@@ -710,10 +711,14 @@ def run_gpu(args):
         r_valid = int((rw["indices"] >= 0).sum())
         rbytes = recurrent_algorithmic_bytes(r_valid, rw["B"], rw["T"])
         kernel = "kda_recurrent_tc_kernel (chunk form, tensor cores)" if T_r >= 8 else "kda_recurrent_kernel (per token)"
+        # the stored DRAM traffic was captured at 128 rows x 8 tokens: it scales by the
+        # valid rows (the slots dominate), so it is quoted for that shape only
+        traffic = (stored_traffic("kda_recurrent_tc_kernel", kernel_sources_sha(RECURRENT_KERNEL_SOURCES), r_valid)
+                   if T_r == RECURRENT_T else None)
         return {"us_per_step": 1e6 * r_avg, "rows": rw["B"], "tokens_per_row": rw["T"], "n_valid_rows": r_valid,
                 "tokens_per_s": rw["B"] * rw["T"] / r_avg,
                 "roofline": {"bound": "hbm", "achieved": rbytes / r_avg / 1e9, "unit": "GB/s",
-                             "algorithmic_bytes": rbytes, "kernel": kernel}}
+                             "algorithmic_bytes": rbytes, "kernel": kernel, "traffic": traffic}}
 
     rec = rec_long = None
     if args.only in ("all", "recurrent"):

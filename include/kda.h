@@ -114,7 +114,10 @@ typedef enum {
  * Numerics of the BF16 path: S stays fp32 on chip; the contractions run on
  * tensor cores with fp32 accumulation, S rounded to bf16 as an operand, and
  * (with the delta rule on) the corrected values U in fp16, which assumes
- * |U| < 65504 (values are saturated, never turned into inf).
+ * |U| < 65504 (values are saturated, never turned into inf, and no status is
+ * reported). With KDA_FLAG_L2NORM_QK and dk = dv = 128 the operand held in fp16
+ * is U / |k~| (k~ the token's key before the norm), so the bound applies to
+ * that scaled value there.
  */
 typedef struct kda_chunk_args {
   int32_t dtype;       /* kda_dtype */

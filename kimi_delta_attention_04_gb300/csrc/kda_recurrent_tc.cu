@@ -84,6 +84,18 @@ struct RtcSmem {
 // set, so the eight rows of one ldmatrix 8x8 load fall on distinct banks.
 __device__ __forceinline__ int rt_cm_off(int row, int half) { return row * 16 + ((half ^ (row >> 2)) & 1) * 8; }
 
+// Key order inside the state step. Within each block of 16 keys, the key the
+// MMAs call 8 j + 2 t + e (n-tile j of the pair, accumulator column pair of lane
+// t) is stored key 4 t + 2 j + e, so the four keys a lane holds across the pair
+// are consecutive in memory and the state moves between L2 and registers as one
+// 16-byte access per row and pair of n-tiles. The operands indexed by key
+// (q_dec, k_res, k_dec, gamma) are laid out in the MMAs' order; L and Mqk sum
+// over every key and do not care.
+__device__ __forceinline__ int rt_mma_key(int key) {
+  const int r = key & 15;
+  return (key & ~15) + ((r >> 1) & 1) * 8 + (r >> 2) * 2 + (r & 1);
+}
+
 __device__ __forceinline__ int rt_row_tok(int s, int r) { return (r / s) * 2 * s + s + (r % s); }
 __device__ __forceinline__ int rt_col_tok(int s, int r) { return (r / s) * 2 * s + (r % s); }
 
@@ -250,10 +262,11 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
 #pragma unroll
       for (int i = 14; i >= 0; --i) Rs[i] = Rs[i + 1] * al[i + 1];
       // channel ch's 16 tokens of each channel-major tile, two 16-byte stores each
+      const int mk = rt_mma_key(ch);  // this channel's row in the key-indexed operand tiles
       auto put16 = [&](void* tile, const uint32_t (&w)[8]) {
         uint16_t* base = reinterpret_cast<uint16_t*>(tile);
-        *reinterpret_cast<uint4*>(base + rt_cm_off(ch, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(base + rt_cm_off(ch, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+        *reinterpret_cast<uint4*>(base + rt_cm_off(mk, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(base + rt_cm_off(mk, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
       };
       uint32_t w[8];
 #pragma unroll
@@ -266,7 +279,7 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
 #pragma unroll
       for (int i = 0; i < 8; ++i) w[i] = QK::pack(kv[2 * i] * P[2 * i], kv[2 * i + 1] * P[2 * i + 1]);
       put16(&sm.kdec[0][0], w);
-      sm.gamma[ch] = P[15];
+      sm.gamma[mk] = P[15];
 #pragma unroll
       for (int lv = 0; lv < 4; ++lv) {
         const int s = 8 >> lv;
@@ -291,7 +304,11 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) w[i] = QK::pack(ar[2 * i], ar[2 * i + 1]);
-        put16(&lvo.A[lv][0][0], w);
+        {  // the level tiles are summed over every channel: physical order
+          uint16_t* base = reinterpret_cast<uint16_t*>(&lvo.A[lv][0][0]);
+          *reinterpret_cast<uint4*>(base + rt_cm_off(ch, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(base + rt_cm_off(ch, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+        }
         *reinterpret_cast<uint4*>(&lvo.B[lv][ch][0]) =
             make_uint4(QK::pack(bc[0], bc[1]), QK::pack(bc[2], bc[3]), QK::pack(bc[4], bc[5]), QK::pack(bc[6], bc[7]));
       }
@@ -378,12 +395,14 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
     for (int mt = 0; mt < MT; ++mt) {
       const int r0 = (warp + WARPS * mt) * 16;  // first value row of the tile
       float S[NT][4];
-      {  // the state, in the accumulator layout (its lines are in L2 by now)
+      {  // the state, in the accumulator layout (its lines are in L2 by now): stored keys
+         // 16 pp + 4 t .. + 3 are MMA keys 16 pp + 2 t (+1) and 16 pp + 8 + 2 t (+1)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          const float2 x = __ldcs(reinterpret_cast<const float2*>(S_slot + (r0 + g) * K + 8 * nt + 2 * t));
-          const float2 y = __ldcs(reinterpret_cast<const float2*>(S_slot + (r0 + g + 8) * K + 8 * nt + 2 * t));
-          S[nt][0] = x.x; S[nt][1] = x.y; S[nt][2] = y.x; S[nt][3] = y.y;
+        for (int pp = 0; pp < NT / 2; ++pp) {
+          const float4 x = __ldcs(reinterpret_cast<const float4*>(S_slot + (r0 + g) * K + 16 * pp + 4 * t));
+          const float4 y = __ldcs(reinterpret_cast<const float4*>(S_slot + (r0 + g + 8) * K + 16 * pp + 4 * t));
+          S[2 * pp][0] = x.x; S[2 * pp][1] = x.y; S[2 * pp + 1][0] = x.z; S[2 * pp + 1][1] = x.w;
+          S[2 * pp][2] = y.x; S[2 * pp][3] = y.y; S[2 * pp + 1][2] = y.z; S[2 * pp + 1][3] = y.w;
         }
       }
 
@@ -457,17 +476,18 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
       // The tile goes back to its slot after every chunk (each warp rereads only
       // its own rows, after the next chunk's preparation): between chunks it is
       // an L2 round trip instead of registers held across the preparation.
-      if (c + 1 < nch) {
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          __stcg(reinterpret_cast<float2*>(S_slot + (r0 + g) * K + 8 * nt + 2 * t), make_float2(S[nt][0], S[nt][1]));
-          __stcg(reinterpret_cast<float2*>(S_slot + (r0 + g + 8) * K + 8 * nt + 2 * t), make_float2(S[nt][2], S[nt][3]));
-        }
-      } else {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          __stcs(reinterpret_cast<float2*>(S_slot + (r0 + g) * K + 8 * nt + 2 * t), make_float2(S[nt][0], S[nt][1]));
-          __stcs(reinterpret_cast<float2*>(S_slot + (r0 + g + 8) * K + 8 * nt + 2 * t), make_float2(S[nt][2], S[nt][3]));
+      for (int pp = 0; pp < NT / 2; ++pp) {
+        float4* d0 = reinterpret_cast<float4*>(S_slot + (r0 + g) * K + 16 * pp + 4 * t);
+        float4* d1 = reinterpret_cast<float4*>(S_slot + (r0 + g + 8) * K + 16 * pp + 4 * t);
+        const float4 x = make_float4(S[2 * pp][0], S[2 * pp][1], S[2 * pp + 1][0], S[2 * pp + 1][1]);
+        const float4 y = make_float4(S[2 * pp][2], S[2 * pp][3], S[2 * pp + 1][2], S[2 * pp + 1][3]);
+        if (c + 1 < nch) {
+          __stcg(d0, x);
+          __stcg(d1, y);
+        } else {
+          __stcs(d0, x);
+          __stcs(d1, y);
         }
       }
     }

@@ -54,6 +54,18 @@ constexpr int kFusedThreads = 480;   // 4 recurrence warps, 2 x 4 prep warps, mo
 // bit 2 is set, so the eight rows one ldmatrix 8x8 load reads fall on distinct
 // banks. cm_off gives the element offset of half `half` of row `row`.
 __device__ __forceinline__ int cm_off(int row, int half) { return row * 16 + ((half ^ (row >> 2)) & 1) * 8; }
+// Key order of the recurrence. Within each block of 32 keys, the key the MMAs
+// call 16 j + 8 h + g (m-tile j of the pair, row half h, accumulator row g) is
+// stored key 4 g + 2 j + h, so the four keys a lane holds over a pair of m-tiles
+// are consecutive in memory and a state row moves as one 16-byte access per pair
+// (full 128-byte lines per warp access). The prep thread that writes row r of
+// the key-indexed operand tiles (q_dec, k_res, k_dec and so -W, gamma) takes its
+// q, k and gate from stored key key_of_mma_row(r); the level tiles sum over every
+// key and do not care which.
+__device__ __forceinline__ int key_of_mma_row(int r) {
+  const int x = r & 31;
+  return (r & ~31) + (x & 7) * 4 + ((x >> 4) & 1) * 2 + ((x >> 3) & 1);
+}
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // The chunk operands are those of the unnormalised q, k (the L2 norm is folded
@@ -251,30 +263,32 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     constexpr bool outp = MODE == 2;
     float S[8][4];
     // element (key 16 mi + g (+8), value dv0 + 2t (+1)) of a stored [dv][dk] state
+    // rows dv0 + 2t and dv0 + 2t + 1 of a stored [dv][dk] state; MMA keys
+    // 32 m2 + 16 j + 8 h + g are stored keys 32 m2 + 4 g + 2 j + h (key_of_mma_row)
     auto load_state = [&](const float* src) {
-      const float* b0 = src + static_cast<size_t>(dv0 + 2 * t) * FD + g;
+      const float* b0 = src + static_cast<size_t>(dv0 + 2 * t) * FD + 4 * g;
 #pragma unroll
-      for (int mi = 0; mi < 8; ++mi) {
-        S[mi][0] = __ldcs(b0 + 16 * mi);
-        S[mi][1] = __ldcs(b0 + FD + 16 * mi);
-        S[mi][2] = __ldcs(b0 + 16 * mi + 8);
-        S[mi][3] = __ldcs(b0 + FD + 16 * mi + 8);
+      for (int m2 = 0; m2 < 4; ++m2) {
+        const float4 x = __ldcs(reinterpret_cast<const float4*>(b0 + 32 * m2));
+        const float4 y = __ldcs(reinterpret_cast<const float4*>(b0 + FD + 32 * m2));
+        S[2 * m2][0] = x.x; S[2 * m2][2] = x.y; S[2 * m2 + 1][0] = x.z; S[2 * m2 + 1][2] = x.w;
+        S[2 * m2][1] = y.x; S[2 * m2][3] = y.y; S[2 * m2 + 1][1] = y.z; S[2 * m2 + 1][3] = y.w;
       }
     };
     auto store_state = [&](float* dst, bool streaming) {
-      float* b0 = dst + static_cast<size_t>(dv0 + 2 * t) * FD + g;
+      float* b0 = dst + static_cast<size_t>(dv0 + 2 * t) * FD + 4 * g;
 #pragma unroll
-      for (int mi = 0; mi < 8; ++mi) {
+      for (int m2 = 0; m2 < 4; ++m2) {
+        float4* d0 = reinterpret_cast<float4*>(b0 + 32 * m2);
+        float4* d1 = reinterpret_cast<float4*>(b0 + FD + 32 * m2);
+        const float4 x = make_float4(S[2 * m2][0], S[2 * m2][2], S[2 * m2 + 1][0], S[2 * m2 + 1][2]);
+        const float4 y = make_float4(S[2 * m2][1], S[2 * m2][3], S[2 * m2 + 1][1], S[2 * m2 + 1][3]);
         if (streaming) {
-          __stcs(b0 + 16 * mi, S[mi][0]);
-          __stcs(b0 + FD + 16 * mi, S[mi][1]);
-          __stcs(b0 + 16 * mi + 8, S[mi][2]);
-          __stcs(b0 + FD + 16 * mi + 8, S[mi][3]);
+          __stcs(d0, x);
+          __stcs(d1, y);
         } else {
-          b0[16 * mi] = S[mi][0];
-          b0[FD + 16 * mi] = S[mi][1];
-          b0[16 * mi + 8] = S[mi][2];
-          b0[FD + 16 * mi + 8] = S[mi][3];
+          *d0 = x;
+          *d1 = y;
         }
       }
     };
@@ -384,14 +398,15 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     // (c = rank + 4 j), so two chunks are in flight and each group's latency
     // hides behind the other's.
     const int grp = (warp - 4) >> 2;
-    const int pt = tid - 128 * (1 + grp);  // key / value channel owned by this thread
+    const int pt = tid - 128 * (1 + grp);  // value channel and key-operand row owned by this thread
+    const int kc = key_of_mma_row(pt);     // the key channel behind that row
     const int pw = pt >> 5;                // warp index 0..3 within the group
     const uint32_t bar_id = grp == 0 ? 1u : 4u;
     auto prep_bar = [bar_id] { named_bar_sync(bar_id, 128); };
     PrepScratch<Q>& ps = sm.ps[grp];
     constexpr float kLog2e = 1.4426950408889634f;
     const float Aexp = (p.gate_mode == 2) ? expf(p.A_log[h]) : 0.f;
-    const float dtb2 = (p.gate_mode == 2) ? p.dt_bias[h * FD + pt] * kLog2e : 0.f;  // dt_bias in log2 units
+    const float dtb2 = (p.gate_mode == 2) ? p.dt_bias[h * FD + kc] * kLog2e : 0.f;  // dt_bias in log2 units
     bool failed = false;
     int c = static_cast<int>(rank) + kCtas * grp;
     // beta and the per-head gate of the group's chunks: lanes 0-15 of the
@@ -482,8 +497,8 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       float qv[16], kv[16], al[16], vv[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        qv[i] = __bfloat162float(in.q[i][pt]);
-        kv[i] = __bfloat162float(in.k[i][pt]);
+        qv[i] = __bfloat162float(in.q[i][kc]);
+        kv[i] = __bfloat162float(in.k[i][kc]);
         vv[i] = __bfloat162float(in.v[i][pt]);
       }
       // One branch for the gate mode around the whole token loop, so the 16
@@ -497,7 +512,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         const float nA = -Aexp;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float y = fmaf(in.a[i][pt], kLog2e, dtb2);
+          const float y = fmaf(in.a[i][kc], kLog2e, dtb2);
           const float sp2 = fmaxf(lg2_approx(1.f + ex2_approx(fminf(y, kClamp))), y);
           al[i] = ex2_approx(nA * sp2);
         }
@@ -506,7 +521,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         for (int i = 0; i < 16; ++i) al[i] = ex2_approx(ps.ghead[jb][i] * kLog2e);
       } else if (p.gate_mode == 1) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) al[i] = ex2_approx(in.a[i][pt] * kLog2e);
+        for (int i = 0; i < 16; ++i) al[i] = ex2_approx(in.a[i][kc] * kLog2e);
       } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i) al[i] = 1.f;
@@ -547,25 +562,27 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
 #pragma unroll
       for (int i = 14; i >= 0; --i) Rs[i] = Rs[i + 1] * al[i + 1];
       {
-        // channel pt's 16 tokens of each channel-major tile, two 16-byte stores each
-        auto put16 = [&](uint16_t* tile, const uint32_t (&w)[8]) {
-          *reinterpret_cast<uint4*>(tile + cm_off(pt, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
-          *reinterpret_cast<uint4*>(tile + cm_off(pt, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+        // channel pt's 16 tokens of each channel-major tile, two 16-byte stores each,
+        // at row `row` (the MMA key order for the key-indexed tiles, the channel
+        // itself for the value and level tiles)
+        auto put16 = [&](uint16_t* tile, const uint32_t (&w)[8], int row) {
+          *reinterpret_cast<uint4*>(tile + cm_off(row, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(tile + cm_off(row, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
         };
         uint32_t w[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) w[i] = Bf16::pack(qv[2 * i] * P[2 * i], qv[2 * i + 1] * P[2 * i + 1]);
-        put16(&po.qd[0][0], w);
+        put16(&po.qd[0][0], w, pt);
 #pragma unroll
         for (int i = 0; i < 8; ++i) w[i] = ST2::pack(kv[2 * i] * Rs[2 * i], kv[2 * i + 1] * Rs[2 * i + 1]);
-        put16(&po.kr[0][0], w);
+        put16(&po.kr[0][0], w, pt);
         if (DELTA) {
 #pragma unroll
           for (int i = 0; i < 8; ++i) w[i] = QK::pack(kv[2 * i] * P[2 * i], kv[2 * i + 1] * P[2 * i + 1]);
-          put16(reinterpret_cast<uint16_t*>(&ps.kdec[0][0]), w);
+          put16(reinterpret_cast<uint16_t*>(&ps.kdec[0][0]), w, pt);
 #pragma unroll
           for (int i = 0; i < 8; ++i) w[i] = Bf16::pack(vv[2 * i], vv[2 * i + 1]);
-          put16(reinterpret_cast<uint16_t*>(&ps.vs[0][0]), w);
+          put16(reinterpret_cast<uint16_t*>(&ps.vs[0][0]), w, pt);
         }
         po.gamma[pt] = P[15];
 #pragma unroll
@@ -592,7 +609,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           }
 #pragma unroll
           for (int i = 0; i < 8; ++i) w[i] = QK::pack(ar[2 * i], ar[2 * i + 1]);
-          put16(reinterpret_cast<uint16_t*>(&ps.A_lv[lv][0][0]), w);
+          put16(reinterpret_cast<uint16_t*>(&ps.A_lv[lv][0][0]), w, pt);
           *reinterpret_cast<uint4*>(&ps.B_lv[lv][pt][0]) =
               make_uint4(QK::pack(bc[0], bc[1]), QK::pack(bc[2], bc[3]), QK::pack(bc[4], bc[5]), QK::pack(bc[6], bc[7]));
         }

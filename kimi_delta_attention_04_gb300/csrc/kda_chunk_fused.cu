@@ -68,6 +68,11 @@ __device__ __forceinline__ int key_of_mma_row(int r) {
 }
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+// Rows of U~ are padded to 20 floats: a recurrence lane reads rows 2t and 2t + 1
+// of its value columns at token g, and with 80-byte rows the four t of a warp
+// fall on distinct banks (16-float rows put them all on one).
+constexpr int kUtPitch = 20;
+
 // The chunk operands are those of the unnormalised q, k (the L2 norm is folded
 // in, see the prep): U' = diag(rk) U is the U operand, o_i = sr_i O'_i with
 // O' = qd S + mqk U' and sr_i = scale rq_i.
@@ -78,10 +83,10 @@ struct __align__(16) Stage {
   uint16_t mqk[16][24];    // st2, raw q_i . k_j e^{G_i - G_j} (j <= i)
   float gamma[FD];         // e^{G_last}
   float sr[16];            // output factor of each token: scale rq_i
-  float ut[kRows][16];     // U~' rows of this CTA (transposed)
+  float ut[kRows][kUtPitch];  // U~' rows of this CTA (transposed; tokens 0-15 of each row used)
 };
 constexpr uint32_t kSharedBytes = offsetof(Stage, ut);
-constexpr uint32_t kUtSliceBytes = sizeof(float) * kRows * 16;
+constexpr uint32_t kUtSliceBytes = sizeof(float) * kRows * kUtPitch;
 constexpr uint32_t kStageTx = kSharedBytes + kUtSliceBytes;
 static_assert(kSharedBytes % 16 == 0 && kStageTx == sizeof(Stage), "stage layout");
 
@@ -92,7 +97,7 @@ struct __align__(16) PrepOut {
   uint16_t mqk[16][24];
   float gamma[FD];
   float sr[16];
-  float ut[FD][16];  // all value rows
+  float ut[FD][kUtPitch];  // all value rows
 };
 static_assert(offsetof(PrepOut, ut) == kSharedBytes, "prep-out and stage share the layout");
 

@@ -68,11 +68,13 @@ __device__ __forceinline__ int key_of_mma_row(int r) {
 }
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
-// Rows of U~ are padded to 20 floats: a recurrence lane reads rows 2t and 2t + 1
-// of its value columns at token g, and with 80-byte rows the four t of a warp
-// fall on distinct banks (16-float rows put them all on one).
-constexpr int kUtPitch = 20;
-
+// U~ is kept in the order of an m16n8 accumulator: ut[j][lane] holds, for value
+// rows 8 j .. 8 j + 7, the four values lane (g, t) of an accumulator holds
+// (rows 8 j + 2 t, 8 j + 2 t + 1 at tokens g and g + 8). The prep lane that
+// computes them and the recurrence lane that adds them to its U accumulator are
+// the same (g, t), so each moves them as one 16-byte access.
+// gamma is indexed by stored key: a recurrence lane's four decay factors of a
+// pair of m-tiles are then one 16-byte load.
 // The chunk operands are those of the unnormalised q, k (the L2 norm is folded
 // in, see the prep): U' = diag(rk) U is the U operand, o_i = sr_i O'_i with
 // O' = qd S + mqk U' and sr_i = scale rq_i.
@@ -81,12 +83,12 @@ struct __align__(16) Stage {
   uint16_t qd[FD][16];     // bf16, (q e^{G})^T, channel-major
   uint16_t kr[FD][16];     // st2, (k e^{G_last - G})^T, channel-major
   uint16_t mqk[16][24];    // st2, raw q_i . k_j e^{G_i - G_j} (j <= i)
-  float gamma[FD];         // e^{G_last}
+  float gamma[FD];         // e^{G_last} by stored key
   float sr[16];            // output factor of each token: scale rq_i
-  float ut[kRows][kUtPitch];  // U~' rows of this CTA (transposed; tokens 0-15 of each row used)
+  float ut[kRows / 8][32][4];  // U~' of this CTA's value rows, accumulator order
 };
 constexpr uint32_t kSharedBytes = offsetof(Stage, ut);
-constexpr uint32_t kUtSliceBytes = sizeof(float) * kRows * kUtPitch;
+constexpr uint32_t kUtSliceBytes = sizeof(float) * kRows * 16;
 constexpr uint32_t kStageTx = kSharedBytes + kUtSliceBytes;
 static_assert(kSharedBytes % 16 == 0 && kStageTx == sizeof(Stage), "stage layout");
 
@@ -97,7 +99,7 @@ struct __align__(16) PrepOut {
   uint16_t mqk[16][24];
   float gamma[FD];
   float sr[16];
-  float ut[FD][kUtPitch];  // all value rows
+  float ut[FD / 8][32][4];  // all value rows
 };
 static_assert(offsetof(PrepOut, ut) == kSharedBytes, "prep-out and stage share the layout");
 
@@ -345,10 +347,10 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       const Stage& st = sm.ring[s];
       // U = U~ + (-W) S over all keys (the serial path), two accumulator chains
       float u[4], u2[4] = {0.f, 0.f, 0.f, 0.f};
-      u[0] = st.ut[dvl + 2 * t][g];
-      u[1] = st.ut[dvl + 2 * t + 1][g];
-      u[2] = st.ut[dvl + 2 * t][g + 8];
-      u[3] = st.ut[dvl + 2 * t + 1][g + 8];
+      {
+        const float4 x = *reinterpret_cast<const float4*>(&st.ut[warp][lane][0]);
+        u[0] = x.x; u[1] = x.y; u[2] = x.z; u[3] = x.w;
+      }
       if (DELTA) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -364,11 +366,13 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       const uint32_t ub0 = movmatrix_trans(ST2::pack(u[0], u[1]));
       const uint32_t ub1 = movmatrix_trans(ST2::pack(u[2], u[3]));
       // S = diag(gamma) S + k_res^T U, key rows 16 mi .. 16 mi + 15 at a time
+      float4 gq;  // decay of key rows 16 mi + g, + 8 of m-tiles mi and mi + 1 (mi even)
 #pragma unroll
       for (int mi = 0; mi < (outp ? 0 : 8); ++mi) {
         uint32_t a[4];
         ldsm_x4(a, &st.kr[0][0] + cm_off(16 * mi + ak_row, ak_half));
-        const float g0 = st.gamma[16 * mi + g], g1 = st.gamma[16 * mi + g + 8];
+        if ((mi & 1) == 0) gq = *reinterpret_cast<const float4*>(&st.gamma[32 * (mi >> 1) + 4 * g]);
+        const float g0 = (mi & 1) ? gq.z : gq.x, g1 = (mi & 1) ? gq.w : gq.y;
         S[mi][0] *= g0; S[mi][1] *= g0; S[mi][2] *= g1; S[mi][3] *= g1;
         mma16816<ST2>(S[mi], a, ub0, ub1);
       }
@@ -589,7 +593,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           for (int i = 0; i < 8; ++i) w[i] = Bf16::pack(vv[2 * i], vv[2 * i + 1]);
           put16(reinterpret_cast<uint16_t*>(&ps.vs[0][0]), w, pt);
         }
-        po.gamma[pt] = P[15];
+        po.gamma[kc] = P[15];
 #pragma unroll
         for (int lv = 0; lv < 4; ++lv) {
           const int s = 8 >> lv;
@@ -750,23 +754,19 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           mma16816<Bf16>(u0, alo, b[0], b[1]);
           mma16816<Bf16>(u1, ahi, b[2], b[3]);
           mma16816<Bf16>(u1, alo, b[2], b[3]);
-          po.ut[n0 + 2 * t][g] = u0[0];
-          po.ut[n0 + 2 * t + 1][g] = u0[1];
-          po.ut[n0 + 2 * t][g + 8] = u0[2];
-          po.ut[n0 + 2 * t + 1][g + 8] = u0[3];
-          po.ut[n0 + 8 + 2 * t][g] = u1[0];
-          po.ut[n0 + 8 + 2 * t + 1][g] = u1[1];
-          po.ut[n0 + 8 + 2 * t][g + 8] = u1[2];
-          po.ut[n0 + 8 + 2 * t + 1][g + 8] = u1[3];
+          *reinterpret_cast<float4*>(&po.ut[n0 >> 3][lane][0]) = make_float4(u0[0], u0[1], u0[2], u0[3]);
+          *reinterpret_cast<float4*>(&po.ut[(n0 >> 3) + 1][lane][0]) = make_float4(u1[0], u1[1], u1[2], u1[3]);
         }
       } else {
         // delta rule off: U' = diag(rk) v, value channel pt of the 16 tokens
         float uv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) uv[i] = vv[i] * __shfl_sync(0xffffffffu, rk_l, i);
-        float4* ut = reinterpret_cast<float4*>(&po.ut[pt][0]);
+        // value row pt at token i sits in lane 4 (i % 8) + (pt % 8) / 2 of its
+        // 8-row group, entry 2 (i / 8) + pt % 2
+        float(*ut)[4] = po.ut[pt >> 3];
 #pragma unroll
-        for (int i = 0; i < 16; i += 4) ut[i / 4] = make_float4(uv[i], uv[i + 1], uv[i + 2], uv[i + 3]);
+        for (int i = 0; i < 16; ++i) ut[4 * (i & 7) + ((pt & 7) >> 1)][2 * (i >> 3) + (pt & 1)] = uv[i];
       }
       prep_bar();  // (G) every store into the slot precedes the hand-off
       sig_pending = j;

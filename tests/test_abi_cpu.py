@@ -129,8 +129,8 @@ def test_workspace_size_formula(lib):
     # bf16 d=128 runs the fused kernel: the varlen plan header (N + 2 int32, rounded to 256),
     # then a fixed pool: a 256-byte map of 40 per-cluster rings, each 16 slots of one
     # prepared chunk (3 x 128 x 16 16-bit operands, 16 x 24 Mqk, 128 gamma, 16 output
-    # factors, 128 rows of U~ padded to 20 floats)
-    slot = 3 * 128 * 16 * 2 + 16 * 24 * 2 + 128 * 4 + 16 * 4 + 128 * 20 * 4
+    # factors, 128 x 16 U~)
+    slot = 3 * 128 * 16 * 2 + 16 * 24 * 2 + 128 * 4 + 16 * 4 + 128 * 16 * 4
     pool = 256 + 40 * 16 * slot
     assert _ws(lib, a) == 256 + pool
     assert _ws(lib, _chunk(cu_seqlens=FAKE, N=100)) == 512 + pool

@@ -47,45 +47,55 @@ constexpr int kRows = FD / kCtas;    // value rows per CTA
 constexpr int kRing = 4;             // local stages per CTA
 constexpr int kGRing = 16;           // global ring slots per cluster (a multiple of kCtas)
 constexpr int kPool = 40;            // cluster rings in the workspace pool (> clusters resident at once)
-constexpr int kFusedThreads = 480;   // 4 recurrence warps, 2 x 4 prep warps, mover, publisher, output
+constexpr int kRecWarps = 2;         // recurrence warps, 16 value rows each
+// 16 warps. A warp issues from sub-partition (warp id mod 4); the serial
+// recurrence gets sub-partitions 0 and 1 to itself and the light roles, the
+// eight prep warps take sub-partitions 2 and 3:
+//   warps 0, 1: recurrence; 4: mover; 5: publisher; 13: output; 8, 9, 12: idle
+//   (the output pass, which has no chain, runs warps 8, 9 as a second
+//   recurrence pair on the odd chunks); warps 2, 3, 6, 7: prep group 0;
+//   10, 11, 14, 15: prep group 1.
+constexpr int kFusedThreads = 512;
+constexpr int kMoverWarp = 4, kPublisherWarp = 5, kOutputWarp = 13;
 // Channel-major 16-bit tiles [channel][16 tokens]: one channel's 16 tokens are
 // one 32-byte row, so the thread that owns a channel writes it with two 16-byte
 // stores. The two 16-byte halves (tokens 0-7, 8-15) are swapped on rows whose
 // bit 2 is set, so the eight rows one ldmatrix 8x8 load reads fall on distinct
 // banks. cm_off gives the element offset of half `half` of row `row`.
 __device__ __forceinline__ int cm_off(int row, int half) { return row * 16 + ((half ^ (row >> 2)) & 1) * 8; }
-// Key order of the recurrence. Within each block of 32 keys, the key the MMAs
-// call 16 j + 8 h + g (m-tile j of the pair, row half h, accumulator row g) is
-// stored key 4 g + 2 j + h, so the four keys a lane holds over a pair of m-tiles
-// are consecutive in memory and a state row moves as one 16-byte access per pair
-// (full 128-byte lines per warp access). The prep thread that writes row r of
-// the key-indexed operand tiles (q_dec, k_res, k_dec and so -W, gamma) takes its
-// q, k and gate from stored key key_of_mma_row(r); the level tiles sum over every
-// key and do not care which.
+// Key order of the recurrence. It holds S^T [value x key] as m16n8 accumulators
+// whose n-tile nt covers MMA keys 8 nt .. 8 nt + 7. Within each block of 16
+// keys, the key the MMAs call 8 j + 2 t + e (n-tile j of the pair, column pair
+// of lane t) is stored key 4 t + 2 j + e, so the four keys a lane holds over a
+// pair of n-tiles are consecutive in memory and a state row moves as one
+// 16-byte access per pair. The prep thread that writes row r of the
+// key-indexed operand tiles (q_dec, k_res, k_dec and so -W) takes its q, k and
+// gate from stored key key_of_mma_row(r); the level tiles sum over every key
+// and do not care which.
 __device__ __forceinline__ int key_of_mma_row(int r) {
-  const int x = r & 31;
-  return (r & ~31) + (x & 7) * 4 + ((x >> 4) & 1) * 2 + ((x >> 3) & 1);
+  const int x = r & 15;
+  return (r & ~15) + ((x >> 1) & 3) * 4 + ((x >> 3) & 1) * 2 + (x & 1);
 }
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
-// U~ is kept in the order of an m16n8 accumulator: ut[j][lane] holds, for value
-// rows 8 j .. 8 j + 7, the four values lane (g, t) of an accumulator holds
-// (rows 8 j + 2 t, 8 j + 2 t + 1 at tokens g and g + 8). The prep lane that
-// computes them and the recurrence lane that adds them to its U accumulator are
-// the same (g, t), so each moves them as one 16-byte access.
-// gamma is indexed by stored key: a recurrence lane's four decay factors of a
-// pair of m-tiles are then one 16-byte load.
+// -W'^T and U~'^T travel in the recurrence's register order. W[kk][lane] holds
+// lane's B fragments of -W'^T for keys 16 kk .. 16 kk + 15 (token tiles 0 and 1);
+// ut[m][j][lane] holds lane's accumulator of U~'^T for value rows 16 m .. 16 m +
+// 15 and tokens 8 j .. 8 j + 7. The prep lane that computes them and the
+// recurrence lane that uses them are the same (g, t), so each moves them as one
+// 16-byte access. gamma is indexed by stored key: a lane's four decay factors
+// of a pair of n-tiles are then one 16-byte load.
 // The chunk operands are those of the unnormalised q, k (the L2 norm is folded
 // in, see the prep): U' = diag(rk) U is the U operand, o_i = sr_i O'_i with
 // O' = qd S + mqk U' and sr_i = scale rq_i.
 struct __align__(16) Stage {
-  uint16_t W[FD][16];      // bf16, -W'^T = -(diag(rk) INV diag(beta rk) k_dec)^T, channel-major
+  uint4 W[FD / 16][32];    // bf16 pairs, -W'^T = -(diag(rk) INV diag(beta rk) k_dec)^T, B fragments
   uint16_t qd[FD][16];     // bf16, (q e^{G})^T, channel-major
   uint16_t kr[FD][16];     // st2, (k e^{G_last - G})^T, channel-major
   uint16_t mqk[16][24];    // st2, raw q_i . k_j e^{G_i - G_j} (j <= i)
   float gamma[FD];         // e^{G_last} by stored key
   float sr[16];            // output factor of each token: scale rq_i
-  float ut[kRows / 8][32][4];  // U~' of this CTA's value rows, accumulator order
+  float4 ut[kRows / 16][2][32];  // U~'^T of this CTA's value rows, accumulators
 };
 constexpr uint32_t kSharedBytes = offsetof(Stage, ut);
 constexpr uint32_t kUtSliceBytes = sizeof(float) * kRows * 16;
@@ -93,13 +103,13 @@ constexpr uint32_t kStageTx = kSharedBytes + kUtSliceBytes;
 static_assert(kSharedBytes % 16 == 0 && kStageTx == sizeof(Stage), "stage layout");
 
 struct __align__(16) PrepOut {
-  uint16_t W[FD][16];
+  uint4 W[FD / 16][32];
   uint16_t qd[FD][16];
   uint16_t kr[FD][16];
   uint16_t mqk[16][24];
   float gamma[FD];
   float sr[16];
-  float ut[FD / 8][32][4];  // all value rows
+  float4 ut[FD / 16][2][32];  // all value rows
 };
 static_assert(offsetof(PrepOut, ut) == kSharedBytes, "prep-out and stage share the layout");
 
@@ -136,7 +146,20 @@ struct __align__(16) RecScratch {
   float opart[kRing][16][kOPitch];  // [stage][token][value row]: O of the stage's chunk
 };
 
-template <typename Q>
+// Output pass: each of the four recurrence warps (two pairs, even and odd
+// chunks) keeps its 16 rows of the state entering its next chunk in s[wi][pair],
+// bulk-loaded row by row (rows padded to 144 floats, so a quarter warp's
+// 16-byte reads of rows g and g + 1 fall on distinct banks).
+constexpr int kSnapPitch = FD + 16;
+template <bool ON>
+struct __align__(16) SnapStage {  // 16-byte rows: bulk-copy destinations and float4 reads
+  float s[kRecWarps][2][16][kSnapPitch];
+  uint64_t bar[kRecWarps][2];
+};
+template <>
+struct SnapStage<false> {};
+
+template <typename Q, int MODE>
 struct __align__(128) FusedSmem {
   Stage ring[kRing];
   PrepIn pin[2];                   // input tiles of prep group g
@@ -150,6 +173,7 @@ struct __align__(128) FusedSmem {
   uint64_t sig[kGRing / kCtas];    // this CTA's slot written (prep -> publisher)
   uint64_t pinbar[2];              // input tiles of group g loaded (TMA -> prep)
   int ring_id;                     // pool ring of this cluster (CTA 0's copy is authoritative)
+  SnapStage<MODE == 2> snap;
 };
 
 __device__ __forceinline__ int row_tok_f(int s, int r) { return (r / s) * 2 * s + s + (r % s); }
@@ -210,7 +234,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
   using QK = std::conditional_t<L2N, F16, Bf16>;
   using ST2 = std::conditional_t<DELTA, F16, Bf16>;
   using Q = typename QK::T;
-  using Smem = FusedSmem<Q>;
+  using Smem = FusedSmem<Q, MODE>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
 
@@ -227,8 +251,8 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
   if (tid == 0) {
     for (int s = 0; s < kRing; ++s) {
       mbar_init(&sm.full[s], 1);
-      mbar_init(&sm.empty[s], 5);
-      mbar_init(&sm.ofull[s], 4);
+      mbar_init(&sm.empty[s], kRecWarps + 1);
+      mbar_init(&sm.ofull[s], kRecWarps);
     }
     for (int i = 0; i < kGRing; ++i) {
       mbar_init(&sm.ready[i], 1);
@@ -238,6 +262,9 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.pinbar[b], 1);
     }
+    if constexpr (MODE == 2)
+      for (int w = 0; w < kRecWarps; ++w)
+        for (int b = 0; b < 2; ++b) mbar_init(&sm.snap.bar[w][b], 1);
     sm.ring_id = (rank == 0 && nch0 > 0) ? claim_ring(p.records, p.err) : -1;
     fence_mbarrier_init_cluster();
   }
@@ -250,46 +277,54 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
   unsigned char* const gring =
       p.records + kPoolHeader + static_cast<size_t>(ring_id >= 0 ? ring_id : 0) * kRingBytes;
 
-  if (warp < 4) {
+  if (warp < kRecWarps || (MODE == 2 && (warp == 8 || warp == 9))) {
     // ===================== recurrence warps =====================
-    // Warp w owns value columns [dv0, dv0 + 8) of the CTA's 32 and all 128 key
-    // rows: S [d_k x 8] fp32 as eight m16n8 accumulators, S[mi] = key rows
-    // 16 mi .. 16 mi + 15. Every contraction over d_k is then inside the warp.
+    // Warp w owns value rows [dv0, dv0 + 16) of the CTA's 32 and all 128 keys:
+    // S^T [16 x d_k] fp32 in registers as sixteen m16n8 accumulators, ST[nt] =
+    // MMA keys 8 nt .. 8 nt + 7. Every contraction over d_k stays inside the
+    // warp, and two n-tiles of an accumulator are one A fragment, so S^T and U^T
+    // enter their next MMAs by a conversion alone:
+    //   U^T = U~^T + S^T (-W)^T,  O^T = S^T q_dec^T + U^T Mqk^T,
+    //   S^T <- S^T diag(gamma) + U^T k_res.
     const int g = lane >> 2, t = lane & 3;
-    const int dvl = warp * 8;                                 // first value column within the CTA
-    const int dv0 = static_cast<int>(rank) * kRows + dvl;    // first value row of the stored state
-    // ldmatrix row addresses: A fragments [token][key] of a channel-major tile
-    // ([key][16 tokens]) come from .trans loads with lane matrix m = (key half
-    // m >> 1, token half m & 1); A fragments [key][token] (k_res^T) from plain
-    // loads with m = (key half m & 1, token half m >> 1).
-    const int at_row = (lane >> 4) * 8 + (lane & 7), at_half = (lane >> 3) & 1;
-    const int ak_row = ((lane >> 3) & 1) * 8 + (lane & 7), ak_half = lane >> 4;
-    const int mq_row = ((lane >> 3) & 1) * 8 + (lane & 7), mq_col = (lane >> 4) * 8;
-    // Output pass: no recurrence; S holds the next chunk's entering state,
-    // loaded from h_chunks one chunk ahead of its use.
+    const int wi = warp & 1;                                 // which 16 of the CTA's value rows
+    const int dvl = wi * 16;                                 // first value row within the CTA
+    const int dv0 = static_cast<int>(rank) * kRows + dvl;   // first value row of the stored state
+    // ldmatrix lane addresses (lane matrix m = lane / 8). B fragments of q_dec^T
+    // ([key][token]) from .trans loads of the channel-major tile, m = (key half
+    // m & 1, token half m >> 1); of k_res ([token][key]) from plain loads, m =
+    // (key half m >> 1, token half m & 1); of Mqk^T from plain loads of the
+    // row-major [i][j] tile, m = (i half m >> 1, j half m & 1).
+    const int bq_row = ((lane >> 3) & 1) * 8 + (lane & 7), bq_half = lane >> 4;
+    const int bk_row = (lane >> 4) * 8 + (lane & 7), bk_half = (lane >> 3) & 1;
+    const int mq_row = (lane >> 4) * 8 + (lane & 7), mq_col = ((lane >> 3) & 1) * 8;
+    // Output pass: no recurrence; each chunk's entering state comes from
+    // h_chunks through the warp's snapshot buffer, and pair `pair` takes the
+    // chunks of its parity.
     constexpr bool outp = MODE == 2;
-    float S[8][4];
-    // element (key 16 mi + g (+8), value dv0 + 2t (+1)) of a stored [dv][dk] state
-    // rows dv0 + 2t and dv0 + 2t + 1 of a stored [dv][dk] state; MMA keys
-    // 32 m2 + 16 j + 8 h + g are stored keys 32 m2 + 4 g + 2 j + h (key_of_mma_row)
+    const int pair = outp ? (warp >> 3) : 0;
+    constexpr int kStep = outp ? 2 : 1;
+    float ST[16][4];
+    // rows dv0 + g and dv0 + g + 8 of a stored [dv][dk] state: stored keys
+    // 16 pp + 4 t .. + 3 are MMA keys 16 pp + 2 t (+1) and 16 pp + 8 + 2 t (+1)
     auto load_state = [&](const float* src) {
-      const float* b0 = src + static_cast<size_t>(dv0 + 2 * t) * FD + 4 * g;
+      const float* r0 = src + static_cast<size_t>(dv0 + g) * FD + 4 * t;
 #pragma unroll
-      for (int m2 = 0; m2 < 4; ++m2) {
-        const float4 x = __ldcs(reinterpret_cast<const float4*>(b0 + 32 * m2));
-        const float4 y = __ldcs(reinterpret_cast<const float4*>(b0 + FD + 32 * m2));
-        S[2 * m2][0] = x.x; S[2 * m2][2] = x.y; S[2 * m2 + 1][0] = x.z; S[2 * m2 + 1][2] = x.w;
-        S[2 * m2][1] = y.x; S[2 * m2][3] = y.y; S[2 * m2 + 1][1] = y.z; S[2 * m2 + 1][3] = y.w;
+      for (int pp = 0; pp < 8; ++pp) {
+        const float4 x = __ldcs(reinterpret_cast<const float4*>(r0 + 16 * pp));
+        const float4 y = __ldcs(reinterpret_cast<const float4*>(r0 + 8 * FD + 16 * pp));
+        ST[2 * pp][0] = x.x; ST[2 * pp][1] = x.y; ST[2 * pp + 1][0] = x.z; ST[2 * pp + 1][1] = x.w;
+        ST[2 * pp][2] = y.x; ST[2 * pp][3] = y.y; ST[2 * pp + 1][2] = y.z; ST[2 * pp + 1][3] = y.w;
       }
     };
     auto store_state = [&](float* dst, bool streaming) {
-      float* b0 = dst + static_cast<size_t>(dv0 + 2 * t) * FD + 4 * g;
+      float* r0 = dst + static_cast<size_t>(dv0 + g) * FD + 4 * t;
 #pragma unroll
-      for (int m2 = 0; m2 < 4; ++m2) {
-        float4* d0 = reinterpret_cast<float4*>(b0 + 32 * m2);
-        float4* d1 = reinterpret_cast<float4*>(b0 + FD + 32 * m2);
-        const float4 x = make_float4(S[2 * m2][0], S[2 * m2][2], S[2 * m2 + 1][0], S[2 * m2 + 1][2]);
-        const float4 y = make_float4(S[2 * m2][1], S[2 * m2][3], S[2 * m2 + 1][1], S[2 * m2 + 1][3]);
+      for (int pp = 0; pp < 8; ++pp) {
+        float4* d0 = reinterpret_cast<float4*>(r0 + 16 * pp);
+        float4* d1 = reinterpret_cast<float4*>(r0 + 8 * FD + 16 * pp);
+        const float4 x = make_float4(ST[2 * pp][0], ST[2 * pp][1], ST[2 * pp + 1][0], ST[2 * pp + 1][1]);
+        const float4 y = make_float4(ST[2 * pp][2], ST[2 * pp][3], ST[2 * pp + 1][2], ST[2 * pp + 1][3]);
         if (streaming) {
           __stcs(d0, x);
           __stcs(d1, y);
@@ -300,43 +335,53 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       }
     };
     auto snapshot = [&](int cc) { return p.h_chunks + (static_cast<size_t>(cb + cc) * H + h) * FD * FD; };
-    if (outp ? nch > 0 : (ok && p.h0 != nullptr)) {
-      load_state(outp ? snapshot(0) : p.h0 + (static_cast<size_t>(n) * H + h) * FD * FD);
-    } else {
+    if (!outp) {
+      if (ok && p.h0 != nullptr) {
+        load_state(p.h0 + (static_cast<size_t>(n) * H + h) * FD * FD);
+      } else {
 #pragma unroll
-      for (int mi = 0; mi < 8; ++mi) S[mi][0] = S[mi][1] = S[mi][2] = S[mi][3] = 0.f;
+        for (int nt = 0; nt < 16; ++nt) ST[nt][0] = ST[nt][1] = ST[nt][2] = ST[nt][3] = 0.f;
+      }
     }
     bool failed = false;
-    // O of the previous chunk, handed to the output warp once the next chunk's
-    // U MMAs are issued (its MMAs have completed by then)
-    float o[4] = {0.f, 0.f, 0.f, 0.f};
+    float o[2][4];  // O^T of the chunk: value rows g, g + 8, tokens 8 j + 2 t (+1)
     auto post_output = [&](int cc) {
       float (*op)[kOPitch] = sm.rs.opart[cc & (kRing - 1)];
-      *reinterpret_cast<float2*>(&op[g][dvl + 2 * t]) = make_float2(o[0], o[1]);
-      *reinterpret_cast<float2*>(&op[g + 8][dvl + 2 * t]) = make_float2(o[2], o[3]);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int tk = 8 * j + 2 * t;
+        op[tk][dvl + g] = o[j][0];
+        op[tk + 1][dvl + g] = o[j][1];
+        op[tk][dvl + g + 8] = o[j][2];
+        op[tk + 1][dvl + g + 8] = o[j][3];
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive_local(&sm.ofull[cc & (kRing - 1)]);
     };
-    uint32_t sb[8][2];  // S as bf16 B fragments [key][value], one pair per k-step
-    auto pack_state = [&] {
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        sb[kk][0] = movmatrix_trans(Bf16::pack(S[kk][0], S[kk][1]));
-        sb[kk][1] = movmatrix_trans(Bf16::pack(S[kk][2], S[kk][3]));
-      }
-    };
-    pack_state();
     // this CTA's 32 value rows of chunk cc's state: one contiguous 16 KB slab, pulled
-    // into L2 kSnapAhead chunks before its loads
+    // into L2 kSnapAhead chunks before its loads (by the first warp of the pair)
     constexpr int kSnapAhead = 4;
     auto prefetch_state = [&](int cc) {
-      if (warp == 0 && lane == 0 && cc < nch) bulk_prefetch_l2(snapshot(cc) + rank * kRows * FD, kRows * FD * 4);
+      if (wi == 0 && lane == 0 && cc < nch) bulk_prefetch_l2(snapshot(cc) + rank * kRows * FD, kRows * FD * 4);
+    };
+    // the warp's 16 rows of chunk cc's entering state into its snapshot buffer
+    auto load_snap = [&](int cc) {
+      if constexpr (outp) {
+        if (cc < nch) {
+          uint64_t* bar = &sm.snap.bar[wi][cc & 1];
+          if (lane == 0) mbar_arrive_expect_tx_local(bar, 16 * FD * 4);
+          __syncwarp();
+          if (lane < 16)
+            bulk_load_g2s(&sm.snap.s[wi][cc & 1][lane][0], snapshot(cc) + static_cast<size_t>(dv0 + lane) * FD,
+                          FD * 4, bar);
+        }
+      }
     };
     if (outp) {
-      for (int cc = 2; cc < 2 + kSnapAhead; ++cc) prefetch_state(cc);
-      if (nch > 1) load_state(snapshot(1));
+      for (int cc = pair + 2; cc < pair + 2 + kSnapAhead; cc += 2) prefetch_state(cc);
+      load_snap(pair);
     }
-    for (int c = 0; c < nch; ++c) {
+    for (int c = pair; c < nch; c += kStep) {
       const int s = c & (kRing - 1);
       const uint32_t par = static_cast<uint32_t>(c / kRing) & 1u;
       if (MODE == 1) store_state(snapshot(c), true);  // the state entering chunk c, before its decay
@@ -344,70 +389,124 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         failed = true;
         if (lane == 0) set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
       }
+      if constexpr (outp) {
+        if (!failed && !mbar_wait_bounded(smem_u32(&sm.snap.bar[wi][c & 1]), static_cast<uint32_t>(c >> 1) & 1u,
+                                          kWaitLimitNs)) {
+          failed = true;
+          if (lane == 0) set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
+        }
+      }
       const Stage& st = sm.ring[s];
-      // U = U~ + (-W) S over all keys (the serial path), two accumulator chains
-      float u[4], u2[4] = {0.f, 0.f, 0.f, 0.f};
-      {
-        const float4 x = *reinterpret_cast<const float4*>(&st.ut[warp][lane][0]);
-        u[0] = x.x; u[1] = x.y; u[2] = x.z; u[3] = x.w;
+      // U^T = U~^T + S^T (-W)^T (the serial path, two accumulator chains per
+      // token tile) and O^T = S^T q_dec^T, one key step of S^T at a time. The
+      // MMAs and ldmatrix loads keep their program order, so each key step's
+      // shared-memory operands are loaded one step ahead of their MMAs.
+      uint32_t bq[2][4];
+      uint4 wv[2];
+      ldsm_x4_trans(bq[0], &st.qd[0][0] + cm_off(bq_row, bq_half));
+      if (DELTA) wv[0] = st.W[0][lane];
+      float u[2][4], u2[2][4];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float4 x = st.ut[wi][j][lane];
+        u[j][0] = x.x; u[j][1] = x.y; u[j][2] = x.z; u[j][3] = x.w;
+        u2[j][0] = u2[j][1] = u2[j][2] = u2[j][3] = 0.f;
+        o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+      }
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        const int cur = kk & 1;
+        if (kk + 1 < 8) {
+          ldsm_x4_trans(bq[cur ^ 1], &st.qd[0][0] + cm_off(16 * (kk + 1) + bq_row, bq_half));
+          if (DELTA) wv[cur ^ 1] = st.W[kk + 1][lane];
+        }
+        uint32_t sa[4];
+        if constexpr (outp) {
+          const float* r0 = &sm.snap.s[wi][c & 1][g][16 * kk + 4 * t];
+          const float4 x = *reinterpret_cast<const float4*>(r0);
+          const float4 y = *reinterpret_cast<const float4*>(r0 + 8 * kSnapPitch);
+          sa[0] = Bf16::pack(x.x, x.y);
+          sa[1] = Bf16::pack(y.x, y.y);
+          sa[2] = Bf16::pack(x.z, x.w);
+          sa[3] = Bf16::pack(y.z, y.w);
+        } else {
+          sa[0] = Bf16::pack(ST[2 * kk][0], ST[2 * kk][1]);
+          sa[1] = Bf16::pack(ST[2 * kk][2], ST[2 * kk][3]);
+          sa[2] = Bf16::pack(ST[2 * kk + 1][0], ST[2 * kk + 1][1]);
+          sa[3] = Bf16::pack(ST[2 * kk + 1][2], ST[2 * kk + 1][3]);
+        }
+        if (DELTA) {
+          float (&acc)[2][4] = cur ? u2 : u;
+          mma16816<Bf16>(acc[0], sa, wv[cur].x, wv[cur].y);
+          mma16816<Bf16>(acc[1], sa, wv[cur].z, wv[cur].w);
+        }
+        mma16816<Bf16>(o[0], sa, bq[cur][0], bq[cur][1]);
+        mma16816<Bf16>(o[1], sa, bq[cur][2], bq[cur][3]);
+      }
+      // the operands of Mqk^T and of the first key step of the state update
+      uint32_t bm[4], bk[2][4];
+      float4 gq[2];
+      ldsm_x4(bm, &st.mqk[mq_row][mq_col]);
+      if (!outp) {
+        ldsm_x4(bk[0], &st.kr[0][0] + cm_off(bk_row, bk_half));
+        gq[0] = *reinterpret_cast<const float4*>(&st.gamma[4 * t]);
+      }
+      if constexpr (outp) {  // the snapshot buffer is read: refill it with the pair's next chunk
+        __syncwarp();
+        fence_proxy_async_smem();
+        load_snap(c + 2);
+        prefetch_state(c + 2 + kSnapAhead);
       }
       if (DELTA) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          uint32_t a[4];
-          ldsm_x4_trans(a, &st.W[0][0] + cm_off(16 * kk + at_row, at_half));
-          mma16816<Bf16>((kk & 1) ? u2 : u, a, sb[kk][0], sb[kk][1]);
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) u[j][e] += u2[j][e];
+      }
+      // U^T as an A fragment [value][token]
+      uint32_t ua[4];
+      ua[0] = ST2::pack(u[0][0], u[0][1]);
+      ua[1] = ST2::pack(u[0][2], u[0][3]);
+      ua[2] = ST2::pack(u[1][0], u[1][1]);
+      ua[3] = ST2::pack(u[1][2], u[1][3]);
+      if (!outp) {
+        // S^T = S^T diag(gamma) + U^T k_res, keys 16 np .. 16 np + 15 at a time,
+        // operands one step ahead
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {
+          const int cur = np & 1;
+          if (np + 1 < 8) {
+            ldsm_x4(bk[cur ^ 1], &st.kr[0][0] + cm_off(16 * (np + 1) + bk_row, bk_half));
+            gq[cur ^ 1] = *reinterpret_cast<const float4*>(&st.gamma[16 * (np + 1) + 4 * t]);
+          }
+          // decay of MMA keys 16 np + 2 t (+1) and 16 np + 8 + 2 t (+1)
+          const float4 gm = gq[cur];
+          ST[2 * np][0] *= gm.x; ST[2 * np][1] *= gm.y; ST[2 * np][2] *= gm.x; ST[2 * np][3] *= gm.y;
+          ST[2 * np + 1][0] *= gm.z; ST[2 * np + 1][1] *= gm.w; ST[2 * np + 1][2] *= gm.z; ST[2 * np + 1][3] *= gm.w;
+          mma16816<ST2>(ST[2 * np], ua, bk[cur][0], bk[cur][1]);
+          mma16816<ST2>(ST[2 * np + 1], ua, bk[cur][2], bk[cur][3]);
+          if (np == 0) {  // O^T += U^T Mqk^T, off the serial path
+            mma16816<ST2>(o[0], ua, bm[0], bm[1]);
+            mma16816<ST2>(o[1], ua, bm[2], bm[3]);
+          }
         }
-#pragma unroll
-        for (int e = 0; e < 4; ++e) u[e] += u2[e];
+      } else {  // O^T += U^T Mqk^T
+        mma16816<ST2>(o[0], ua, bm[0], bm[1]);
+        mma16816<ST2>(o[1], ua, bm[2], bm[3]);
       }
-      if (c > 0) post_output(c - 1);
-      // U as B fragments [token][value]
-      const uint32_t ub0 = movmatrix_trans(ST2::pack(u[0], u[1]));
-      const uint32_t ub1 = movmatrix_trans(ST2::pack(u[2], u[3]));
-      // S = diag(gamma) S + k_res^T U, key rows 16 mi .. 16 mi + 15 at a time
-      float4 gq;  // decay of key rows 16 mi + g, + 8 of m-tiles mi and mi + 1 (mi even)
-#pragma unroll
-      for (int mi = 0; mi < (outp ? 0 : 8); ++mi) {
-        uint32_t a[4];
-        ldsm_x4(a, &st.kr[0][0] + cm_off(16 * mi + ak_row, ak_half));
-        if ((mi & 1) == 0) gq = *reinterpret_cast<const float4*>(&st.gamma[32 * (mi >> 1) + 4 * g]);
-        const float g0 = (mi & 1) ? gq.z : gq.x, g1 = (mi & 1) ? gq.w : gq.y;
-        S[mi][0] *= g0; S[mi][1] *= g0; S[mi][2] *= g1; S[mi][3] *= g1;
-        mma16816<ST2>(S[mi], a, ub0, ub1);
-      }
-      // O = q_dec S_old + Mqk U behind the state update in the tensor pipe
-      o[0] = o[1] = o[2] = o[3] = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        uint32_t a[4];
-        ldsm_x4_trans(a, &st.qd[0][0] + cm_off(16 * kk + at_row, at_half));
-        mma16816<Bf16>(o, a, sb[kk][0], sb[kk][1]);
-      }
-      {
-        uint32_t a[4];
-        ldsm_x4(a, &st.mqk[mq_row][mq_col]);
-        mma16816<ST2>(o, a, ub0, ub1);
-      }
-      pack_state();
-      if (outp) {
-        if (c + 2 < nch) load_state(snapshot(c + 2));
-        prefetch_state(c + 2 + kSnapAhead);
-      }
-      __syncwarp();
+      post_output(c);
       if (lane == 0) mbar_arrive_local(&sm.empty[s]);
     }
-    if (nch > 0) post_output(nch - 1);
     if (ok && p.hT != nullptr && !outp) store_state(p.hT + (static_cast<size_t>(n) * H + h) * FD * FD, false);
-  } else if (warp < 12) {
+  } else if ((warp & 3) >= 2) {
     // ===================== prep warps =====================
     // Chunk c is prepared in shared memory (pout), then copied into global slot
     // c mod kGRing once all four CTAs have loaded that slot's previous chunk.
     // Two groups of four warps; group g prepares this CTA's chunks j = g mod 2
     // (c = rank + 4 j), so two chunks are in flight and each group's latency
     // hides behind the other's.
-    const int grp = (warp - 4) >> 2;
-    const int pt = tid - 128 * (1 + grp);  // value channel and key-operand row owned by this thread
+    const int grp = warp >> 3;
+    const int pt = 32 * (((warp >> 2) & 1) * 2 + (warp & 1)) + lane;  // value channel and key-operand row owned
     const int kc = key_of_mma_row(pt);     // the key channel behind that row
     const int pw = pt >> 5;                // warp index 0..3 within the group
     const uint32_t bar_id = grp == 0 ? 1u : 4u;
@@ -726,7 +825,6 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       }
       prep_bar();  // (F) INV' fragments, Mqk~, the next chunk's beta, clear scratch
       if (DELTA) {
-        const int g = lane >> 2, t = lane & 3;
         uint32_t a[4], ahi[4], alo[4];
         {
           const uint4 x0 = ps.inv[lane][0], x1 = ps.inv[lane][1], x2 = ps.inv[lane][2];
@@ -742,37 +840,40 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
           mma16816<QK>(c0, a, b[0], b[1]);
           mma16816<QK>(c1, a, b[2], b[3]);
-          // -W' blocks (tokens x 8 channels) transposed in registers into -W'^T rows
-          uint16_t* wt = &po.W[0][0];
-          *reinterpret_cast<uint32_t*>(wt + cm_off(n0 + g, 0) + 2 * t) = movmatrix_trans(Bf16::pack(-c0[0], -c0[1]));
-          *reinterpret_cast<uint32_t*>(wt + cm_off(n0 + g, 1) + 2 * t) = movmatrix_trans(Bf16::pack(-c0[2], -c0[3]));
-          *reinterpret_cast<uint32_t*>(wt + cm_off(n0 + 8 + g, 0) + 2 * t) = movmatrix_trans(Bf16::pack(-c1[0], -c1[1]));
-          *reinterpret_cast<uint32_t*>(wt + cm_off(n0 + 8 + g, 1) + 2 * t) = movmatrix_trans(Bf16::pack(-c1[2], -c1[3]));
-          ldsm_x4(b, &ps.vs[0][0] + cm_off(n0 + (lane >> 4) * 8 + (lane & 7), (lane >> 3) & 1));
+          // -W' [tokens x keys n0 .. n0 + 15]: this lane's accumulators are its
+          // B fragments of -W'^T in the recurrence (token tiles 0 and 1)
+          po.W[n0 >> 4][lane] = make_uint4(Bf16::pack(-c0[0], -c0[1]), Bf16::pack(-c1[0], -c1[1]),
+                                           Bf16::pack(-c0[2], -c0[3]), Bf16::pack(-c1[2], -c1[3]));
+          // U~'^T [value rows n0 .. n0 + 15 x tokens] = v^T INV_U^T: A from the
+          // channel-major v tile; the B fragments of INV_U^T are INV_U's A
+          // fragments taken in another order (hi and lo parts)
+          ldsm_x4(b, &ps.vs[0][0] + cm_off(n0 + ((lane >> 3) & 1) * 8 + (lane & 7), lane >> 4));
           float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};
-          mma16816<Bf16>(u0, ahi, b[0], b[1]);
-          mma16816<Bf16>(u0, alo, b[0], b[1]);
-          mma16816<Bf16>(u1, ahi, b[2], b[3]);
-          mma16816<Bf16>(u1, alo, b[2], b[3]);
-          *reinterpret_cast<float4*>(&po.ut[n0 >> 3][lane][0]) = make_float4(u0[0], u0[1], u0[2], u0[3]);
-          *reinterpret_cast<float4*>(&po.ut[(n0 >> 3) + 1][lane][0]) = make_float4(u1[0], u1[1], u1[2], u1[3]);
+          mma16816<Bf16>(u0, b, ahi[0], ahi[2]);
+          mma16816<Bf16>(u0, b, alo[0], alo[2]);
+          mma16816<Bf16>(u1, b, ahi[1], ahi[3]);
+          mma16816<Bf16>(u1, b, alo[1], alo[3]);
+          po.ut[n0 >> 4][0][lane] = make_float4(u0[0], u0[1], u0[2], u0[3]);
+          po.ut[n0 >> 4][1][lane] = make_float4(u1[0], u1[1], u1[2], u1[3]);
         }
       } else {
         // delta rule off: U' = diag(rk) v, value channel pt of the 16 tokens
         float uv[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) uv[i] = vv[i] * __shfl_sync(0xffffffffu, rk_l, i);
-        // value row pt at token i sits in lane 4 (i % 8) + (pt % 8) / 2 of its
-        // 8-row group, entry 2 (i / 8) + pt % 2
-        float(*ut)[4] = po.ut[pt >> 3];
+        // value row pt (row r of its 16-row tile) at token i sits in token tile
+        // i / 8, lane 4 (r % 8) + (i % 8) / 2, entry 2 (r / 8) + i % 2
+        float* ut = reinterpret_cast<float*>(&po.ut[pt >> 4][0][0]);
+        const int r = pt & 15;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) ut[4 * (i & 7) + ((pt & 7) >> 1)][2 * (i >> 3) + (pt & 1)] = uv[i];
+        for (int i = 0; i < 16; ++i)
+          ut[((i >> 3) * 32 + 4 * (r & 7) + ((i & 7) >> 1)) * 4 + 2 * (r >> 3) + (i & 1)] = uv[i];
       }
       prep_bar();  // (G) every store into the slot precedes the hand-off
       sig_pending = j;
     }
     signal_written();
-  } else if (warp == 12) {
+  } else if (warp == kMoverWarp) {
     // ===================== mover warp =====================
     // Loads chunk c from its global slot into local stage c mod kRing once the
     // slot is published and the recurrence warps have released the stage; a
@@ -812,7 +913,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         }
     }
     __syncwarp();
-  } else if (warp == 13) {
+  } else if (warp == kPublisherWarp) {
     // ===================== publisher warp =====================
     // Publishes each chunk the prep groups wrote into the global ring: lanes
     // 0-3 each make the group's stores visible at cluster scope and arrive on
@@ -830,7 +931,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       }
       __syncwarp();
     }
-  } else {
+  } else if (warp == kOutputWarp) {
     // ===================== output warp =====================
     // Stores each chunk's 16 x 32 block of o (lane: one token, 16 value rows)
     // from the staged O and releases the stage.
@@ -902,7 +1003,7 @@ cudaError_t check_cluster_residency_once(Kernel kernel, size_t smem, std::atomic
 template <bool DELTA, bool L2N, int MODE>
 cudaError_t launch_fused_t(const ChunkCall& c, cudaStream_t s) {
   using QK = std::conditional_t<L2N, F16, Bf16>;
-  const size_t smem = sizeof(FusedSmem<typename QK::T>);
+  const size_t smem = sizeof(FusedSmem<typename QK::T, MODE>);
   static std::atomic<uint64_t> smem_set{0}, resident_ok{0}, resident_bad{0};
   {
     cudaError_t e = set_smem_limit_once(kda_chunk_fused_kernel<DELTA, L2N, MODE>, smem, smem_set);
@@ -923,7 +1024,8 @@ cudaError_t launch_fused_t(const ChunkCall& c, cudaStream_t s) {
 
 }  // namespace
 
-static_assert(sizeof(FusedSmem<__half>) <= 227 * 1024 && sizeof(FusedSmem<__nv_bfloat16>) <= 227 * 1024,
+static_assert(sizeof(FusedSmem<__half, 0>) <= 227 * 1024 && sizeof(FusedSmem<__nv_bfloat16, 0>) <= 227 * 1024 &&
+                  sizeof(FusedSmem<__half, 2>) <= 227 * 1024 && sizeof(FusedSmem<__nv_bfloat16, 2>) <= 227 * 1024,
               "fused kernel shared memory");
 
 size_t fused_workspace_bytes() { return kPoolHeader + static_cast<size_t>(kPool) * kRingBytes; }

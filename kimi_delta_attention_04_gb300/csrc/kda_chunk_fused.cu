@@ -384,7 +384,9 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     for (int c = pair; c < nch; c += kStep) {
       const int s = c & (kRing - 1);
       const uint32_t par = static_cast<uint32_t>(c / kRing) & 1u;
-      if (MODE == 1) store_state(snapshot(c), true);  // the state entering chunk c, before its decay
+      // the state entering chunk c (before its decay) goes to h_chunks one key
+      // pair per step of the U loop below, where the MMAs leave issue slots free
+      float* const snap_row = MODE == 1 ? snapshot(c) + static_cast<size_t>(dv0 + g) * FD + 4 * t : nullptr;
       if (!failed && !mbar_wait_bounded(smem_u32(&sm.full[s]), par, kWaitLimitNs)) {
         failed = true;
         if (lane == 0) set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
@@ -434,6 +436,12 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           sa[1] = Bf16::pack(ST[2 * kk][2], ST[2 * kk][3]);
           sa[2] = Bf16::pack(ST[2 * kk + 1][0], ST[2 * kk + 1][1]);
           sa[3] = Bf16::pack(ST[2 * kk + 1][2], ST[2 * kk + 1][3]);
+          if (MODE == 1) {
+            __stcs(reinterpret_cast<float4*>(snap_row + 16 * kk),
+                   make_float4(ST[2 * kk][0], ST[2 * kk][1], ST[2 * kk + 1][0], ST[2 * kk + 1][1]));
+            __stcs(reinterpret_cast<float4*>(snap_row + 8 * FD + 16 * kk),
+                   make_float4(ST[2 * kk][2], ST[2 * kk][3], ST[2 * kk + 1][2], ST[2 * kk + 1][3]));
+          }
         }
         if (DELTA) {
           float (&acc)[2][4] = cur ? u2 : u;

@@ -7,14 +7,17 @@
 // placement:
 //
 //  * CTA r of the cluster owns value rows [32r, 32r + 32) of the state. Each of
-//    its four recurrence warps owns 8 of those value columns and all 128 key
-//    rows: S [128 x 8] fp32 in registers as eight m16n8 mma.sync accumulators,
-//    so every contraction over the keys stays inside the warp (no exchange
-//    between warps on the serial path). S and U reach the B-operand layout by
-//    movmatrix transposes of their accumulators; -W, q_dec and k_res are A
-//    operands loaded from the channel-major tiles. Each warp's O (q_dec S +
-//    Mqk U) is computed behind the state update and staged in shared memory;
-//    an output warp stores o, off the serial path.
+//    its two recurrence warps owns 16 of those rows and all 128 keys: S^T
+//    [16 x 128] fp32 in registers as sixteen m16n8 mma.sync accumulators, so
+//    every contraction over the keys stays inside the warp (no exchange
+//    between warps on the serial path), and two n-tiles of an accumulator are
+//    one A fragment, so S^T and U^T enter their next MMAs by a conversion
+//    alone. q_dec^T and k_res are B operands loaded from the channel-major
+//    tiles; -W'^T and U~'^T arrive in the warp's register order. O^T (S^T
+//    q_dec^T + U^T Mqk^T) is staged in shared memory; an output warp stores o,
+//    off the serial path. The recurrence warps issue from SM sub-partitions 0
+//    and 1 and the prep warps from 2 and 3, so the chain never shares a
+//    scheduler with the prep.
 //  * The same CTA's prep warps prepare every 4th chunk (chunks c = r mod 4):
 //    gate, beta, L2 norm, decay products, L / Mqk, Neumann inverse, W and U~.
 //    Two groups of four warps take alternate ones, each loading its next

@@ -737,38 +737,8 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       prep_bar();  // (D) tiles, level operands and norm partial sums written
       if (pt == 0 && c + 2 * kCtas < nch)
         issue_inputs(maps, sm.pin[buf], &sm.pinbar[buf], h, ts + (c + 2 * kCtas) * kChunk, p.gate_mode);
-      {  // level pw of the anchored split: raw L (rows 0-7, times beta) and Mqk (rows 8-15)
-        const int lv = pw;
-        const int s = 8 >> lv;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kk = 0; kk < FD / 16; ++kk) {
-          uint32_t a[4], b[2];
-          // A^T and B^T are stored [channel][row]: .trans loads; lane matrix m of
-          // A = (row half m & 1, channel half m >> 1)
-          ldsm_x4_trans(a, &ps.A_lv[lv][0][0] + cm_off(16 * kk + (lane >> 4) * 8 + (lane & 7), (lane >> 3) & 1));
-          ldsm_x2_trans(b, &ps.B_lv[lv][16 * kk + (lane & 15)][0]);
-          mma16816<QK>(acc, a, b[0], b[1]);
-        }
-        const int g = lane >> 2, t = lane & 3;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int r = g + ((e & 2) ? 8 : 0);
-          const int cidx = 2 * t + (e & 1);
-          const int rr = r & 7;
-          if (rr / s != cidx / s) continue;
-          const int i = row_tok_f(s, rr), jx = col_tok_f(s, cidx);
-          if (r < 8) {
-            if (DELTA) ps.Lm[i][jx] = ps.beta[jb][i] * acc[e];
-          } else {
-            ps.Mq[i][jx] = acc[e];
-          }
-        }
-        if (pw == 0 && lane < 16)  // the diagonal of Mqk: q~_i . k~_i
-          ps.Mq[lane][lane] = ps.red[0][32 + lane] + ps.red[1][32 + lane] + ps.red[2][32 + lane] + ps.red[3][32 + lane];
-      }
-      prep_bar();  // (E) raw L and Mqk complete
-      // the norm factors of the 16 tokens: lane i < 16 of every warp holds token i's
+      // the norm factors of the 16 tokens (the partial sums are complete): lane
+      // i < 16 of every warp holds token i's
       float rq_l = 1.f, rk_l = 1.f;
       if (L2N && lane < 16) {
         float sq = 0.f, sk = 0.f;
@@ -780,8 +750,47 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         rq_l = rsqrtf(sq + 1e-6f);
         rk_l = rsqrtf(sk + 1e-6f);
       }
+      if (pw == 0 && lane < 16) po.sr[lane] = p.scale * rq_l;
+      {  // level pw of the anchored split: raw L (rows 0-7, times beta) and Mqk (rows 8-15),
+         // two accumulator chains, operands loaded one step ahead
+        const int lv = pw;
+        const int s = 8 >> lv;
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        // A^T and B^T are stored [channel][row]: .trans loads; lane matrix m of
+        // A = (row half m & 1, channel half m >> 1)
+        const int a_row = (lane >> 4) * 8 + (lane & 7), a_half = (lane >> 3) & 1;
+        uint32_t a[2][4], b[2][2];
+        ldsm_x4_trans(a[0], &ps.A_lv[lv][0][0] + cm_off(a_row, a_half));
+        ldsm_x2_trans(b[0], &ps.B_lv[lv][lane & 15][0]);
+#pragma unroll
+        for (int kk = 0; kk < FD / 16; ++kk) {
+          const int cur = kk & 1;
+          if (kk + 1 < FD / 16) {
+            ldsm_x4_trans(a[cur ^ 1], &ps.A_lv[lv][0][0] + cm_off(16 * (kk + 1) + a_row, a_half));
+            ldsm_x2_trans(b[cur ^ 1], &ps.B_lv[lv][16 * (kk + 1) + (lane & 15)][0]);
+          }
+          mma16816<QK>(acc[cur], a[cur], b[cur][0], b[cur][1]);
+        }
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = g + ((e & 2) ? 8 : 0);
+          const int cidx = 2 * t + (e & 1);
+          const int rr = r & 7;
+          if (rr / s != cidx / s) continue;
+          const int i = row_tok_f(s, rr), jx = col_tok_f(s, cidx);
+          const float v = acc[0][e] + acc[1][e];
+          if (r < 8) {
+            if (DELTA) ps.Lm[i][jx] = ps.beta[jb][i] * v;
+          } else {
+            ps.Mq[i][jx] = v;
+          }
+        }
+        if (pw == 0 && lane < 16)  // the diagonal of Mqk: q~_i . k~_i
+          ps.Mq[lane][lane] = ps.red[0][32 + lane] + ps.red[1][32 + lane] + ps.red[2][32 + lane] + ps.red[3][32 + lane];
+      }
+      prep_bar();  // (E) raw L and Mqk complete
       if (pw == 0) {
-        if (lane < 16) po.sr[lane] = p.scale * rq_l;
         if (DELTA) {
           // X = -L = -diag(beta rk) raw diag(rk) in registers, then INV' forms
           const int g = lane >> 2, t = lane & 3;
@@ -800,8 +809,6 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
 #pragma unroll
             for (int e = 0; e < 4; ++e)
               X.c[nt][e] = -ps.Lm[g + 8 * (e >> 1)][8 * nt + 2 * t + (e & 1)] * rkr[e >> 1] * rkc[nt][e & 1];
-          __syncwarp();
-          for (int i = lane; i < 16 * 17; i += 32) (&ps.Lm[0][0])[i] = 0.f;  // clear for the next chunk
           const Frag16 inv = neumann_inverse16_frag<QK>(X, lane);
           Frag16 iw, ihi, ilo;
 #pragma unroll
@@ -821,10 +828,12 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           for (int jj = 0; jj < 3; ++jj) ps.inv[lane][jj] = make_uint4(f[jj][0], f[jj][1], f[jj][2], f[jj][3]);
         }
       } else {
-        // warps 1-3: Mqk~ into the slot, clearing its scratch for the next chunk
+        // warps 1-3: Mqk~ into the slot. The level MMAs rewrite every strictly
+        // lower entry of L and Mqk each chunk (each pair i > j belongs to exactly
+        // one level) and the diagonal of Mqk is rewritten too, so the entries
+        // never written stay at their initial zero: no clearing between chunks.
         for (int e = pt - 32; e < 256; e += 96) {
           const float x = ps.Mq[e >> 4][e & 15];
-          ps.Mq[e >> 4][e & 15] = 0.f;
           const typename ST2::T v = ST2::cvt(x);
           po.mqk[e >> 4][e & 15] = *reinterpret_cast<const uint16_t*>(&v);
         }
@@ -834,7 +843,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           if (c + 4 * kCtas < nch) load_next(c + 4 * kCtas);
         }
       }
-      prep_bar();  // (F) INV' fragments, Mqk~, the next chunk's beta, clear scratch
+      prep_bar();  // (F) INV' fragments, Mqk~, the next chunk's beta
       if (DELTA) {
         uint32_t a[4], ahi[4], alo[4];
         {

@@ -655,23 +655,52 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           }
         }
       }
-      {  // this warp's partial sums of q~.q~, k~.k~, q~.k~ over its 32 channels
-        float red[16];
+      {  // this warp's partial sums of q~.q~, k~.k~ and q~.k~ per token over its 32
+         // channels: the diagonals of Q Q^T, K K^T and Q K^T on the tensor cores (bf16
+         // products are exact in fp32). The warp stages raw channel-major rows of its
+         // own 32 channels in level tiles 2 and 3, which the level operands below
+         // overwrite; as A operands [token][channel] they come from .trans loads, and
+         // the B fragments of Q^T (K^T) are the A fragments of Q (K) in another order.
+        uint16_t* const rq_t = reinterpret_cast<uint16_t*>(&ps.A_lv[2][0][0]);
+        uint16_t* const rk_t = reinterpret_cast<uint16_t*>(&ps.A_lv[3][0][0]);
+        uint32_t w[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) red[i] = qv[i] * qv[i];
-        const float t1 = warp_transpose_reduce16(red, lane);
+        for (int i = 0; i < 8; ++i) w[i] = Bf16::pack(qv[2 * i], qv[2 * i + 1]);
+        *reinterpret_cast<uint4*>(rq_t + cm_off(pt, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(rq_t + cm_off(pt, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) red[i] = kv[i] * kv[i];
-        const float t2 = warp_transpose_reduce16(red, lane);
+        for (int i = 0; i < 8; ++i) w[i] = Bf16::pack(kv[2 * i], kv[2 * i + 1]);
+        *reinterpret_cast<uint4*>(rk_t + cm_off(pt, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(rk_t + cm_off(pt, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+        __syncwarp();
+        // lane matrix m of an A fragment: (channel half m >> 1, token half m & 1)
+        const int r_row = ((lane >> 4) & 1) * 8 + (lane & 7), r_half = (lane >> 3) & 1;
+        float dqq[2][4] = {}, dkk[2][4] = {}, dqk[2][4] = {};
 #pragma unroll
-        for (int i = 0; i < 16; ++i) red[i] = qv[i] * kv[i];
-        const float t3 = warp_transpose_reduce16(red, lane);
-        if ((lane & 1) == 0) {
-          const int jj = lane >> 1;
-          ps.red[pw][jj] = t1;
-          ps.red[pw][16 + jj] = t2;
-          ps.red[pw][32 + jj] = t3;
+        for (int ks = 0; ks < 2; ++ks) {
+          uint32_t aq[4], ak[4];
+          ldsm_x4_trans(aq, rq_t + cm_off(32 * pw + 16 * ks + r_row, r_half));
+          ldsm_x4_trans(ak, rk_t + cm_off(32 * pw + 16 * ks + r_row, r_half));
+          mma16816<Bf16>(dqq[0], aq, aq[0], aq[2]);
+          mma16816<Bf16>(dqq[1], aq, aq[1], aq[3]);
+          mma16816<Bf16>(dkk[0], ak, ak[0], ak[2]);
+          mma16816<Bf16>(dkk[1], ak, ak[1], ak[3]);
+          mma16816<Bf16>(dqk[0], aq, ak[0], ak[2]);
+          mma16816<Bf16>(dqk[1], aq, ak[1], ak[3]);
         }
+        // diagonal element (i, i): token tile i / 8, held by lane (g, g / 2) with
+        // g = i % 8, entry (i % 8) % 2 (+2 in the second token tile)
+        const int g = lane >> 2;
+        if ((g >> 1) == (lane & 3)) {
+          const int e = g & 1;
+          ps.red[pw][g] = e ? dqq[0][1] : dqq[0][0];
+          ps.red[pw][8 + g] = e ? dqq[1][3] : dqq[1][2];
+          ps.red[pw][16 + g] = e ? dkk[0][1] : dkk[0][0];
+          ps.red[pw][24 + g] = e ? dkk[1][3] : dkk[1][2];
+          ps.red[pw][32 + g] = e ? dqk[0][1] : dqk[0][0];
+          ps.red[pw][40 + g] = e ? dqk[1][3] : dqk[1][2];
+        }
+        __syncwarp();  // the staged rows are read before the level operands overwrite them
       }
       float P[16], Rs[16];
       P[0] = al[0];

@@ -89,7 +89,8 @@ __device__ __forceinline__ int rt_cm_off(int row, int half) { return row * 16 + 
 // t) is stored key 4 t + 2 j + e, so the four keys a lane holds across the pair
 // are consecutive in memory and the state moves between L2 and registers as one
 // 16-byte access per row and pair of n-tiles. The operands indexed by key
-// (q_dec, k_res, k_dec, gamma) are laid out in the MMAs' order; L and Mqk sum
+// (q_dec, k_res, k_dec) are laid out in the MMAs' order and gamma by stored key (a
+// lane's four decay factors of a pair of n-tiles are one 16-byte load); L and Mqk sum
 // over every key and do not care.
 __device__ __forceinline__ int rt_mma_key(int key) {
   const int r = key & 15;
@@ -205,21 +206,53 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
         const float sp2 = x > 20.f ? x * kLog2e : l2;
         al[i] = valid ? ex2_approx(nA * sp2) : 1.f;
       }
-      float red[16];
+      // this warp's partial sums of q.q, k.k and q.k per token over its 32 channels:
+      // the diagonals of Q Q^T, K K^T and Q K^T on the tensor cores (bf16 products
+      // are exact in fp32), from raw channel-major rows staged in the q_dec and
+      // k_dec tiles (written again only after the next two barriers); as A
+      // operands [token][channel] they come from .trans loads, and the B fragments
+      // of Q^T (K^T) are the A fragments of Q (K) in another order
+      uint16_t* const rq_t = reinterpret_cast<uint16_t*>(&sm.qd[0][0]);
+      uint16_t* const rk_t = reinterpret_cast<uint16_t*>(&sm.kdec[0][0]);
+      {
+        uint32_t w[8];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) red[i] = qv[i] * qv[i];
-      const float t1 = warp_transpose_reduce16(red, lane);
+        for (int i = 0; i < 8; ++i) w[i] = Bf16::pack(qv[2 * i], qv[2 * i + 1]);
+        *reinterpret_cast<uint4*>(rq_t + rt_cm_off(ch, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(rq_t + rt_cm_off(ch, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
 #pragma unroll
-      for (int i = 0; i < 16; ++i) red[i] = kv[i] * kv[i];
-      const float t2 = warp_transpose_reduce16(red, lane);
+        for (int i = 0; i < 8; ++i) w[i] = Bf16::pack(kv[2 * i], kv[2 * i + 1]);
+        *reinterpret_cast<uint4*>(rk_t + rt_cm_off(ch, 0)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(rk_t + rt_cm_off(ch, 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      __syncwarp();
+      {
+        // lane matrix m of an A fragment: (channel half m >> 1, token half m & 1)
+        const int r_row = ((lane >> 4) & 1) * 8 + (lane & 7), r_half = (lane >> 3) & 1;
+        float dqq[2][4] = {}, dkk[2][4] = {}, dqk[2][4] = {};
 #pragma unroll
-      for (int i = 0; i < 16; ++i) red[i] = qv[i] * kv[i];
-      const float t3 = warp_transpose_reduce16(red, lane);
-      if ((lane & 1) == 0) {
-        const int j = lane >> 1;
-        sm.red[warp][j] = t1;
-        sm.red[warp][16 + j] = t2;
-        sm.red[warp][32 + j] = t3;
+        for (int ks = 0; ks < 2; ++ks) {
+          uint32_t aq[4], ak[4];
+          ldsm_x4_trans(aq, rq_t + rt_cm_off(32 * warp + 16 * ks + r_row, r_half));
+          ldsm_x4_trans(ak, rk_t + rt_cm_off(32 * warp + 16 * ks + r_row, r_half));
+          mma16816<Bf16>(dqq[0], aq, aq[0], aq[2]);
+          mma16816<Bf16>(dqq[1], aq, aq[1], aq[3]);
+          mma16816<Bf16>(dkk[0], ak, ak[0], ak[2]);
+          mma16816<Bf16>(dkk[1], ak, ak[1], ak[3]);
+          mma16816<Bf16>(dqk[0], aq, ak[0], ak[2]);
+          mma16816<Bf16>(dqk[1], aq, ak[1], ak[3]);
+        }
+        // diagonal element (i, i): token tile i / 8, lane (i % 8, (i % 8) / 2),
+        // entry (i % 8) % 2 (+2 in the second token tile)
+        if ((g >> 1) == t) {
+          const int e = g & 1;
+          sm.red[warp][g] = e ? dqq[0][1] : dqq[0][0];
+          sm.red[warp][8 + g] = e ? dqq[1][3] : dqq[1][2];
+          sm.red[warp][16 + g] = e ? dkk[0][1] : dkk[0][0];
+          sm.red[warp][24 + g] = e ? dkk[1][3] : dkk[1][2];
+          sm.red[warp][32 + g] = e ? dqk[0][1] : dqk[0][0];
+          sm.red[warp][40 + g] = e ? dqk[1][3] : dqk[1][2];
+        }
       }
     }
     if (vown) {  // v rows into the channel-major tile (raw bf16 bits, two tokens per word)
@@ -279,7 +312,7 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
 #pragma unroll
       for (int i = 0; i < 8; ++i) w[i] = QK::pack(kv[2 * i] * P[2 * i], kv[2 * i + 1] * P[2 * i + 1]);
       put16(&sm.kdec[0][0], w);
-      sm.gamma[mk] = P[15];
+      sm.gamma[ch] = P[15];
 #pragma unroll
       for (int lv = 0; lv < 4; ++lv) {
         const int s = 8 >> lv;
@@ -317,16 +350,26 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
     if (warp < 4) {  // level `warp` of the anchored split: L (rows 0-7) and Mqk (rows 8-15)
       const int lv = warp;
       const int s = 8 >> lv;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      // two accumulator chains, operands loaded one step ahead (mma.sync and
+      // ldmatrix keep their program order). A and B are stored [channel][row]:
+      // .trans loads; lane matrix m of A = (row half m & 1, channel half m >> 1)
+      float acc2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+      const int a_row = (lane >> 4) * 8 + (lane & 7), a_half = (lane >> 3) & 1;
+      uint32_t a[2][4], bq[2][2];
+      ldsm_x4_trans(a[0], &lvo.A[lv][0][0] + rt_cm_off(a_row, a_half));
+      ldsm_x2_trans(bq[0], &lvo.B[lv][lane & 15][0]);
 #pragma unroll
       for (int kk = 0; kk < KK; ++kk) {
-        uint32_t a[4], bq[2];
-        // A and B are stored [channel][row]: .trans loads; lane matrix m of A =
-        // (row half m & 1, channel half m >> 1)
-        ldsm_x4_trans(a, &lvo.A[lv][0][0] + rt_cm_off(16 * kk + (lane >> 4) * 8 + (lane & 7), (lane >> 3) & 1));
-        ldsm_x2_trans(bq, &lvo.B[lv][16 * kk + (lane & 15)][0]);
-        mma16816<QK>(acc, a, bq[0], bq[1]);
+        const int cur = kk & 1;
+        if (kk + 1 < KK) {
+          ldsm_x4_trans(a[cur ^ 1], &lvo.A[lv][0][0] + rt_cm_off(16 * (kk + 1) + a_row, a_half));
+          ldsm_x2_trans(bq[cur ^ 1], &lvo.B[lv][16 * (kk + 1) + (lane & 15)][0]);
+        }
+        mma16816<QK>(acc2[cur], a[cur], bq[cur][0], bq[cur][1]);
       }
+      float acc[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[e] = acc2[0][e] + acc2[1][e];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int r = g + ((e & 2) ? 8 : 0);
@@ -416,25 +459,38 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
         for (int e = 0; e < 4; ++e) { u2[nt][e] = 0.f; o[nt][e] = 0.f; }
       }
       // U^T = U~^T + S^T (-W)^T ; O^T = S^T q_dec^T (S^T as bf16 A fragments, one
-      // k-step at a time: the accumulator layout of two n-tiles is the A layout)
+      // k-step at a time: the accumulator layout of two n-tiles is the A layout).
+      // mma.sync and ldmatrix keep their program order, so each k-step's operands
+      // are loaded one step ahead of their MMAs.
+      const int w_row = ((lane >> 4) << 3) + (lane & 7), w_col = ((lane >> 3) & 1) * 8;
+      const int q_row = ((lane >> 3) & 1) * 8 + (lane & 7), q_half = lane >> 4;
+      uint32_t bw[2][4], bqd[2][4];
+      ldsm_x4(bw[0], &st.W[w_row][w_col]);
+      ldsm_x4_trans(bqd[0], &sm.qd[0][0] + rt_cm_off(q_row, q_half));
 #pragma unroll
       for (int kk = 0; kk < KK; ++kk) {
+        const int cur = kk & 1;
+        if (kk + 1 < KK) {
+          ldsm_x4(bw[cur ^ 1], &st.W[w_row][16 * (kk + 1) + w_col]);
+          ldsm_x4_trans(bqd[cur ^ 1], &sm.qd[0][0] + rt_cm_off(16 * (kk + 1) + q_row, q_half));
+        }
         uint32_t sa[4];
         sa[0] = Bf16::pack(S[2 * kk][0], S[2 * kk][1]);
         sa[1] = Bf16::pack(S[2 * kk][2], S[2 * kk][3]);
         sa[2] = Bf16::pack(S[2 * kk + 1][0], S[2 * kk + 1][1]);
         sa[3] = Bf16::pack(S[2 * kk + 1][2], S[2 * kk + 1][3]);
-        const int row = ((lane >> 4) << 3) + (lane & 7);
-        const int col = 16 * kk + ((lane >> 3) & 1) * 8;
-        uint32_t bm[4];
-        ldsm_x4(bm, &st.W[row][col]);
-        float (&acc)[2][4] = (kk & 1) ? u2 : u;
-        mma16816<Bf16>(acc[0], sa, bm[0], bm[1]);
-        mma16816<Bf16>(acc[1], sa, bm[2], bm[3]);
-        ldsm_x4_trans(bm, &sm.qd[0][0] + rt_cm_off(16 * kk + ((lane >> 3) & 1) * 8 + (lane & 7), lane >> 4));
-        mma16816<Bf16>(o[0], sa, bm[0], bm[1]);
-        mma16816<Bf16>(o[1], sa, bm[2], bm[3]);
+        float (&acc)[2][4] = cur ? u2 : u;
+        mma16816<Bf16>(acc[0], sa, bw[cur][0], bw[cur][1]);
+        mma16816<Bf16>(acc[1], sa, bw[cur][2], bw[cur][3]);
+        mma16816<Bf16>(o[0], sa, bqd[cur][0], bqd[cur][1]);
+        mma16816<Bf16>(o[1], sa, bqd[cur][2], bqd[cur][3]);
       }
+      // the first k-step's operands of the state update
+      const int k_row = (lane >> 4) * 8 + (lane & 7), k_half = (lane >> 3) & 1;
+      uint32_t bk[2][4];
+      float4 gq[2];
+      ldsm_x4(bk[0], &sm.kr[0][0] + rt_cm_off(k_row, k_half));
+      gq[0] = *reinterpret_cast<const float4*>(&sm.gamma[4 * t]);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -444,18 +500,20 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
       ua[1] = F16::pack(u[0][2], u[0][3]);
       ua[2] = F16::pack(u[1][0], u[1][1]);
       ua[3] = F16::pack(u[1][2], u[1][3]);
-      // S^T = S^T diag(gamma) + U^T k_res
+      // S^T = S^T diag(gamma) + U^T k_res, operands one step ahead; gamma is indexed
+      // by stored key: entries 0-1 are MMA keys 16 np + 2 t (+1), 2-3 are + 8
 #pragma unroll
       for (int np = 0; np < KK; ++np) {
-        uint32_t bm[4];
-        ldsm_x4(bm, &sm.kr[0][0] + rt_cm_off(16 * np + (lane >> 4) * 8 + (lane & 7), (lane >> 3) & 1));
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const int nt = 2 * np + half;
-          const float2 gm = *reinterpret_cast<const float2*>(&sm.gamma[8 * nt + 2 * t]);
-          S[nt][0] *= gm.x; S[nt][1] *= gm.y; S[nt][2] *= gm.x; S[nt][3] *= gm.y;
-          mma16816<F16>(S[nt], ua, bm[2 * half], bm[2 * half + 1]);
+        const int cur = np & 1;
+        if (np + 1 < KK) {
+          ldsm_x4(bk[cur ^ 1], &sm.kr[0][0] + rt_cm_off(16 * (np + 1) + k_row, k_half));
+          gq[cur ^ 1] = *reinterpret_cast<const float4*>(&sm.gamma[16 * (np + 1) + 4 * t]);
         }
+        const float4 gm = gq[cur];
+        S[2 * np][0] *= gm.x; S[2 * np][1] *= gm.y; S[2 * np][2] *= gm.x; S[2 * np][3] *= gm.y;
+        mma16816<F16>(S[2 * np], ua, bk[cur][0], bk[cur][1]);
+        S[2 * np + 1][0] *= gm.z; S[2 * np + 1][1] *= gm.w; S[2 * np + 1][2] *= gm.z; S[2 * np + 1][3] *= gm.w;
+        mma16816<F16>(S[2 * np + 1], ua, bk[cur][2], bk[cur][3]);
       }
       // O^T += U^T Mqk^T
       {

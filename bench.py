@@ -90,6 +90,11 @@ CHUNK_LAUNCHES_PER_STEP = 1   # kda_chunk_fused_kernel (bf16, d = 128, no cu_seq
 DECODE_LAUNCHES_PER_STEP = 1  # kda_decode_kernel
 
 
+# GB300's nominal HBM3e bandwidth (8 stacks, 7.9 TB/s): a second denominator for the
+# roofline fractions, beside the measured copy bandwidth they are quoted against.
+SPEC_HBM_GBS = 7900.0
+
+
 def load_peaks():
     p = ROOT / "MEASURED_PEAKS.json"
     if p.exists():
@@ -808,9 +813,11 @@ def run_gpu(args):
                        "wall_us_per_step_with_launch": None if dec_wall is None else 1e6 * dec_wall,
                        "graph_replay_us_per_step": None if dec_graph is None else 1e6 * dec_graph,
                        "roofline": {"bound": "hbm", "achieved": dach, "peak": hbm, "unit": "GB/s",
-                                    "frac": dach / hbm, "algorithmic_bytes": dbytes,
+                                    "frac": dach / hbm, "frac_of_spec_peak": dach / SPEC_HBM_GBS,
+                                    "spec_peak": SPEC_HBM_GBS, "algorithmic_bytes": dbytes,
                                     "traffic": stored_traffic("kda_decode_kernel", dec_sha, n_valid), "peak_kind": peak_kind}},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "frac_of_spec_peak": achieved / SPEC_HBM_GBS, "spec_peak": SPEC_HBM_GBS,
                          "traffic": stored_traffic("kda_chunk_fused_kernel", chunk_sha, T), "kernel": "kda_chunk_fused_kernel (prep + recurrence in one launch)",
                          "algorithmic_bytes": abytes, "peak_kind": peak_kind},
             "e2e": {"value": T * world / e2e_s if e2e_steps else None, "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -823,6 +830,7 @@ def run_gpu(args):
         }
         if var is not None:
             var["frac_of_roofline"] = var["achieved_gbs"] / hbm
+            var["frac_of_spec_peak"] = var["achieved_gbs"] / SPEC_HBM_GBS
         if gate_g is not None:
             gate_g["frac_of_roofline"] = gate_g["achieved_gbs"] / hbm
         if rms is not None:

@@ -367,10 +367,13 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     auto prefetch_state = [&](int cc) {
       if (wi == 0 && lane == 0 && cc < nch) bulk_prefetch_l2(snapshot(cc) + rank * kRows * FD, kRows * FD * 4);
     };
-    // the warp's 16 rows of chunk cc's entering state into its snapshot buffer
+    // the warp's 16 rows of chunk cc's entering state into its snapshot buffer;
+    // after a failed wait no new copy is started (decided for the whole warp)
+    int snap_issued[2] = {-1, -1}, snap_seen[2] = {-1, -1};
     auto load_snap = [&](int cc) {
       if constexpr (outp) {
-        if (cc < nch) {
+        if (cc < nch && !__any_sync(0xffffffffu, failed)) {
+          snap_issued[cc & 1] = cc;
           uint64_t* bar = &sm.snap.bar[wi][cc & 1];
           if (lane == 0) mbar_arrive_expect_tx_local(bar, 16 * FD * 4);
           __syncwarp();
@@ -400,6 +403,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           failed = true;
           if (lane == 0) set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
         }
+        if (!failed) snap_seen[c & 1] = c;
       }
       const Stage& st = sm.ring[s];
       // U^T = U~^T + S^T (-W)^T (the serial path, two accumulator chains per
@@ -509,6 +513,15 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       if (lane == 0) mbar_arrive_local(&sm.empty[s]);
     }
     if (ok && p.hT != nullptr && !outp) store_state(p.hT + (static_cast<size_t>(n) * H + h) * FD * FD, false);
+    if constexpr (outp) {  // no snapshot copy may still be landing when the CTA exits
+#pragma unroll
+      for (int b = 0; b < 2; ++b)
+        if (snap_issued[b] > snap_seen[b] &&
+            !mbar_wait_bounded(smem_u32(&sm.snap.bar[wi][b]), static_cast<uint32_t>(snap_issued[b] >> 1) & 1u,
+                               kWaitLimitNs) &&
+            lane == 0)
+          set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
+    }
   } else if ((warp & 3) >= 2) {
     // ===================== prep warps =====================
     // Chunk c is prepared in shared memory (pout), then copied into global slot
@@ -599,7 +612,14 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       if (!failed && !mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pinbar[buf])),
                                         static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs)) {
         failed = true;
-        if (pt == 0) set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
+        if (pt == 0) {
+          set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
+          // the copy waited for is the only one that can be in flight (none is
+          // started after a failed wait): it gets one more bounded wait, so no
+          // input copy lands once the CTA has exited
+          mbar_wait_bounded(static_cast<uint32_t>(__cvta_generic_to_shared(&sm.pinbar[buf])),
+                            static_cast<uint32_t>(j >> 1) & 1u, kWaitLimitNs);
+        }
       }
       // the chunk is written straight into global slot c mod kGRing, once all
       // four CTAs have loaded that slot's previous chunk
@@ -764,7 +784,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       }
       fence_proxy_async_smem();  // the reads of pin[buf] precede the next TMA write into it
       prep_bar();  // (D) tiles, level operands and norm partial sums written
-      if (pt == 0 && c + 2 * kCtas < nch)
+      if (pt == 0 && !failed && c + 2 * kCtas < nch)  // (no new copy after a failed wait)
         issue_inputs(maps, sm.pin[buf], &sm.pinbar[buf], h, ts + (c + 2 * kCtas) * kChunk, p.gate_mode);
       // the norm factors of the 16 tokens (the partial sums are complete): lane
       // i < 16 of every warp holds token i's
@@ -929,6 +949,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
     // released stage also returns its chunk's global slot to the producer.
     if (lane == 0) {
       bool failed = false;
+      int last_issued = -1;
       for (int c = 0; c < nch; ++c) {
         const int s = c & (kRing - 1);
         const int gs = c % kGRing;
@@ -946,20 +967,21 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           failed = true;
           set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
         }
+        if (failed) continue;  // after a failed wait no new copy is started
         fence_proxy_async_global();  // the bulk loads below read what the acquire made visible
         const unsigned char* slot = gring + static_cast<size_t>(gs) * kSlotBytes;
         unsigned char* stage = reinterpret_cast<unsigned char*>(&sm.ring[s]);
         mbar_arrive_expect_tx_local(&sm.full[s], kStageTx);
         bulk_load_g2s(stage, slot, kSharedBytes, &sm.full[s]);
         bulk_load_g2s(stage + kSharedBytes, slot + kSharedBytes + rank * kUtSliceBytes, kUtSliceBytes, &sm.full[s]);
+        last_issued = c;
       }
-      // no load may still be landing in this CTA's shared memory when it exits
-      for (int c = max(0, nch - kRing); c < nch; ++c)
-        if (!failed && !mbar_wait_bounded(smem_u32(&sm.full[c & (kRing - 1)]), static_cast<uint32_t>(c / kRing) & 1u,
-                                          kWaitLimitNs)) {
-          failed = true;
+      // no load may still be landing in this CTA's shared memory when it exits:
+      // the last stages' copies are waited for (bounded) even after a failure
+      for (int c = max(0, last_issued - kRing + 1); c <= last_issued; ++c)
+        if (!mbar_wait_bounded(smem_u32(&sm.full[c & (kRing - 1)]), static_cast<uint32_t>(c / kRing) & 1u,
+                               kWaitLimitNs))
           set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
-        }
     }
     __syncwarp();
   } else if (warp == kPublisherWarp) {

@@ -179,8 +179,11 @@ struct __align__(128) FusedSmem {
   SnapStage<MODE == 2> snap;
 };
 
-__device__ __forceinline__ int row_tok_f(int s, int r) { return (r / s) * 2 * s + s + (r % s); }
-__device__ __forceinline__ int col_tok_f(int s, int r) { return (r / s) * 2 * s + (r % s); }
+// Token of row r (column r) of a level's 8-row block, the level's half-block size
+// being s = 2^ls (shifts: the level is a warp index, so a division would be a
+// run-time one).
+__device__ __forceinline__ int row_tok_f(int ls, int r) { return ((r >> ls) << (ls + 1)) + (1 << ls) + (r & ((1 << ls) - 1)); }
+__device__ __forceinline__ int col_tok_f(int ls, int r) { return ((r >> ls) << (ls + 1)) + (r & ((1 << ls) - 1)); }
 
 // One thread issues the TMA loads of one chunk's input tiles (16 tokens x 128
 // channels of q, k, v and, with a gate, a or g) into a PrepIn buffer; the bytes
@@ -803,7 +806,7 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       {  // level pw of the anchored split: raw L (rows 0-7, times beta) and Mqk (rows 8-15),
          // two accumulator chains, operands loaded one step ahead
         const int lv = pw;
-        const int s = 8 >> lv;
+        const int ls = 3 - lv;  // half-block size 2^ls = 8 >> lv
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         // A^T and B^T are stored [channel][row]: .trans loads; lane matrix m of
         // A = (row half m & 1, channel half m >> 1)
@@ -826,8 +829,8 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           const int r = g + ((e & 2) ? 8 : 0);
           const int cidx = 2 * t + (e & 1);
           const int rr = r & 7;
-          if (rr / s != cidx / s) continue;
-          const int i = row_tok_f(s, rr), jx = col_tok_f(s, cidx);
+          if ((rr >> ls) != (cidx >> ls)) continue;
+          const int i = row_tok_f(ls, rr), jx = col_tok_f(ls, cidx);
           const float v = acc[0][e] + acc[1][e];
           if (r < 8) {
             if (DELTA) ps.Lm[i][jx] = ps.beta[jb][i] * v;

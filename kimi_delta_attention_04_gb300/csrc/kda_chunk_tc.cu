@@ -79,8 +79,11 @@ struct PrepSmem {
 };
 
 // Row / column token of slot r at a level with half-block size s.
-__device__ __forceinline__ int row_tok(int s, int r) { return (r / s) * 2 * s + s + (r % s); }
-__device__ __forceinline__ int col_tok(int s, int r) { return (r / s) * 2 * s + (r % s); }
+// Token of row r (column r) of a level's 8-row block, the level's half-block size
+// being s = 2^ls (shifts: the level is a warp index, so a division would be a
+// run-time one).
+__device__ __forceinline__ int row_tok(int ls, int r) { return ((r >> ls) << (ls + 1)) + (1 << ls) + (r & ((1 << ls) - 1)); }
+__device__ __forceinline__ int col_tok(int ls, int r) { return ((r >> ls) << (ls + 1)) + (r & ((1 << ls) - 1)); }
 
 // C = (A [+ I]) (B [+ I]) for 16x16 fp32 matrices in shared memory (row stride
 // 17), one warp, operands rounded to Op; C must not alias A or B.
@@ -306,7 +309,7 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_tc_kernel(const ChunkCa
   // ---- L and Mqk: warp lv multiplies the operands of level lv ----
   {
     const int lv = warp;
-    const int s = 8 >> lv;
+    const int ls = 3 - lv;  // half-block size 2^ls = 8 >> lv
     // Without the delta rule rows 0-7 (k rows) are never written and their
     // results are discarded; MMA rows are independent, so they cannot leak.
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -323,8 +326,8 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_tc_kernel(const ChunkCa
       const int r = g + ((e & 2) ? 8 : 0);
       const int cidx = 2 * t + (e & 1);
       const int rr = r & 7;
-      if (rr / s != cidx / s) continue;  // not a pair of this level
-      const int i = row_tok(s, rr), j = col_tok(s, cidx);
+      if ((rr >> ls) != (cidx >> ls)) continue;  // not a pair of this level
+      const int i = row_tok(ls, rr), j = col_tok(ls, cidx);
       if (r < 8) {
         if (DELTA) sm.Lm[i][j] = sm.beta[i] * acc[e];
       } else {

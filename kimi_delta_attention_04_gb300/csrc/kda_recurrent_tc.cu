@@ -97,8 +97,11 @@ __device__ __forceinline__ int rt_mma_key(int key) {
   return (key & ~15) + ((r >> 1) & 1) * 8 + (r >> 2) * 2 + (r & 1);
 }
 
-__device__ __forceinline__ int rt_row_tok(int s, int r) { return (r / s) * 2 * s + s + (r % s); }
-__device__ __forceinline__ int rt_col_tok(int s, int r) { return (r / s) * 2 * s + (r % s); }
+// Token of row r (column r) of a level's 8-row block, the level's half-block size
+// being s = 2^ls (shifts: the level is a warp index, so a division would be a
+// run-time one).
+__device__ __forceinline__ int rt_row_tok(int ls, int r) { return ((r >> ls) << (ls + 1)) + (1 << ls) + (r & ((1 << ls) - 1)); }
+__device__ __forceinline__ int rt_col_tok(int ls, int r) { return ((r >> ls) << (ls + 1)) + (r & ((1 << ls) - 1)); }
 
 template <int K, int V, bool L2N>
 __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const RecurrentCall p) {
@@ -349,7 +352,7 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
     __syncthreads();
     if (warp < 4) {  // level `warp` of the anchored split: L (rows 0-7) and Mqk (rows 8-15)
       const int lv = warp;
-      const int s = 8 >> lv;
+      const int ls = 3 - lv;  // half-block size 2^ls = 8 >> lv
       // two accumulator chains, operands loaded one step ahead (mma.sync and
       // ldmatrix keep their program order). A and B are stored [channel][row]:
       // .trans loads; lane matrix m of A = (row half m & 1, channel half m >> 1)
@@ -375,8 +378,8 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
         const int r = g + ((e & 2) ? 8 : 0);
         const int cidx = 2 * t + (e & 1);
         const int rr = r & 7;
-        if (rr / s != cidx / s) continue;  // not a pair of this level
-        const int i = rt_row_tok(s, rr), j = rt_col_tok(s, cidx);
+        if ((rr >> ls) != (cidx >> ls)) continue;  // not a pair of this level
+        const int i = rt_row_tok(ls, rr), j = rt_col_tok(ls, cidx);
         if (r < 8) sm.Lm[i][j] = sm.beta[i] * acc[e];
         else sm.Mq[i][j] = p.scale * acc[e];
       }

@@ -454,7 +454,10 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
           }
         }
         if (DELTA) {
-          float (&acc)[2][4] = cur ? u2 : u;
+          // The plain forward keeps one accumulator chain: under the 128-register
+          // cap its body then runs faster than with two (measured); the snapshot
+          // modes, which hold more registers, keep two.
+          float (&acc)[2][4] = (cur && MODE != 0) ? u2 : u;
           mma16816<Bf16>(acc[0], sa, wv[cur].x, wv[cur].y);
           mma16816<Bf16>(acc[1], sa, wv[cur].z, wv[cur].w);
         }
@@ -512,8 +515,16 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         mma16816<ST2>(o[0], ua, bm[0], bm[1]);
         mma16816<ST2>(o[1], ua, bm[2], bm[3]);
       }
-      post_output(c);
-      if (lane == 0) mbar_arrive_local(&sm.empty[s]);
+      if constexpr (MODE == 0) {
+        // the stage is read: released before the O stores, which go to another
+        // buffer (measured faster in the forward; the snapshot modes spill with it)
+        __syncwarp();
+        if (lane == 0) mbar_arrive_local(&sm.empty[s]);
+        post_output(c);
+      } else {
+        post_output(c);
+        if (lane == 0) mbar_arrive_local(&sm.empty[s]);
+      }
     }
     if (ok && p.hT != nullptr && !outp) store_state(p.hT + (static_cast<size_t>(n) * H + h) * FD * FD, false);
     if constexpr (outp) {  // no snapshot copy may still be landing when the CTA exits

@@ -390,13 +390,20 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
       for (int cc = pair + 2; cc < pair + 2 + kSnapAhead; cc += 2) prefetch_state(cc);
       load_snap(pair);
     }
+    // set mid-chunk when every lane's non-blocking test saw the next chunk's stage
+    // loaded: its blocking wait (whose latency sits on the serial path) is skipped.
+    // Not in the snapshot forward, which spills with it.
+    constexpr bool kPretest = MODE != 1;
+    bool next_ready = false;
     for (int c = pair; c < nch; c += kStep) {
       const int s = c & (kRing - 1);
       const uint32_t par = static_cast<uint32_t>(c / kRing) & 1u;
+      const bool stage_ready = next_ready;
+      next_ready = false;
       // the state entering chunk c (before its decay) goes to h_chunks one key
       // pair per step of the U loop below, where the MMAs leave issue slots free
       float* const snap_row = MODE == 1 ? snapshot(c) + static_cast<size_t>(dv0 + g) * FD + 4 * t : nullptr;
-      if (!failed && !mbar_wait_bounded(smem_u32(&sm.full[s]), par, kWaitLimitNs)) {
+      if (!failed && !stage_ready && !mbar_wait_bounded(smem_u32(&sm.full[s]), par, kWaitLimitNs)) {
         failed = true;
         if (lane == 0) set_err(p.err, 4 /* KDA_ERR_TIMEOUT */);
       }
@@ -463,6 +470,12 @@ __global__ void __cluster_dims__(kCtas, 1, 1) __launch_bounds__(kFusedThreads, 1
         }
         mma16816<Bf16>(o[0], sa, bq[cur][0], bq[cur][1]);
         mma16816<Bf16>(o[1], sa, bq[cur][2], bq[cur][3]);
+      }
+      if constexpr (kPretest) {  // the next chunk's stage, tested without blocking
+        const int cn = c + kStep;
+        const bool t_ok = cn < nch && mbar_test_wait(smem_u32(&sm.full[cn & (kRing - 1)]),
+                                                     static_cast<uint32_t>(cn / kRing) & 1u);
+        next_ready = __all_sync(0xffffffffu, t_ok);
       }
       // the operands of Mqk^T and of the first key step of the state update
       uint32_t bm[4], bk[2][4];

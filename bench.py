@@ -83,7 +83,7 @@ def decode_algorithmic_bytes(n_valid, H=32, HV=32, K=128, V=128, B=256):
 # figure is only reported while these files are unchanged).
 CHUNK_KERNEL_SOURCES = ["kda_chunk_fused.cu", "kda_common.cuh", "kda_cluster.cuh", "kda_tma.h", "kda_tma.cpp"]
 DECODE_KERNEL_SOURCES = ["kda_decode.cu", "kda_common.cuh"]
-RECURRENT_KERNEL_SOURCES = ["kda_recurrent_tc.cu", "kda_common.cuh", "kda_cluster.cuh"]
+RECURRENT_KERNEL_SOURCES = ["kda_recurrent_tc.cu", "kda_common.cuh", "kda_cluster.cuh", "kda_tcgen05.cuh"]
 RECURRENT_B, RECURRENT_T, RECURRENT_SLOTS = 128, 8, 256  # speculative-style step: 128 rows x 8 tokens
 RECURRENT_LONG_B, RECURRENT_LONG_T = 64, 64              # the longest T the entry point takes
 CHUNK_LAUNCHES_PER_STEP = 1   # kda_chunk_fused_kernel (bf16, d = 128, no cu_seqlens)
@@ -847,6 +847,13 @@ def run_gpu(args):
                 r["roofline"]["peak_kind"] = peak_kind
         if args.only != "all" or T != PREFILL_T:
             line["config"]["partial"] = f"only={args.only}, seq_len={T}: a profiling run, not the benchmark line"
+        # a leg that did not run reports nothing (its events bracket an empty region)
+        if args.only not in ("all", "chunk"):
+            line["value"] = None
+            line["chunk_fwd"] = None
+            line["roofline"] = None
+        if args.only not in ("all", "decode"):
+            line["decode"] = None
         if world == 1 and not args.no_cpu_baseline:
             v, sample, cores = oracle_parallel_baseline(budget_s=args.cpu_budget)
             line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}

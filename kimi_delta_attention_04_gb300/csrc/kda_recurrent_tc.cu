@@ -20,10 +20,15 @@
 //    forming the inverse in registers for its columns of W and U~);
 //  * each warp owns V / 4 value rows of the state and steps them 16 at a
 //    time, S^T [16 x K] fp32 in registers as MMA accumulators, loaded after
-//    the chunk's preparation and stored back after its step (between chunks
-//    of a long T the rows make an L2 round trip rather than stay live across
-//    the next preparation): U^T = U~^T - S^T W^T, O^T = S^T q_dec^T + U^T
-//    Mqk^T, S^T = S^T diag(gamma) + U^T k_res;
+//    the chunk's preparation and stored back after its step: U^T = U~^T -
+//    S^T W^T, O^T = S^T q_dec^T + U^T Mqk^T, S^T = S^T diag(gamma) + U^T k_res.
+//    The slot is read before the first chunk and written after the last; in
+//    between, with d_k = 128, a row of more than 16 tokens keeps its state tiles
+//    in tensor memory (tcgen05.st / tcgen05.ld: each warp its own lane quarter,
+//    MT * 64 columns per CTA, so four CTAs fill at most an SM's 512 columns)
+//    instead of an L2 round trip per chunk, which at 64 tokens per row made ~40 %
+//    of the L1 data-pipe wavefronts (16-byte state accesses, each warp access
+//    touching eight half-used lines);
 //  * o is staged in shared memory and written as 16-byte rows.
 // Operand precision as in the chunk forward: S, W, q_dec bf16; U, k_res, Mqk
 // fp16; L/Mqk/INV operands fp16 (q, k normalised) or bf16; U~ fp32.
@@ -31,6 +36,7 @@
 
 #include "kda_cluster.cuh"
 #include "kda_common.cuh"
+#include "kda_tcgen05.cuh"
 
 namespace kda {
 namespace {
@@ -73,6 +79,7 @@ struct RtcSmem {
   float Mq[16][17];
   float red[K / 32][48];
   float rnq[16], rnk[16], beta[16];
+  uint32_t tmem_base;  // tensor-memory columns holding the state between chunks (rows of > 16 tokens)
   __device__ __forceinline__ In& in() { return *reinterpret_cast<In*>(region); }
   __device__ __forceinline__ Lv& lv() { return *reinterpret_cast<Lv*>(region); }
   __device__ __forceinline__ St& st() { return *reinterpret_cast<St*>(region); }
@@ -103,7 +110,13 @@ __device__ __forceinline__ int rt_mma_key(int key) {
 __device__ __forceinline__ int rt_row_tok(int ls, int r) { return ((r >> ls) << (ls + 1)) + (1 << ls) + (r & ((1 << ls) - 1)); }
 __device__ __forceinline__ int rt_col_tok(int ls, int r) { return ((r >> ls) << (ls + 1)) + (r & ((1 << ls) - 1)); }
 
-template <int K, int V, bool L2N>
+// RES: the state stays in tensor memory between chunks (d_k = 128, T > 16). Rows of
+// one chunk launch the instance without it, which holds no tcgen05 instruction: a CTA
+// of a kernel that allocates tensor memory keeps the SM's allocation permit until it
+// relinquishes it or exits, and at 8 tokens per row the allocating instance ran at
+// half speed even where it allocated nothing (185 vs 98 us at 128 rows; relinquishing
+// at the start of every CTA took it back to 101 us).
+template <int K, int V, bool L2N, bool RES>
 __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const RecurrentCall p) {
   using QK = std::conditional_t<L2N, F16, Bf16>;
   using Q = typename QK::T;
@@ -157,6 +170,30 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
   const float dtb = kown ? p.dt_bias[hv * K + ch] : 0.f;
 
   const int nch = (T + 15) / 16;
+  // Tensor memory for the state between chunks (d_k = 128 only: at d_k = 64 the
+  // round trip is half as large and that instance has no registers to spare for
+  // it). Occupancy is at most four CTAs per SM (registers), so the columns are
+  // there (a fifth CTA would only wait in the allocation until another one exits);
+  // every CTA that allocates reaches the release after the chunk loop (no return
+  // in between).
+  static_assert(!RES || K == 128, "tensor-memory state at d_k = 128 only");
+  constexpr bool kTmemState = RES;
+  constexpr int kTileCols = NT * 4;  // one 16-row tile: 64 fp32 accumulators per lane
+  constexpr uint32_t kTmemCols = MT * kTileCols;
+  static_assert(!kTmemState || (kTmemCols >= 32 && kTmemCols <= 128 && (kTmemCols & (kTmemCols - 1)) == 0),
+                "a power of two of at most 512 / 4 columns");
+  const bool resident = kTmemState && nch > 1;  // (the launcher takes RES only for T > 16)
+  uint32_t tbase = 0;
+  if (resident) {
+    if (warp == 0) {
+      tc05::tmem_alloc(&sm.tmem_base, kTmemCols);
+      tc05::tmem_relinquish();
+    }
+    tc05::fence_before_sync();
+    __syncthreads();
+    tc05::fence_after_sync();
+    tbase = sm.tmem_base + (static_cast<uint32_t>(32 * warp) << 16);  // this warp's lane quarter
+  }
   for (int c = 0; c < nch; ++c) {
     const int tok0 = 16 * c;
     const int ntok = min(16, T - tok0);
@@ -441,8 +478,13 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
     for (int mt = 0; mt < MT; ++mt) {
       const int r0 = (warp + WARPS * mt) * 16;  // first value row of the tile
       float S[NT][4];
-      {  // the state, in the accumulator layout (its lines are in L2 by now): stored keys
-         // 16 pp + 4 t .. + 3 are MMA keys 16 pp + 2 t (+1) and 16 pp + 8 + 2 t (+1)
+      const uint32_t taddr = tbase + static_cast<uint32_t>(mt * kTileCols);
+      // (S as one array of kTileCols floats: column 4 j + e of the tile holds S[j][e])
+      float (&s_cols)[kTileCols] = *reinterpret_cast<float(*)[kTileCols]>(&S[0][0]);
+      if (kTmemState && c > 0) {  // the tile as this warp left it after the previous chunk
+        if constexpr (kTmemState) tc05::ld64_wait(taddr, s_cols);
+      } else {  // from the slot, in the accumulator layout (its lines are in L2 by now): stored
+                // keys 16 pp + 4 t .. + 3 are MMA keys 16 pp + 2 t (+1) and 16 pp + 8 + 2 t (+1)
 #pragma unroll
         for (int pp = 0; pp < NT / 2; ++pp) {
           const float4 x = __ldcs(reinterpret_cast<const float4*>(S_slot + (r0 + g) * K + 16 * pp + 4 * t));
@@ -534,21 +576,25 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
         st.ostage[tok][r0 + g + 8] = __float2bfloat16_rn(o[nt][2]);
         st.ostage[tok + 1][r0 + g + 8] = __float2bfloat16_rn(o[nt][3]);
       }
-      // The tile goes back to its slot after every chunk (each warp rereads only
-      // its own rows, after the next chunk's preparation): between chunks it is
-      // an L2 round trip instead of registers held across the preparation.
+      // Between chunks the tile waits in tensor memory (each warp rereads only its
+      // own tiles, after the next chunk's preparation) rather than in registers held
+      // across the preparation; after the last chunk it goes back to its slot.
+      if (kTmemState && c + 1 < nch) {
+        if constexpr (kTmemState) tc05::st64_wait(taddr, s_cols);
+      } else {  // (at d_k = 64 also between chunks: an L2 round trip)
 #pragma unroll
-      for (int pp = 0; pp < NT / 2; ++pp) {
-        float4* d0 = reinterpret_cast<float4*>(S_slot + (r0 + g) * K + 16 * pp + 4 * t);
-        float4* d1 = reinterpret_cast<float4*>(S_slot + (r0 + g + 8) * K + 16 * pp + 4 * t);
-        const float4 x = make_float4(S[2 * pp][0], S[2 * pp][1], S[2 * pp + 1][0], S[2 * pp + 1][1]);
-        const float4 y = make_float4(S[2 * pp][2], S[2 * pp][3], S[2 * pp + 1][2], S[2 * pp + 1][3]);
-        if (c + 1 < nch) {
-          __stcg(d0, x);
-          __stcg(d1, y);
-        } else {
-          __stcs(d0, x);
-          __stcs(d1, y);
+        for (int pp = 0; pp < NT / 2; ++pp) {
+          float4* d0 = reinterpret_cast<float4*>(S_slot + (r0 + g) * K + 16 * pp + 4 * t);
+          float4* d1 = reinterpret_cast<float4*>(S_slot + (r0 + g + 8) * K + 16 * pp + 4 * t);
+          const float4 x = make_float4(S[2 * pp][0], S[2 * pp][1], S[2 * pp + 1][0], S[2 * pp + 1][1]);
+          const float4 y = make_float4(S[2 * pp][2], S[2 * pp][3], S[2 * pp + 1][2], S[2 * pp + 1][3]);
+          if (c + 1 < nch) {
+            __stcg(d0, x);
+            __stcg(d1, y);
+          } else {
+            __stcs(d0, x);
+            __stcs(d1, y);
+          }
         }
       }
     }
@@ -561,25 +607,41 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
     }
     __syncthreads();  // the next chunk's preparation reuses every buffer above
   }
+  if (resident) {  // every warp's tensor-memory accesses were waited for before this point
+    tc05::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) {
+      tc05::fence_after_sync();
+      tc05::tmem_dealloc(sm.tmem_base, kTmemCols);
+    }
+  }
 }
 
-template <int K, int V, bool L2N>
+template <int K, int V, bool L2N, bool RES>
 cudaError_t launch_rtc_t(const RecurrentCall& c, cudaStream_t s) {
   using Q = typename std::conditional_t<L2N, F16, Bf16>::T;
   constexpr size_t smem = sizeof(RtcSmem<K, V, Q>);
   static std::atomic<uint64_t> smem_set{0};
   {
-    const cudaError_t e = set_smem_limit_once(kda_recurrent_tc_kernel<K, V, L2N>, smem, smem_set);
+    const cudaError_t e = set_smem_limit_once(kda_recurrent_tc_kernel<K, V, L2N, RES>, smem, smem_set);
     if (e != cudaSuccess) return e;
   }
   const unsigned grid = static_cast<unsigned>(c.B) * static_cast<unsigned>(c.HV);
-  kda_recurrent_tc_kernel<K, V, L2N><<<grid, 128, smem, s>>>(c);
+  kda_recurrent_tc_kernel<K, V, L2N, RES><<<grid, 128, smem, s>>>(c);
   return cudaGetLastError();
+}
+
+template <int K, int V, bool RES>
+cudaError_t launch_rtc_kvr(const RecurrentCall& c, cudaStream_t s) {
+  return c.l2norm ? launch_rtc_t<K, V, true, RES>(c, s) : launch_rtc_t<K, V, false, RES>(c, s);
 }
 
 template <int K, int V>
 cudaError_t launch_rtc_kv(const RecurrentCall& c, cudaStream_t s) {
-  return c.l2norm ? launch_rtc_t<K, V, true>(c, s) : launch_rtc_t<K, V, false>(c, s);
+  if constexpr (K == 128) {
+    if (c.T > 16) return launch_rtc_kvr<K, V, true>(c, s);
+  }
+  return launch_rtc_kvr<K, V, false>(c, s);
 }
 
 }  // namespace

@@ -88,6 +88,15 @@ def test_recurrent_full_size():
     _check(W.recurrent_workload())
 
 
+def test_recurrent_full_size_long():
+    """B=64 rows of T=64 tokens (four chunks each), H=HV=32, K=V=128, fp32 pool
+    [128, 32, 128, 128], 6 padded rows: the long recurrent step of the benchmark.
+    Each CTA keeps its state in tensor memory between chunks, and there are more
+    CTAs than fit on the GPU at once, so later ones allocate columns that earlier
+    ones released; every valid row is compared with the oracle."""
+    _check(W.recurrent_workload(seed=5, B=64, T=64, num_slots=128))
+
+
 def test_recurrent_t1_matches_decode_kernel():
     """One token per row through both entry points (decode reads a packed row)."""
     wl = W.recurrent_workload(seed=97, B=9, T=1, H=2, HV=4, K=128, V=128, num_slots=12, pad_frac=0.2)

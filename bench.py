@@ -716,10 +716,12 @@ def run_gpu(args):
         r_valid = int((rw["indices"] >= 0).sum())
         rbytes = recurrent_algorithmic_bytes(r_valid, rw["B"], rw["T"])
         kernel = "kda_recurrent_tc_kernel (chunk form, tensor cores)" if T_r >= 8 else "kda_recurrent_kernel (per token)"
-        # the stored DRAM traffic was captured at 128 rows x 8 tokens: it scales by the
-        # valid rows (the slots dominate), so it is quoted for that shape only
-        traffic = (stored_traffic("kda_recurrent_tc_kernel", kernel_sources_sha(RECURRENT_KERNEL_SOURCES), r_valid)
-                   if T_r == RECURRENT_T else None)
+        # the stored DRAM traffic was captured at 128 rows x 8 tokens and at 64 rows x 64
+        # tokens (the instance that keeps the state in tensor memory between chunks); at a
+        # given T it scales by the valid rows (the slots dominate)
+        rsha = kernel_sources_sha(RECURRENT_KERNEL_SOURCES)
+        traffic = (stored_traffic("kda_recurrent_tc_kernel", rsha, r_valid) if T_r == RECURRENT_T else
+                   stored_traffic("kda_recurrent_tc_kernel_T64", rsha, r_valid) if T_r == RECURRENT_LONG_T else None)
         return {"us_per_step": 1e6 * r_avg, "rows": rw["B"], "tokens_per_row": rw["T"], "n_valid_rows": r_valid,
                 "tokens_per_s": rw["B"] * rw["T"] / r_avg,
                 "roofline": {"bound": "hbm", "achieved": rbytes / r_avg / 1e9, "unit": "GB/s",

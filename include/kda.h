@@ -290,6 +290,11 @@ kda_status kda_decode_conv_step(const kda_decode_conv_args* args, kda_stream_t s
  * Supported: K, V in {64, 128}; 1 <= T <= KDA_RECURRENT_MAX_T (longer
  * sequences belong to kda_chunk_fwd). q, k, v, a, dt_bias, state_pool and o
  * must be 16-byte aligned.
+ * Resources: with K = 128 and T > 16 each CTA (one per row and value head)
+ * holds V columns of tensor memory while it runs, at most four CTAs per SM.
+ * A kernel on another stream that holds tensor memory on the same SMs at the
+ * same time only delays this one's CTAs (their allocation waits); nothing is
+ * left allocated when the call completes.
  */
 #define KDA_RECURRENT_MAX_T 64
 typedef struct kda_recurrent_args {

@@ -87,9 +87,22 @@ struct RtcSmem {
 
 // Channel-major 16-bit tiles [channel][16 tokens]: a channel's 16 tokens are one
 // 32-byte row, written by the thread that owns the channel with two 16-byte
-// stores; the two halves (tokens 0-7, 8-15) are swapped on rows whose bit 2 is
-// set, so the eight rows of one ldmatrix 8x8 load fall on distinct banks.
-__device__ __forceinline__ int rt_cm_off(int row, int half) { return row * 16 + ((half ^ (row >> 2)) & 1) * 8; }
+// stores; the two halves (tokens 0-7, 8-15) are swapped on rows whose bits 2 and 3
+// differ. The eight rows of one ldmatrix 8x8 load (bit 3 fixed) fall on distinct
+// banks, and so do the rows eight consecutive channels write, both in channel
+// order and in the MMAs' key order (rt_mma_key), where they are rows
+// {0, 1, 8, 9, 2, 3, 10, 11} (+ 4) of a 16-row block.
+__device__ __forceinline__ int rt_cm_off(int row, int half) {
+  return row * 16 + ((half ^ (row >> 2) ^ (row >> 3)) & 1) * 8;
+}
+
+// Column of U~^T [value row][token] in shared memory. With SWZ = 8 the token index is
+// XORed with 8 on rows whose bit 2 is set, so the scalar stores of one MMA fragment
+// (rows 2 t apart, columns g) are conflict-free as well as the float2 loads of the step
+// (rows g, columns 2 t). The d_k = 64 instances keep the plain layout (SWZ = 0): one of
+// them has no register to spare for the extra index arithmetic.
+template <int SWZ>
+__device__ __forceinline__ int rt_ut_col(int row, int tok) { return tok ^ (((row >> 2) & 1) * SWZ); }
 
 // Key order inside the state step. Within each block of 16 keys, the key the
 // MMAs call 8 j + 2 t + e (n-tile j of the pair, accumulator column pair of lane
@@ -125,6 +138,7 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
   constexpr int MT = V / (16 * WARPS);  // 16-row tiles of the state per warp
   constexpr int NT = K / 8;             // n-tiles of a state row
   constexpr int KK = K / 16;            // k-steps over the key channels
+  constexpr int kUtSwz = K == 128 ? 8 : 0;  // column swizzle of U~^T (rt_ut_col)
   static_assert(NTHR >= K && NTHR >= V, "one thread per key and per value channel");
   extern __shared__ __align__(16) unsigned char smem_raw[];
   using Smem = RtcSmem<K, V, Q>;
@@ -461,14 +475,14 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
         mma16816<Bf16>(u0, alo, bv[0], bv[1]);
         mma16816<Bf16>(u1, ahi, bv[2], bv[3]);
         mma16816<Bf16>(u1, alo, bv[2], bv[3]);
-        st.ut[n0 + 2 * t][g] = u0[0];
-        st.ut[n0 + 2 * t + 1][g] = u0[1];
-        st.ut[n0 + 2 * t][g + 8] = u0[2];
-        st.ut[n0 + 2 * t + 1][g + 8] = u0[3];
-        st.ut[n0 + 8 + 2 * t][g] = u1[0];
-        st.ut[n0 + 8 + 2 * t + 1][g] = u1[1];
-        st.ut[n0 + 8 + 2 * t][g + 8] = u1[2];
-        st.ut[n0 + 8 + 2 * t + 1][g + 8] = u1[3];
+        st.ut[n0 + 2 * t][rt_ut_col<kUtSwz>(n0 + 2 * t, g)] = u0[0];
+        st.ut[n0 + 2 * t + 1][rt_ut_col<kUtSwz>(n0 + 2 * t + 1, g)] = u0[1];
+        st.ut[n0 + 2 * t][rt_ut_col<kUtSwz>(n0 + 2 * t, g + 8)] = u0[2];
+        st.ut[n0 + 2 * t + 1][rt_ut_col<kUtSwz>(n0 + 2 * t + 1, g + 8)] = u0[3];
+        st.ut[n0 + 8 + 2 * t][rt_ut_col<kUtSwz>(n0 + 8 + 2 * t, g)] = u1[0];
+        st.ut[n0 + 8 + 2 * t + 1][rt_ut_col<kUtSwz>(n0 + 8 + 2 * t + 1, g)] = u1[1];
+        st.ut[n0 + 8 + 2 * t][rt_ut_col<kUtSwz>(n0 + 8 + 2 * t, g + 8)] = u1[2];
+        st.ut[n0 + 8 + 2 * t + 1][rt_ut_col<kUtSwz>(n0 + 8 + 2 * t + 1, g + 8)] = u1[3];
       }
     }
     __syncthreads();
@@ -497,8 +511,8 @@ __global__ void __launch_bounds__(128, 4) kda_recurrent_tc_kernel(const Recurren
       float u[2][4], u2[2][4], o[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        const float2 x = *reinterpret_cast<const float2*>(&st.ut[r0 + g][8 * nt + 2 * t]);
-        const float2 y = *reinterpret_cast<const float2*>(&st.ut[r0 + g + 8][8 * nt + 2 * t]);
+        const float2 x = *reinterpret_cast<const float2*>(&st.ut[r0 + g][rt_ut_col<kUtSwz>(r0 + g, 8 * nt + 2 * t)]);
+        const float2 y = *reinterpret_cast<const float2*>(&st.ut[r0 + g + 8][rt_ut_col<kUtSwz>(r0 + g + 8, 8 * nt + 2 * t)]);
         u[nt][0] = x.x; u[nt][1] = x.y; u[nt][2] = y.x; u[nt][3] = y.y;
 #pragma unroll
         for (int e = 0; e < 4; ++e) { u2[nt][e] = 0.f; o[nt][e] = 0.f; }
